@@ -1,0 +1,35 @@
+"""Builds the CPU oracle (oracle.c) into liboracle.so next to this file.
+
+Test infrastructure: plain gcc, no CUDA.  ``-ffp-contract=off`` keeps the double
+arithmetic free of fused multiply-adds so x86 and Arm hosts round identically.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCES = ["oracle.c", "oracle_core.inc", "oracle.h"]
+LIB = os.path.join(HERE, "liboracle.so")
+
+
+def needs_build() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    return any(os.path.getmtime(os.path.join(HERE, s)) > t for s in SOURCES)
+
+
+def build(force: bool = False) -> str:
+    if force or needs_build():
+        tmp = LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=gnu11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+               "-Wall", "-o", tmp, os.path.join(HERE, "oracle.c"), "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv))
