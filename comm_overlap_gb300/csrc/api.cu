@@ -1,0 +1,701 @@
+// api.cu -- the C ABI (include/domino.h): argument validation, workspace layout, TMA maps and
+// the chunk scheduler that pipelines the shard-sum of chunk k (reduction stream) against the
+// GEMMs of chunk k+1 (compute stream).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/domino.h"
+#include "kernels.h"
+
+using dm::GemmArgs;
+
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+struct domino_handle_s {
+  int device = 0;
+  int num_sms = 0;
+  cudaStream_t s_comp = nullptr;  // GEMMs, LayerNorm
+  cudaStream_t s_red = nullptr;   // shard-sums (the AllReduce stand-in)
+  cudaEvent_t ev_fork = nullptr, ev_join_c = nullptr, ev_join_r = nullptr;
+  cudaEvent_t ev_part[2] = {nullptr, nullptr};  // partial slot s written (compute -> reduce)
+  cudaEvent_t ev_red[2] = {nullptr, nullptr};   // partial slot s consumed (reduce -> compute)
+  std::vector<cudaEvent_t> ev_row;              // row chunk j of the previous layer reduced
+  bool timing = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> timing_pool;
+  int64_t launches = 0;
+};
+
+namespace {
+
+thread_local std::string t_last_error;
+
+domino_status fail(domino_status s, const std::string& msg) {
+  t_last_error = msg;
+  return s;
+}
+
+domino_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DOMINO_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define DM_CUDA(call, what)                     \
+  do {                                          \
+    const cudaError_t e_ = (call);              \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+constexpr size_t kAlign = 1024;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool gated(int act) { return act == DOMINO_ACT_SWIGLU || act == DOMINO_ACT_BILINEAR; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int64_t M, h, F, Fi, m, n, a_rows, Ri;
+  int t, p, q, act, sched, layers, nslots;
+  float eps;
+  bool gated;
+  // workspace offsets
+  size_t off_h = 0, off_ln = 0, off_dz = 0, off_hb = 0, off_part = 0, part_slot = 0, total = 0;
+};
+
+domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
+  if (!c) return fail(DOMINO_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->flags != 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->flags must be 0");
+  if (c->M < 0 || c->h <= 0 || c->ffn <= 0 || c->t < 1 || c->p < 1 || c->q < 1)
+    return fail(DOMINO_ERR_INVALID_ARG, "need M >= 0, h > 0, ffn > 0, t >= 1, p >= 1, q >= 1");
+  if (c->act < DOMINO_ACT_NONE || c->act > DOMINO_ACT_BILINEAR)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown activation");
+  if (c->sched < DOMINO_SCHED_SERIAL || c->sched > DOMINO_SCHED_INTER)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
+  if (c->M % c->p != 0) return fail(DOMINO_ERR_INVALID_ARG, "M must be divisible by p");
+  if (c->h % c->q != 0) return fail(DOMINO_ERR_INVALID_ARG, "h must be divisible by q");
+  if (c->ffn % c->t != 0) return fail(DOMINO_ERR_INVALID_ARG, "ffn must be divisible by t");
+  const int64_t Fi = c->ffn / c->t;
+  if (c->h % 8 != 0 || Fi % 8 != 0 || (c->h / c->q) % 8 != 0)
+    return fail(DOMINO_ERR_ALIGNMENT, "h, ffn/t and h/q must be multiples of 8 (16-byte rows)");
+  if (c->M > (int64_t(1) << 31) - 1 || c->h > (int64_t(1) << 20) || c->ffn > (int64_t(1) << 24))
+    return fail(DOMINO_ERR_UNSUPPORTED, "size beyond the supported range");
+  if (pass == DOMINO_PASS_STACK) {
+    if (c->layers < 1) return fail(DOMINO_ERR_INVALID_ARG, "layers must be >= 1");
+    if (!(c->ln_eps > 0.0f)) return fail(DOMINO_ERR_INVALID_ARG, "ln_eps must be > 0");
+  }
+  if (pass < DOMINO_PASS_FWD || pass > DOMINO_PASS_STACK) return fail(DOMINO_ERR_INVALID_ARG, "bad pass");
+  Plan& p = *P;
+  p.M = c->M; p.h = c->h; p.F = c->ffn; p.Fi = Fi; p.t = c->t; p.p = c->p; p.q = c->q;
+  p.act = c->act; p.sched = c->sched; p.layers = c->layers; p.eps = c->ln_eps;
+  p.gated = gated(c->act);
+  p.m = c->M / c->p;
+  p.n = c->h / c->q;
+  p.a_rows = p.gated ? 2 * p.F : p.F;
+  p.Ri = p.gated ? 2 * Fi : Fi;
+  p.nslots = (p.p * p.q >= 2) ? 2 : 1;
+  size_t off = 0;
+  if (p.M == 0) {
+    p.total = 0;
+    return DOMINO_OK;
+  }
+  if (pass == DOMINO_PASS_FWD || pass == DOMINO_PASS_STACK) {
+    p.off_h = off;
+    off = align_up(off + size_t(p.m) * p.F * 2);
+    if (pass == DOMINO_PASS_STACK) {
+      p.off_ln = off;
+      off = align_up(off + size_t(p.m) * p.h * 2);
+    }
+  } else {
+    p.off_dz = off;
+    off = align_up(off + size_t(p.m) * p.a_rows * 2);
+    p.off_hb = off;
+    off = align_up(off + size_t(p.m) * p.F * 2);
+  }
+  p.part_slot = align_up(size_t(p.t) * p.m * p.n * 4);
+  p.off_part = off;
+  off += p.part_slot * p.nslots;
+  p.total = off;
+  return DOMINO_OK;
+}
+
+domino_status check_ws(const Plan& P, void* ws, size_t bytes) {
+  if (P.total == 0) return DOMINO_OK;
+  if (!ws) return fail(DOMINO_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(DOMINO_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (bytes < P.total)
+    return fail(DOMINO_ERR_WORKSPACE, "workspace too small: need " + std::to_string(P.total) + " bytes");
+  return DOMINO_OK;
+}
+
+domino_status check_ptr(const void* p, const char* name, bool nullable = false) {
+  if (!p) {
+    if (nullable) return DOMINO_OK;
+    return fail(DOMINO_ERR_INVALID_ARG, std::string(name) + " is NULL");
+  }
+  if (!aligned16(p)) return fail(DOMINO_ERR_ALIGNMENT, std::string(name) + " is not 16-byte aligned");
+  return DOMINO_OK;
+}
+
+#define DM_TRY(expr)                   \
+  do {                                 \
+    const domino_status s_ = (expr);   \
+    if (s_ != DOMINO_OK) return s_;    \
+  } while (0)
+
+// ---- tensor maps --------------------------------------------------------------------------
+
+// 3-D bf16 map: (inner, rows, batch); row stride and batch stride in elements.
+domino_status map3(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t batch,
+                   int64_t row_stride, int64_t batch_stride, uint32_t box_inner, uint32_t box_rows) {
+  const uint64_t dims[3] = {uint64_t(inner), uint64_t(rows), uint64_t(batch)};
+  const uint64_t strides[2] = {uint64_t(row_stride) * 2,
+                               uint64_t(batch > 1 ? batch_stride : row_stride * rows) * 2};
+  const uint32_t box[3] = {box_inner, box_rows, 1};
+  std::string err;
+  if (!dm::make_map_bf16(m, base, 3, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
+  return DOMINO_OK;
+}
+
+// K-major operand: box 64 (K) x rows;  MN-major operand: box 64 (M/N) x 64 (K).
+domino_status map_k(CUtensorMap* m, const void* base, int64_t K, int64_t rows, int64_t batch,
+                    int64_t row_stride, int64_t batch_stride, uint32_t box_rows) {
+  return map3(m, base, K, rows, batch, row_stride, batch_stride, 64, box_rows);
+}
+domino_status map_mn(CUtensorMap* m, const void* base, int64_t MN, int64_t K, int64_t batch,
+                     int64_t k_stride, int64_t batch_stride) {
+  return map3(m, base, MN, K, batch, k_stride, batch_stride, 64, 64);
+}
+
+// ---- launches -----------------------------------------------------------------------------
+
+cudaEvent_t timing_event(domino_handle H) {
+  if (!H->timing_pool.empty()) {
+    cudaEvent_t e = H->timing_pool.back();
+    H->timing_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+template <class Fn>
+domino_status launch(domino_handle H, int kind, cudaStream_t st, const char* what, Fn&& fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (H->timing) {
+    a = timing_event(H);
+    b = timing_event(H);
+    DM_CUDA(cudaEventRecord(a, st), "cudaEventRecord");
+  }
+  const cudaError_t e = fn();
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  H->launches++;
+  if (H->timing) {
+    DM_CUDA(cudaEventRecord(b, st), "cudaEventRecord");
+    H->timed.push_back({kind, a, b});
+  }
+  return DOMINO_OK;
+}
+
+GemmArgs gemm_args(int variant, int batches, int64_t M, int64_t N, int64_t K, int site) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.batches = batches;
+  a.M = int32_t(M);
+  a.N = int32_t(N);
+  a.m_tiles = int32_t(cdiv(M, dm::kBM));
+  a.n_tiles = int32_t(cdiv(N, dm::gemm_out_tile_n(variant)));
+  a.k_blocks = int32_t(cdiv(K, dm::kBK));
+  a.err_site = site << 4;
+  return a;
+}
+
+domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap& ta,
+                       const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st) {
+  const int64_t tiles = int64_t(a.batches) * a.m_tiles * a.n_tiles;
+  if (tiles == 0) return DOMINO_OK;
+  const int grid = int(std::min<int64_t>(tiles, H->num_sms));
+  return launch(H, kind, st, "GEMM launch", [&] {
+    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, a, grid, st)
+                                         : dm::launch_gemm_bwd(variant, ta, tb, a, grid, st);
+  });
+}
+
+domino_status run_shard_sum(domino_handle H, const float* P, int t, int64_t rows, int64_t cols,
+                            const uint16_t* res, int64_t ld_res, uint16_t* Y, int64_t ld_y,
+                            cudaStream_t st) {
+  const int cap = H->num_sms * 4;
+  return launch(H, DOMINO_K_SHARD_SUM, st, "shard-sum launch",
+                [&] { return dm::launch_shard_sum(P, t, rows, cols, res, ld_res, Y, ld_y, cap, st); });
+}
+
+// ---- scheduling helpers ---------------------------------------------------------------------
+
+struct Streams {
+  cudaStream_t comp, red;
+  bool overlap;
+};
+
+domino_status fork(domino_handle H, const Plan& P, cudaStream_t caller, Streams* S) {
+  S->overlap = P.sched != DOMINO_SCHED_SERIAL;
+  if (!S->overlap) {
+    S->comp = S->red = caller;
+    return DOMINO_OK;
+  }
+  S->comp = H->s_comp;
+  S->red = H->s_red;
+  DM_CUDA(cudaEventRecord(H->ev_fork, caller), "cudaEventRecord(fork)");
+  DM_CUDA(cudaStreamWaitEvent(S->comp, H->ev_fork, 0), "cudaStreamWaitEvent");
+  DM_CUDA(cudaStreamWaitEvent(S->red, H->ev_fork, 0), "cudaStreamWaitEvent");
+  return DOMINO_OK;
+}
+
+domino_status join(domino_handle H, const Streams& S, cudaStream_t caller) {
+  if (!S.overlap) return DOMINO_OK;
+  DM_CUDA(cudaEventRecord(H->ev_join_c, S.comp), "cudaEventRecord(join)");
+  DM_CUDA(cudaEventRecord(H->ev_join_r, S.red), "cudaEventRecord(join)");
+  DM_CUDA(cudaStreamWaitEvent(caller, H->ev_join_c, 0), "cudaStreamWaitEvent");
+  DM_CUDA(cudaStreamWaitEvent(caller, H->ev_join_r, 0), "cudaStreamWaitEvent");
+  return DOMINO_OK;
+}
+
+// Chunk k writes partial slot k % nslots on the compute stream and is reduced on the reduction
+// stream; before chunk k + nslots reuses the slot, the compute stream waits for that reduction.
+struct SlotRing {
+  int64_t k = 0;
+};
+
+domino_status slot_acquire(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, int* slot) {
+  *slot = int(R.k % P.nslots);
+  if (S.overlap && R.k >= P.nslots)
+    DM_CUDA(cudaStreamWaitEvent(S.comp, H->ev_red[*slot], 0), "cudaStreamWaitEvent(slot)");
+  return DOMINO_OK;
+}
+
+domino_status slot_handoff(domino_handle H, const Streams& S, int slot) {
+  if (!S.overlap) return DOMINO_OK;
+  DM_CUDA(cudaEventRecord(H->ev_part[slot], S.comp), "cudaEventRecord(part)");
+  DM_CUDA(cudaStreamWaitEvent(S.red, H->ev_part[slot], 0), "cudaStreamWaitEvent(part)");
+  return DOMINO_OK;
+}
+
+domino_status slot_release(domino_handle H, const Streams& S, SlotRing& R, int slot) {
+  R.k++;
+  if (!S.overlap) return DOMINO_OK;
+  DM_CUDA(cudaEventRecord(H->ev_red[slot], S.red), "cudaEventRecord(red)");
+  return DOMINO_OK;
+}
+
+domino_status ready(domino_handle H) {
+  if (!H) return fail(DOMINO_ERR_INVALID_ARG, "handle is NULL");
+  int dev = -1;
+  DM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev != H->device) return fail(DOMINO_ERR_INVALID_ARG, "handle belongs to another device");
+  return DOMINO_OK;
+}
+
+// ---- forward of one MLP for row chunk pc: first linear into H, then the q column chunks of the
+// second linear into partial slots, each followed by its shard-sum on the reduction stream.
+domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, SlotRing& R,
+                            const uint16_t* Xc, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                            uint16_t* Hbuf, float* parts, uint16_t* save_c, const uint16_t* res_c,
+                            uint16_t* Yc, int site) {
+  CUtensorMap mapX, mapH;
+  DM_TRY(map_k(&mapX, Xc, P.h, P.m, 1, P.h, 0, 128));
+  // first linear: H = act(X_c A^T); gated: per shard, 128 output columns per tile
+  {
+    const int variant = P.gated ? dm::GV_FWD_GLU : dm::GV_FWD_ACT;
+    GemmArgs a = gemm_args(variant, P.gated ? P.t : 1, P.m, P.gated ? P.Fi : P.F, P.h, site);
+    a.act = P.act;
+    a.out0 = Hbuf;
+    a.ld0 = P.F;
+    a.bs0 = P.gated ? P.Fi : 0;
+    a.out1 = save_c;
+    a.ld1 = P.a_rows;
+    a.bs1 = P.gated ? 2 * P.Fi : 0;
+    a.off1 = P.Fi;
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD1, variant, mapX, mapA, a, S.comp));
+  }
+  DM_TRY(map_k(&mapH, Hbuf, P.Fi, P.m, P.t, P.F, P.Fi, 128));
+  for (int qc = 0; qc < P.q; ++qc) {
+    int slot;
+    DM_TRY(slot_acquire(H, P, S, R, &slot));
+    float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
+    GemmArgs a = gemm_args(dm::GV_FWD_PARTIAL, P.t, P.m, P.n, P.Fi, site + 1);
+    a.a_bmul = 1;
+    a.b_row_off = int32_t(qc * P.n);
+    a.b_bmul = 1;
+    a.out0 = part;
+    a.ld0 = P.n;
+    a.bs0 = P.m * P.n;
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp));
+    DM_TRY(slot_handoff(H, S, slot));
+    DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, res_c ? res_c + qc * P.n : nullptr, P.h,
+                         Yc + qc * P.n, P.h, S.red));
+    DM_TRY(slot_release(H, S, R, slot));
+  }
+  return DOMINO_OK;
+}
+
+domino_status weight_maps_fwd(const Plan& P, const uint16_t* A, const uint16_t* B, CUtensorMap* mapA,
+                              CUtensorMap* mapB) {
+  if (P.gated) {
+    // A shard i = [gate_i ; up_i], each F_i x h: 4-D view (h, F_i, 2, t)
+    const uint64_t dims[4] = {uint64_t(P.h), uint64_t(P.Fi), 2, uint64_t(P.t)};
+    const uint64_t strides[3] = {uint64_t(P.h) * 2, uint64_t(P.Fi * P.h) * 2, uint64_t(2 * P.Fi * P.h) * 2};
+    const uint32_t box[4] = {64, 128, 1, 1};
+    std::string err;
+    if (!dm::make_map_bf16(mapA, A, 4, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
+  } else {
+    DM_TRY(map_k(mapA, A, P.h, P.F, 1, P.h, 0, 256));
+  }
+  // B shard i is h x F_i: K-major over F_i, rows h, batch t
+  DM_TRY(map_k(mapB, B, P.Fi, P.h, P.t, P.Fi, P.h * P.Fi, 256));
+  return DOMINO_OK;
+}
+
+}  // namespace
+
+// =============================================================================================
+
+extern "C" {
+
+const char* domino_status_string(domino_status s) {
+  switch (s) {
+    case DOMINO_OK: return "DOMINO_OK";
+    case DOMINO_ERR_INVALID_ARG: return "DOMINO_ERR_INVALID_ARG";
+    case DOMINO_ERR_UNSUPPORTED: return "DOMINO_ERR_UNSUPPORTED";
+    case DOMINO_ERR_ALIGNMENT: return "DOMINO_ERR_ALIGNMENT";
+    case DOMINO_ERR_WORKSPACE: return "DOMINO_ERR_WORKSPACE";
+    case DOMINO_ERR_CUDA: return "DOMINO_ERR_CUDA";
+    case DOMINO_ERR_TIMEOUT: return "DOMINO_ERR_TIMEOUT";
+    case DOMINO_ERR_DEVICE: return "DOMINO_ERR_DEVICE";
+  }
+  return "DOMINO_ERR_UNKNOWN";
+}
+
+const char* domino_last_error(void) { return t_last_error.c_str(); }
+
+domino_status domino_create(domino_handle* out) {
+  if (!out) return fail(DOMINO_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  DM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  DM_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute");
+  DM_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute");
+  DM_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(DOMINO_ERR_DEVICE, "this build targets sm_103a; device is sm_" + std::to_string(major) +
+                                       std::to_string(minor));
+  std::string err;
+  if (!dm::tma_encoder_ready(&err)) return fail(DOMINO_ERR_DEVICE, err);
+  domino_handle H = new domino_handle_s();
+  H->device = dev;
+  H->num_sms = sms;
+  cudaError_t e = cudaStreamCreateWithFlags(&H->s_comp, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&H->s_red, cudaStreamNonBlocking);
+  cudaEvent_t* evs[] = {&H->ev_fork, &H->ev_join_c, &H->ev_join_r, &H->ev_part[0],
+                        &H->ev_part[1], &H->ev_red[0], &H->ev_red[1]};
+  for (cudaEvent_t* ev : evs)
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    domino_destroy(H);
+    return cuda_fail(e, "domino_create");
+  }
+  *out = H;
+  return DOMINO_OK;
+}
+
+domino_status domino_destroy(domino_handle H) {
+  if (!H) return DOMINO_OK;
+  if (H->s_comp) cudaStreamSynchronize(H->s_comp);
+  if (H->s_red) cudaStreamSynchronize(H->s_red);
+  for (auto& t : H->timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto e : H->timing_pool) cudaEventDestroy(e);
+  for (auto e : H->ev_row) cudaEventDestroy(e);
+  cudaEvent_t evs[] = {H->ev_fork, H->ev_join_c, H->ev_join_r, H->ev_part[0],
+                       H->ev_part[1], H->ev_red[0], H->ev_red[1]};
+  for (cudaEvent_t e : evs)
+    if (e) cudaEventDestroy(e);
+  if (H->s_comp) cudaStreamDestroy(H->s_comp);
+  if (H->s_red) cudaStreamDestroy(H->s_red);
+  delete H;
+  return DOMINO_OK;
+}
+
+domino_status domino_workspace_size(const domino_cfg* cfg, int32_t pass, size_t* bytes) {
+  if (!bytes) return fail(DOMINO_ERR_INVALID_ARG, "bytes is NULL");
+  Plan P;
+  DM_TRY(make_plan(cfg, pass, &P));
+  *bytes = P.total;
+  return DOMINO_OK;
+}
+
+domino_status domino_mlp_fwd(domino_handle H, const domino_cfg* cfg, const uint16_t* X,
+                             const uint16_t* A, const uint16_t* B, uint16_t* Y, uint16_t* act_save,
+                             void* ws, size_t ws_bytes, void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_FWD, &P));
+  DM_TRY(check_ptr(X, "X"));
+  DM_TRY(check_ptr(A, "A"));
+  DM_TRY(check_ptr(B, "B"));
+  DM_TRY(check_ptr(Y, "Y"));
+  DM_TRY(check_ptr(act_save, "act_save", true));
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  CUtensorMap mapA, mapB;
+  DM_TRY(weight_maps_fwd(P, A, B, &mapA, &mapB));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* Hbuf = reinterpret_cast<uint16_t*>(w + P.off_h);
+  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  Streams S;
+  DM_TRY(fork(H, P, caller, &S));
+  SlotRing R;
+  for (int pc = 0; pc < P.p; ++pc) {
+    const int64_t r0 = pc * P.m;
+    DM_TRY(mlp_chunk_fwd(H, P, S, R, X + r0 * P.h, mapA, mapB, Hbuf, parts,
+                         act_save ? act_save + r0 * P.a_rows : nullptr, nullptr, Y + r0 * P.h, 1));
+  }
+  return join(H, S, caller);
+}
+
+domino_status domino_stack_fwd(domino_handle H, const domino_cfg* cfg, const uint16_t* Z_in,
+                               const uint16_t* A, const uint16_t* B, uint16_t* Z_out, void* ws,
+                               size_t ws_bytes, void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_STACK, &P));
+  DM_TRY(check_ptr(Z_in, "Z_in"));
+  DM_TRY(check_ptr(A, "A"));
+  DM_TRY(check_ptr(B, "B"));
+  DM_TRY(check_ptr(Z_out, "Z_out"));
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  while (int(H->ev_row.size()) < P.p) {
+    cudaEvent_t e;
+    DM_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate");
+    H->ev_row.push_back(e);
+  }
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* Hbuf = reinterpret_cast<uint16_t*>(w + P.off_h);
+  uint16_t* lnbuf = reinterpret_cast<uint16_t*>(w + P.off_ln);
+  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  Streams S;
+  DM_TRY(fork(H, P, caller, &S));
+  SlotRing R;
+  const int64_t a_layer = P.a_rows * P.h, b_layer = P.h * P.F;
+  for (int l = 0; l < P.layers; ++l) {
+    CUtensorMap mapA, mapB;
+    DM_TRY(weight_maps_fwd(P, A + l * a_layer, B + l * b_layer, &mapA, &mapB));
+    const uint16_t* src = (l == 0) ? Z_in : Z_out;
+    for (int pc = 0; pc < P.p; ++pc) {
+      const int64_t r0 = pc * P.m;
+      if (S.overlap && l > 0) {
+        if (P.sched == DOMINO_SCHED_INTER) {
+          // row chunk pc of this layer needs only row chunk pc of the previous layer
+          DM_CUDA(cudaStreamWaitEvent(S.comp, H->ev_row[pc], 0), "cudaStreamWaitEvent(row)");
+        } else if (pc == 0) {
+          // INTRA: the previous layer ends with a synchronisation of all its row chunks
+          for (int j = 0; j < P.p; ++j)
+            DM_CUDA(cudaStreamWaitEvent(S.comp, H->ev_row[j], 0), "cudaStreamWaitEvent(row)");
+        }
+      }
+      DM_TRY(launch(H, DOMINO_K_LAYERNORM, S.comp, "LayerNorm launch", [&] {
+        return dm::launch_layernorm(src + r0 * P.h, P.m, P.h, P.eps, lnbuf, S.comp);
+      }));
+      DM_TRY(mlp_chunk_fwd(H, P, S, R, lnbuf, mapA, mapB, Hbuf, parts, nullptr, src + r0 * P.h,
+                           Z_out + r0 * P.h, 2));
+      if (S.overlap)
+        DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
+    }
+  }
+  return join(H, S, caller);
+}
+
+domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint16_t* X,
+                             const uint16_t* A, const uint16_t* B, const uint16_t* act_save,
+                             const uint16_t* gY, uint16_t* gX, float* gA, float* gB, void* ws,
+                             size_t ws_bytes, void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_BWD, &P));
+  DM_TRY(check_ptr(X, "X"));
+  DM_TRY(check_ptr(A, "A"));
+  DM_TRY(check_ptr(B, "B"));
+  DM_TRY(check_ptr(act_save, "act_save"));
+  DM_TRY(check_ptr(gY, "gY"));
+  DM_TRY(check_ptr(gX, "gX"));
+  DM_TRY(check_ptr(gA, "gA"));
+  DM_TRY(check_ptr(gB, "gB"));
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* dZ = reinterpret_cast<uint16_t*>(w + P.off_dz);
+  uint16_t* Hb = reinterpret_cast<uint16_t*>(w + P.off_hb);
+  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  // weight maps: B_i (h x F_i) read MN-major (N = F_i, K = h); A_i (R_i x h) read MN-major
+  // (N = h, K = R_i)
+  CUtensorMap mapBmn, mapAmn, mapDZk, mapDZmn, mapHmn;
+  DM_TRY(map_mn(&mapBmn, B, P.Fi, P.h, P.t, P.Fi, P.h * P.Fi));
+  DM_TRY(map_mn(&mapAmn, A, P.h, P.Ri, P.t, P.h, P.Ri * P.h));
+  DM_TRY(map_k(&mapDZk, dZ, P.Ri, P.m, P.t, P.a_rows, P.Ri, 128));
+  DM_TRY(map_mn(&mapDZmn, dZ, P.Ri, P.m, P.t, P.a_rows, P.Ri));
+  DM_TRY(map_mn(&mapHmn, Hb, P.Fi, P.m, P.t, P.F, P.Fi));
+  Streams S;
+  DM_TRY(fork(H, P, caller, &S));
+  SlotRing R;
+  // row chunks in reverse order, as the backward pass runs the forward schedule backwards
+  for (int pc = P.p - 1; pc >= 0; --pc) {
+    const int64_t r0 = pc * P.m;
+    CUtensorMap mapGYk, mapGYmn, mapXmn;
+    DM_TRY(map_k(&mapGYk, gY + r0 * P.h, P.h, P.m, 1, P.h, 0, 128));
+    DM_TRY(map_mn(&mapGYmn, gY + r0 * P.h, P.h, P.m, 1, P.h, 0));
+    DM_TRY(map_mn(&mapXmn, X + r0 * P.h, P.h, P.m, 1, P.h, 0));
+    // dH_i = gY_c . B_i, with the activation backward in the epilogue -> dZ (dG|dU), H
+    {
+      const int variant = P.gated ? dm::GV_BWD_GLU : dm::GV_BWD_ACT;
+      GemmArgs a = gemm_args(variant, P.t, P.m, P.Fi, P.h, 3);
+      a.act = P.act;
+      a.b_bmul = 1;
+      a.in0 = act_save + r0 * P.a_rows;
+      a.ldi = P.a_rows;
+      a.bsi = P.Ri;
+      a.offi = P.Fi;
+      a.out0 = dZ;
+      a.ld0 = P.a_rows;
+      a.bs0 = P.Ri;
+      a.off0 = P.Fi;
+      a.out1 = Hb;
+      a.ld1 = P.F;
+      a.bs1 = P.Fi;
+      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_H, variant, mapGYk, mapBmn, a, S.comp));
+    }
+    // gB_i += gY_c^T . H_i   (D = h x F_i, K = tokens of the chunk)
+    {
+      GemmArgs a = gemm_args(dm::GV_WGRAD, P.t, P.h, P.Fi, P.m, 4);
+      a.b_bmul = 1;
+      a.out0 = gB;
+      a.ld0 = P.Fi;
+      a.bs0 = P.h * P.Fi;
+      DM_TRY(run_gemm(H, DOMINO_K_GEMM_WGRAD_B, dm::GV_WGRAD, mapGYmn, mapHmn, a, S.comp));
+    }
+    // gX partials: P_i = dZ_i . A_i (D = m x n per column chunk), reduced on the reduction stream
+    for (int qc = 0; qc < P.q; ++qc) {
+      int slot;
+      DM_TRY(slot_acquire(H, P, S, R, &slot));
+      float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
+      GemmArgs a = gemm_args(dm::GV_BWD_PARTIAL, P.t, P.m, P.n, P.Ri, 5);
+      a.a_bmul = 1;
+      a.b_row_off = int32_t(qc * P.n);
+      a.b_bmul = 1;
+      a.out0 = part;
+      a.ld0 = P.n;
+      a.bs0 = P.m * P.n;
+      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, mapDZk, mapAmn, a, S.comp));
+      DM_TRY(slot_handoff(H, S, slot));
+      DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, nullptr, 0, gX + r0 * P.h + qc * P.n, P.h, S.red));
+      DM_TRY(slot_release(H, S, R, slot));
+    }
+    // gA_i += dZ_i^T . X_c (D = R_i x h, K = tokens), overlapping the gX reduction
+    {
+      GemmArgs a = gemm_args(dm::GV_WGRAD, P.t, P.Ri, P.h, P.m, 6);
+      a.a_bmul = 1;
+      a.out0 = gA;
+      a.ld0 = P.h;
+      a.bs0 = P.Ri * P.h;
+      DM_TRY(run_gemm(H, DOMINO_K_GEMM_WGRAD_A, dm::GV_WGRAD, mapDZmn, mapXmn, a, S.comp));
+    }
+  }
+  return join(H, S, caller);
+}
+
+domino_status domino_shard_sum(const float* Pp, int32_t t, int64_t rows, int64_t cols,
+                               const uint16_t* residual, int64_t ld_res, uint16_t* Y, int64_t ld_y,
+                               void* stream) {
+  if (t < 1 || rows < 0 || cols < 0) return fail(DOMINO_ERR_INVALID_ARG, "need t >= 1, rows, cols >= 0");
+  if (cols % 8 != 0) return fail(DOMINO_ERR_ALIGNMENT, "cols must be a multiple of 8");
+  if (rows * (cols / 8) >= (int64_t(1) << 32)) return fail(DOMINO_ERR_UNSUPPORTED, "too many elements");
+  if (ld_y < cols || (ld_y % 8) != 0) return fail(DOMINO_ERR_ALIGNMENT, "ld_y must be >= cols and a multiple of 8");
+  if (residual && (ld_res < cols || (ld_res % 8) != 0))
+    return fail(DOMINO_ERR_ALIGNMENT, "ld_res must be >= cols and a multiple of 8");
+  if (rows == 0 || cols == 0) return DOMINO_OK;
+  DM_TRY(check_ptr(Pp, "P"));
+  DM_TRY(check_ptr(Y, "Y"));
+  DM_TRY(check_ptr(residual, "residual", true));
+  int dev = 0, sms = 0;
+  DM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  DM_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+  DM_CUDA(dm::launch_shard_sum(Pp, t, rows, cols, residual, ld_res, Y, ld_y, sms * 4,
+                               static_cast<cudaStream_t>(stream)),
+          "shard-sum launch");
+  return DOMINO_OK;
+}
+
+domino_status domino_device_status(domino_handle H, domino_status* out, int32_t* site) {
+  DM_TRY(ready(H));
+  if (!out) return fail(DOMINO_ERR_INVALID_ARG, "out is NULL");
+  DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  int c1 = 0, c2 = 0;
+  DM_CUDA(dm::take_gemm_fwd_error(&c1), "reading the device error word");
+  DM_CUDA(dm::take_gemm_bwd_error(&c2), "reading the device error word");
+  const int code = c1 ? c1 : c2;
+  *out = code ? DOMINO_ERR_TIMEOUT : DOMINO_OK;
+  if (site) *site = code;
+  return DOMINO_OK;
+}
+
+domino_status domino_timing_enable(domino_handle H, int32_t enable) {
+  if (!H) return fail(DOMINO_ERR_INVALID_ARG, "handle is NULL");
+  H->timing = enable != 0;
+  return DOMINO_OK;
+}
+
+domino_status domino_timing_reset(domino_handle H) {
+  if (!H) return fail(DOMINO_ERR_INVALID_ARG, "handle is NULL");
+  for (auto& t : H->timed) {
+    H->timing_pool.push_back(t.a);
+    H->timing_pool.push_back(t.b);
+  }
+  H->timed.clear();
+  return DOMINO_OK;
+}
+
+domino_status domino_timing_read(domino_handle H, int32_t kind, int64_t* launches, double* total_ms) {
+  if (!H || !launches || !total_ms) return fail(DOMINO_ERR_INVALID_ARG, "NULL argument");
+  if (kind < 0 || kind >= DOMINO_K_COUNT) return fail(DOMINO_ERR_INVALID_ARG, "bad kernel kind");
+  int64_t n = 0;
+  double ms = 0.0;
+  for (auto& t : H->timed) {
+    if (t.kind != kind) continue;
+    DM_CUDA(cudaEventSynchronize(t.b), "cudaEventSynchronize");
+    float f = 0.0f;
+    DM_CUDA(cudaEventElapsedTime(&f, t.a, t.b), "cudaEventElapsedTime");
+    ms += f;
+    ++n;
+  }
+  *launches = n;
+  *total_ms = ms;
+  return DOMINO_OK;
+}
+
+domino_status domino_launch_count(domino_handle H, int64_t* launches) {
+  if (!H || !launches) return fail(DOMINO_ERR_INVALID_ARG, "NULL argument");
+  *launches = H->launches;
+  return DOMINO_OK;
+}
+
+}  // extern "C"

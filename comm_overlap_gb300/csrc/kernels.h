@@ -1,0 +1,83 @@
+// kernels.h -- host-side interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace dm {
+
+// Activation codes (same values as domino_act).
+enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2, ACT_SWIGLU = 3, ACT_BILINEAR = 4 };
+
+// GEMM tile shape: one CTA computes a 128 x 256 fp32 accumulator in TMEM per tile; the K loop
+// moves 64 bf16 (128 bytes, one swizzle atom) per pipeline stage.
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4, kThreads = 192;
+
+// Epilogues (what happens to the fp32 accumulator tile D).
+enum GemmEpi : int {
+  EPI_ACT_BF16 = 0,  // out0 = bf16(act(D));  out1 (nullable) = bf16(D)
+  EPI_GLU_BF16 = 1,  // D = [gate(128) | up(128)]: out0 = bf16(glu); out1 (nullable): gate at +0, up at +off1
+  EPI_F32_STORE = 2, // out0 = D (fp32)
+  EPI_F32_ACCUM = 3, // out0 += D (fp32)
+  EPI_ACT_BWD = 4,   // in0 = Z: out0 = bf16(D * act'(Z)); out1 = bf16(act(Z))
+  EPI_GLU_BWD = 5,   // in0: G at +0, U at +offi: out0: dG at +0, dU at +off0; out1 = bf16(glu(G, U))
+};
+
+// The kernel instantiations the library uses.  A/B operand majorness: K = K-major
+// (contiguous along the reduction dim), MN = contiguous along rows/cols of D.
+enum GemmVariant : int {
+  GV_FWD_ACT = 0,     // first linear, non-gated:     EPI_ACT_BF16,  A K, B K
+  GV_FWD_GLU = 1,     // first linear, gated:         EPI_GLU_BF16,  A K, B K (gate/up 4-D map)
+  GV_FWD_PARTIAL = 2, // second linear -> partials:   EPI_F32_STORE, A K, B K
+  GV_BWD_ACT = 3,     // dH with act backward:        EPI_ACT_BWD,   A K, B MN
+  GV_BWD_GLU = 4,     // dH with gated backward:      EPI_GLU_BWD,   A K, B MN
+  GV_BWD_PARTIAL = 5, // dX partials:                 EPI_F32_STORE, A K, B MN
+  GV_WGRAD = 6,       // weight gradients (+=):       EPI_F32_ACCUM, A MN, B MN
+  GV_COUNT = 7
+};
+
+// Per-launch GEMM description.  D[g] (M x N per batch g) = A_op[g] . B_op[g]^T.
+// TMA coordinates: K-major operand (k, row + row_off, g * bmul); MN-major (row + row_off, k, g * bmul);
+// the gated first-linear B operand uses a 4-D map (k, row, half, g).
+struct GemmArgs {
+  int32_t batches, m_tiles, n_tiles, k_blocks;
+  int32_t M, N;
+  int32_t a_row_off, a_bmul;
+  int32_t b_row_off, b_bmul;
+  int32_t act;
+  int32_t err_site;
+  void* out0;
+  int64_t ld0, bs0, off0;
+  void* out1;
+  int64_t ld1, bs1, off1;
+  const void* in0;
+  int64_t ldi, bsi, offi;
+};
+
+int gemm_out_tile_n(int variant);  // 128 for GV_FWD_GLU, else 256
+size_t gemm_smem_bytes();
+
+cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
+                            const GemmArgs& args, int grid, cudaStream_t st);
+cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
+                            const GemmArgs& args, int grid, cudaStream_t st);
+// Reads and clears the device error word of the GEMM kernels in each translation unit.
+cudaError_t take_gemm_fwd_error(int* code);
+cudaError_t take_gemm_bwd_error(int* code);
+
+// Shard-sum (AllReduce stand-in) and LayerNorm.
+cudaError_t launch_shard_sum(const float* P, int t, int64_t rows, int64_t cols,
+                             const uint16_t* res, int64_t ld_res, uint16_t* Y, int64_t ld_y,
+                             int grid_cap, cudaStream_t st);
+cudaError_t launch_layernorm(const uint16_t* Z, int64_t rows, int64_t h, float eps, uint16_t* out,
+                             cudaStream_t st);
+
+// Tensor maps (bf16, 128-byte swizzle, zero fill out of bounds).  dims[0] is innermost;
+// strides_bytes[i] is the stride of dims[i+1].
+bool tma_encoder_ready(std::string* err);
+bool make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box, std::string* err);
+
+}  // namespace dm

@@ -1,0 +1,181 @@
+"""Thin Python binding of libdomino.so (include/domino.h), same names as the C ABI.
+
+Argument marshalling only: tensors are passed as device pointers
+(``Tensor.data_ptr()``), streams as ``cudaStream_t`` handles; every step of the
+computation runs in the library's CUDA kernels.  If the library is missing the
+calls raise ``DominoError`` -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdomino.so")
+
+DOMINO_OK = 0
+STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTED", 3: "DOMINO_ERR_ALIGNMENT",
+          4: "DOMINO_ERR_WORKSPACE", 5: "DOMINO_ERR_CUDA", 6: "DOMINO_ERR_TIMEOUT", 7: "DOMINO_ERR_DEVICE"}
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SWIGLU, ACT_BILINEAR = 0, 1, 2, 3, 4
+SCHED_SERIAL, SCHED_INTRA, SCHED_INTER = 0, 1, 2
+PASS_FWD, PASS_BWD, PASS_STACK = 0, 1, 2
+(K_GEMM_FWD1, K_GEMM_FWD2, K_SHARD_SUM, K_LAYERNORM, K_GEMM_DGRAD_H, K_GEMM_WGRAD_B, K_GEMM_DGRAD_X,
+ K_GEMM_WGRAD_A) = range(8)
+KERNEL_NAMES = ["gemm_fwd1", "gemm_fwd2", "shard_sum", "layernorm", "gemm_dgrad_h", "gemm_wgrad_b",
+                "gemm_dgrad_x", "gemm_wgrad_a"]
+
+
+class DominoError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class domino_cfg(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("h", ctypes.c_int64), ("ffn", ctypes.c_int64), ("t", ctypes.c_int32),
+                ("p", ctypes.c_int32), ("q", ctypes.c_int32), ("act", ctypes.c_int32), ("sched", ctypes.c_int32),
+                ("layers", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("flags", ctypes.c_int32)]
+
+
+def make_cfg(M, h, ffn, t, p=1, q=1, act=ACT_GELU, sched=SCHED_INTRA, layers=1, ln_eps=1e-5, flags=0) -> domino_cfg:
+    return domino_cfg(M, h, ffn, t, p, q, act, sched, layers, ln_eps, flags)
+
+
+_lib = None
+_lock = threading.Lock()
+_P = ctypes.c_void_p
+_S = ctypes.c_int32
+
+_SIGS = {
+    "domino_create": [ctypes.POINTER(ctypes.c_void_p)],
+    "domino_destroy": [_P],
+    "domino_workspace_size": [ctypes.POINTER(domino_cfg), ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
+    "domino_mlp_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "domino_mlp_bwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "domino_stack_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "domino_shard_sum": [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int64, _P,
+                         ctypes.c_int64, _P],
+    "domino_device_status": [_P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+    "domino_timing_enable": [_P, ctypes.c_int32],
+    "domino_timing_reset": [_P],
+    "domino_timing_read": [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)],
+    "domino_launch_count": [_P, ctypes.POINTER(ctypes.c_int64)],
+    "domino_status_string": [ctypes.c_int32],
+    "domino_last_error": [],
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises DominoError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise DominoError(5, f"{LIB_PATH} is missing: build it with `python -m comm_overlap_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, args in _SIGS.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = ctypes.c_char_p if name in ("domino_status_string", "domino_last_error") else _S
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != DOMINO_OK:
+        raise DominoError(status, lib().domino_last_error().decode())
+
+
+def _ptr(x):
+    """Device pointer of a tensor (or an int address, or None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def domino_status_string(status: int) -> str:
+    return lib().domino_status_string(status).decode()
+
+
+def domino_last_error() -> str:
+    return lib().domino_last_error().decode()
+
+
+def domino_create() -> int:
+    h = ctypes.c_void_p()
+    _check(lib().domino_create(ctypes.byref(h)))
+    return h.value
+
+
+def domino_destroy(handle: int) -> None:
+    _check(lib().domino_destroy(handle))
+
+
+def domino_workspace_size(cfg: domino_cfg, pass_: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().domino_workspace_size(ctypes.byref(cfg), pass_, ctypes.byref(n)))
+    return n.value
+
+
+def domino_mlp_fwd(handle, cfg, X, A, B, Y, act_save, workspace, workspace_bytes=None, stream=None) -> None:
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None and workspace is not None else (
+        workspace_bytes or 0)
+    _check(lib().domino_mlp_fwd(handle, ctypes.byref(cfg), _ptr(X), _ptr(A), _ptr(B), _ptr(Y), _ptr(act_save),
+                                _ptr(workspace), wb, _stream(stream)))
+
+
+def domino_mlp_bwd(handle, cfg, X, A, B, act_save, gY, gX, gA, gB, workspace, workspace_bytes=None,
+                   stream=None) -> None:
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None and workspace is not None else (
+        workspace_bytes or 0)
+    _check(lib().domino_mlp_bwd(handle, ctypes.byref(cfg), _ptr(X), _ptr(A), _ptr(B), _ptr(act_save), _ptr(gY),
+                                _ptr(gX), _ptr(gA), _ptr(gB), _ptr(workspace), wb, _stream(stream)))
+
+
+def domino_stack_fwd(handle, cfg, Z_in, A, B, Z_out, workspace, workspace_bytes=None, stream=None) -> None:
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None and workspace is not None else (
+        workspace_bytes or 0)
+    _check(lib().domino_stack_fwd(handle, ctypes.byref(cfg), _ptr(Z_in), _ptr(A), _ptr(B), _ptr(Z_out),
+                                  _ptr(workspace), wb, _stream(stream)))
+
+
+def domino_shard_sum(P, t, rows, cols, residual, ld_res, Y, ld_y, stream=None) -> None:
+    _check(lib().domino_shard_sum(_ptr(P), t, rows, cols, _ptr(residual), ld_res, _ptr(Y), ld_y, _stream(stream)))
+
+
+def domino_device_status(handle) -> tuple[int, int]:
+    st, site = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().domino_device_status(handle, ctypes.byref(st), ctypes.byref(site)))
+    return st.value, site.value
+
+
+def domino_timing_enable(handle, enable: bool) -> None:
+    _check(lib().domino_timing_enable(handle, int(bool(enable))))
+
+
+def domino_timing_reset(handle) -> None:
+    _check(lib().domino_timing_reset(handle))
+
+
+def domino_timing_read(handle, kind: int) -> tuple[int, float]:
+    n, ms = ctypes.c_int64(), ctypes.c_double()
+    _check(lib().domino_timing_read(handle, kind, ctypes.byref(n), ctypes.byref(ms)))
+    return n.value, ms.value
+
+
+def domino_launch_count(handle) -> int:
+    n = ctypes.c_int64()
+    _check(lib().domino_launch_count(handle, ctypes.byref(n)))
+    return n.value

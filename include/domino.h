@@ -1,0 +1,185 @@
+/*
+ * domino.h -- C ABI of the GB300 (sm_103a) chunked tensor-parallel MLP.
+ *
+ * The operation is the tensor-parallel Transformer MLP written as XAB=Y and followed by
+ * AllReduce(Y) ("DeepSpeed-Domino 深度解析", section "TP 的数据依赖：通信为何难以隐藏"):
+ *
+ *     Y = sum_{i<t} act(X . A_i^T) . B_i^T
+ *
+ * with the first linear column-parallel (shard i owns output features of A) and the second
+ * row-parallel (shard i produces a partial sum P_i that the AllReduce adds up), as in the
+ * nxmr.cn DP/TP/PP article, §3.1 "TP的切分方式与计算模式".  On one GPU the t shards are
+ * emulated in device memory: each shard's fp32 partial is written to its own buffer and an
+ * on-device shard-sum kernel stands in for the AllReduce.  The work is split as Domino does
+ * ("Domino 核心设计：三种张量切分策略"): p row chunks of X along the token (batch)
+ * dimension, q column chunks of B along its last (output) dimension, or both (2D).  The
+ * reduction of chunk k runs on a second CUDA stream while the GEMMs of chunk k+1 run.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor arguments are DEVICE pointers owned by the caller.  bf16 tensors are passed
+ *    as uint16_t bit patterns; fp32 tensors as float.  Layouts are row-major, nn.Linear
+ *    [out, in] orientation:
+ *        X, gX, gY, Y, Z : M x h
+ *        A : t contiguous shards; shard i is F_i x h, or 2F_i x h for gated activations
+ *            (F_i gate rows followed by F_i up rows).  F_i = ffn / t.
+ *        B : t contiguous shards; shard i is h x F_i.
+ *        gA, gB : fp32, same shapes as A and B.
+ *  - Every pointer must be 16-byte aligned; h, F_i and h/q must be multiples of 8.
+ *  - The library allocates no device memory.  Scratch space is the caller's workspace,
+ *    whose size domino_workspace_size() returns; it must be 256-byte aligned.
+ *  - Calls are asynchronous with respect to the host: work is ordered after prior work on
+ *    `stream` (a cudaStream_t; NULL is the legacy default stream) and, on return, every
+ *    launch is enqueued and joined back into `stream`.  Inputs must stay valid and outputs
+ *    untouched until `stream` reaches that point.
+ *  - Arguments are validated before anything is launched; a failed validation returns an
+ *    error and launches nothing.  No C++ exception crosses this boundary.
+ *  - A handle is bound to the device current at domino_create() and is not thread-safe:
+ *    use one handle per host thread (or serialise calls).
+ *  - Device-side waits are bounded in time; a wait that expires makes the kernel record an
+ *    error word and return early.  domino_device_status() reads and clears that word.
+ */
+#ifndef DOMINO_H
+#define DOMINO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DOMINO_API __attribute__((visibility("default")))
+#else
+#define DOMINO_API
+#endif
+
+typedef enum {
+  DOMINO_OK = 0,
+  DOMINO_ERR_INVALID_ARG = 1, /* null pointer, bad size, divisibility violated */
+  DOMINO_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  DOMINO_ERR_ALIGNMENT = 3,   /* pointer or leading dimension not 16-byte aligned */
+  DOMINO_ERR_WORKSPACE = 4,   /* workspace missing, misaligned or too small */
+  DOMINO_ERR_CUDA = 5,        /* a CUDA runtime call failed; see domino_last_error() */
+  DOMINO_ERR_TIMEOUT = 6,     /* a device-side wait expired (domino_device_status) */
+  DOMINO_ERR_DEVICE = 7       /* current GPU is not sm_103 or lacks a needed driver entry */
+} domino_status;
+
+typedef enum {
+  DOMINO_ACT_NONE = 0,
+  DOMINO_ACT_RELU = 1,
+  DOMINO_ACT_GELU = 2,     /* exact form: x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
+  DOMINO_ACT_SWIGLU = 3,   /* gated: silu(gate) * up, silu(g) = g / (1 + exp(-g)) */
+  DOMINO_ACT_BILINEAR = 4  /* gated: gate * up */
+} domino_act;
+
+/* How chunks are pipelined ("Domino 核心设计" and "实现与优化", figure 9):
+ *  SERIAL: every kernel on the caller's stream, no overlap (the naive TP order).
+ *  INTRA : reduction of chunk k on a side stream, overlapping the GEMMs of chunk k+1.
+ *  INTER : as INTRA; in the layer stack, row chunk j of layer l+1 starts as soon as the
+ *          reductions of row chunk j of layer l finish (no wait for the whole layer). */
+typedef enum { DOMINO_SCHED_SERIAL = 0, DOMINO_SCHED_INTRA = 1, DOMINO_SCHED_INTER = 2 } domino_sched;
+
+typedef enum { DOMINO_PASS_FWD = 0, DOMINO_PASS_BWD = 1, DOMINO_PASS_STACK = 2 } domino_pass;
+
+typedef struct {
+  int64_t M;      /* tokens (batch x sequence); M % p == 0 */
+  int64_t h;      /* hidden size */
+  int64_t ffn;    /* F: ffn width (per branch for gated activations); F % t == 0 */
+  int32_t t;      /* weight shards (emulated tensor-parallel ranks), >= 1 */
+  int32_t p;      /* row chunks of X (token dimension), >= 1 */
+  int32_t q;      /* column chunks of B's output dimension h, >= 1; h % q == 0 */
+  int32_t act;    /* domino_act */
+  int32_t sched;  /* domino_sched */
+  int32_t layers; /* domino_stack_fwd only: number of layers (>= 1) */
+  float ln_eps;   /* domino_stack_fwd only: LayerNorm epsilon (> 0) */
+  int32_t flags;  /* reserved, must be 0 */
+} domino_cfg;
+
+typedef struct domino_handle_s* domino_handle;
+
+/* Creates a handle on the current device: two internal streams (compute and reduction,
+ * both non-blocking) and a pool of events.  Fails with DOMINO_ERR_DEVICE on a GPU other
+ * than compute capability 10.3.  *out is set to NULL on failure. */
+DOMINO_API domino_status domino_create(domino_handle* out);
+
+/* Destroys the handle after synchronising its internal streams.  NULL is accepted. */
+DOMINO_API domino_status domino_destroy(domino_handle handle);
+
+/* Bytes of workspace that `pass` needs for `cfg` (0 is possible).  Host-only. */
+DOMINO_API domino_status domino_workspace_size(const domino_cfg* cfg, int32_t pass, size_t* bytes);
+
+/* Forward of one MLP: Y = sum_i act(X . A_i^T) . B_i^T, bf16 output rounded once from the
+ * fp32 shard-sum (shard order 0..t-1).  act_save (nullable) receives what the backward
+ * needs: the bf16 first-linear output, M x F for non-gated activations, or M x 2F laid out
+ * per shard as [gate_i | up_i] (columns i*2F_i .. (i+1)*2F_i) for gated ones.
+ * Row-split results are bit-identical to p = 1. */
+DOMINO_API domino_status domino_mlp_fwd(domino_handle handle, const domino_cfg* cfg, const uint16_t* X,
+                             const uint16_t* A, const uint16_t* B, uint16_t* Y, uint16_t* act_save,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of one MLP ("实现与优化" figure 10; "04 · TP/SP 的通信-计算 overlap 与工程优化" §1):
+ *   dH = gY . Bfull,  dZ = dH * act'(.)  (gated: dG, dU),
+ *   gX = sum_i dZ_i . A_i            (bf16; the shard-sum is the dgrad AllReduce stand-in),
+ *   gA += dZ^T . X,  gB += gY^T . H   (fp32 accumulate into caller-owned main_grad buffers).
+ * act_save is the buffer domino_mlp_fwd filled for the same X, A, B.  The gX reduction of
+ * each row chunk overlaps the gA weight-gradient GEMM on the compute stream. */
+DOMINO_API domino_status domino_mlp_bwd(domino_handle handle, const domino_cfg* cfg, const uint16_t* X,
+                             const uint16_t* A, const uint16_t* B, const uint16_t* act_save,
+                             const uint16_t* gY, uint16_t* gX, float* gA, float* gB,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Pre-LN residual stack of cfg->layers layers ("实现与优化": LayerNorm, GeMM + act + GeMM,
+ * residual):  Z_{l+1} = bf16(Z_l + sum_i act(LN(Z_l) . A_{l,i}^T) . B_{l,i}^T).
+ * LN has no affine parameters and eps = cfg->ln_eps; its output is rounded to bf16 before
+ * the first GEMM; the residual is added in fp32 to the shard-sum before the one rounding.
+ * A and B hold cfg->layers consecutive layer blocks.  Z_out may equal Z_in. */
+DOMINO_API domino_status domino_stack_fwd(domino_handle handle, const domino_cfg* cfg, const uint16_t* Z_in,
+                               const uint16_t* A, const uint16_t* B, uint16_t* Z_out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* The reduction step alone (the AllReduce stand-in):
+ *   Y[r, c] = bf16( (residual[r, c]) + (((P_0[r,c] + P_1[r,c]) + ...) + P_{t-1}[r,c]) )
+ * P: t slices of rows x cols fp32, slice i at P + i*rows*cols, row stride cols.
+ * residual (nullable) has row stride ld_res; Y has row stride ld_y (elements).
+ * cols must be a multiple of 8. */
+DOMINO_API domino_status domino_shard_sum(const float* P, int32_t t, int64_t rows, int64_t cols,
+                               const uint16_t* residual, int64_t ld_res, uint16_t* Y,
+                               int64_t ld_y, void* stream);
+
+/* Reads and clears the device error word of every kernel of this library.  *out is
+ * DOMINO_OK or DOMINO_ERR_TIMEOUT; *site (nullable) receives the code of the wait that
+ * expired.  Synchronises the device. */
+DOMINO_API domino_status domino_device_status(domino_handle handle, domino_status* out, int32_t* site);
+
+/* Per-kernel timing: when enabled, each launch is bracketed by CUDA events on the stream it
+ * is launched on.  domino_timing_read() synchronises on those events and returns, for one
+ * kernel kind, the number of launches and their summed duration since the last reset. */
+typedef enum {
+  DOMINO_K_GEMM_FWD1 = 0,   /* first linear + activation epilogue */
+  DOMINO_K_GEMM_FWD2 = 1,   /* second linear -> fp32 shard partials */
+  DOMINO_K_SHARD_SUM = 2,   /* shard-sum (AllReduce stand-in) */
+  DOMINO_K_LAYERNORM = 3,
+  DOMINO_K_GEMM_DGRAD_H = 4,/* gY . Bfull with activation-backward epilogue */
+  DOMINO_K_GEMM_WGRAD_B = 5,/* gB += gY^T . H */
+  DOMINO_K_GEMM_DGRAD_X = 6,/* dZ_i . A_i -> fp32 shard partials of gX */
+  DOMINO_K_GEMM_WGRAD_A = 7,/* gA += dZ^T . X */
+  DOMINO_K_COUNT = 8
+} domino_kernel_kind;
+DOMINO_API domino_status domino_timing_enable(domino_handle handle, int32_t enable);
+DOMINO_API domino_status domino_timing_reset(domino_handle handle);
+DOMINO_API domino_status domino_timing_read(domino_handle handle, int32_t kind, int64_t* launches,
+                                 double* total_ms);
+
+/* Number of kernels this library has launched through `handle` since creation. */
+DOMINO_API domino_status domino_launch_count(domino_handle handle, int64_t* launches);
+
+DOMINO_API const char* domino_status_string(domino_status status);
+
+/* Message of the last failed call on the calling host thread ("" if none). */
+DOMINO_API const char* domino_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DOMINO_H */
