@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked tensor-parallel MLP on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input: for the default
+workload (Llama-3 8B-shaped SwiGLU MLP, M = 8 x 4096 tokens, h = 4096, ffn = 14336, t = 8 shards,
+p = 2 row chunks) the forward (first linear + SwiGLU, second linear into per-shard fp32 partials,
+shard-sum) and the backward (output-gradient GEMM with SwiGLU backward, weight gradients
+accumulated into fp32, input-gradient partials and their shard-sum).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  ``value`` is GEMM TFLOP/s of the whole job (all ranks) with
+inputs resident in HBM; ``e2e`` is the same metric with the per-step host->device copy of the
+activations (X, gY) from pinned memory and the device->host read of the step's outputs (Y, gX)
+inside the timed region.  ``--impl reference`` times the CPU oracle on a bounded sample.
+With N > 1 every rank runs an independent replica (the emulated shards live on one GPU).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from comm_overlap_gb300 import synth  # noqa: E402
+
+METRIC = "TFLOP/s of chunked TP-shard MLP fwd+bwd on 1 GB300; % of dense BF16 peak"
+DEFAULT_WORKLOAD = "llama3_8b_swiglu_fwdbwd"
+ACT_NAMES = {0: "none", 1: "relu", 2: "gelu", 3: "swiglu", 4: "bilinear"}
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by workload and
+# kernel, with the SHA-256 of the GEMM kernel source at capture time; reported only while the
+# source is unchanged.  See profiles/ for the capture commands and summaries.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm.cuh", "ptx.cuh", "actfn.cuh", "kernels.h", "elementwise.cu"):
+        with open(os.path.join(ROOT, "comm_overlap_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def physical_gpu(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# ------------------------------------------------------------------------------ workload
+
+def kernel_work(s: synth.MlpShape):
+    """Algorithmic flops (GEMMs) or bytes (HBM kernels) per launch of each kernel kind."""
+    m, n = s.M // s.p, s.h // s.q
+    a_rows = s.a_rows
+    return {
+        "gemm_fwd1": ("tensor", 2.0 * m * s.h * a_rows),
+        "gemm_fwd2": ("tensor", 2.0 * m * s.F * n),
+        "shard_sum": ("hbm", s.t * m * n * 4.0 + m * n * 2.0 + (m * n * 2.0 if s.layernorm else 0.0)),
+        "layernorm": ("hbm", 2.0 * m * s.h * 2.0),
+        "gemm_dgrad_h": ("tensor", 2.0 * m * s.h * s.F),
+        "gemm_wgrad_b": ("tensor", 2.0 * m * s.h * s.F),
+        "gemm_dgrad_x": ("tensor", 2.0 * m * (2 * s.F if s.gated else s.F) * n),
+        "gemm_wgrad_a": ("tensor", 2.0 * m * (2 * s.F if s.gated else s.F) * s.h),
+    }
+
+
+def config_json(s: synth.MlpShape, sched: str, n_gpus: int):
+    return {"workload": s.name, "M": s.M, "batch": s.batch, "seq": s.seq, "h": s.h, "ffn": s.F,
+            "act": ACT_NAMES[s.act], "t": s.t, "p": s.p, "q": s.q, "layers": s.layers,
+            "layernorm": s.layernorm, "pass": "fwd+bwd" if s.backward else "fwd", "sched": sched,
+            "seed": 0, "l2": "inputs larger than L2 (129 MB); no flush needed",
+            "parallelism": "replicas" if n_gpus > 1 else "single GPU, t shards emulated in HBM"}
+
+
+# ------------------------------------------------------------------------------ CPU baseline
+
+def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
+    """Times the CPU oracle on a bounded sample of the workload; returns (flops, seconds, what)."""
+    import numpy as np
+
+    import oracle
+    X, A, B = inp["X"], inp["A"], inp["B"]
+    fwd_row = 2.0 * s.h * s.a_rows + 2.0 * s.F * s.h
+    n_fwd = max(2, int(round(24 * scale)))
+    rows = synth.sample_indices(s.M, n_fwd, 1)
+    flops = 0.0
+    t0 = time.perf_counter()
+    if s.layernorm:
+        oracle.stack_fwd(X, A, B, s.t, s.act, 1e-5, rows=rows)
+        flops += len(rows) * fwd_row * s.layers
+        what = f"{len(rows)} token rows through all {s.layers} layers"
+    else:
+        oracle.mlp_fwd(X, A[0], B[0], s.t, s.act, rows=rows)
+        flops += len(rows) * fwd_row
+        what = f"forward of {len(rows)} token rows"
+    if s.backward:
+        n_dx = max(1, int(round(8 * scale)))
+        n_ft = max(1, int(round(24 * scale)))
+        rows_b = synth.sample_indices(s.M, n_dx, 2)
+        feats = synth.sample_indices(s.F, n_ft, 3)
+        oracle.mlp_bwd(X, A[0], B[0], inp["gY"], s.t, s.act, rows=rows_b, want_dw=False)
+        oracle.mlp_bwd(X, A[0], B[0], inp["gY"], s.t, s.act, feats=feats, want_dx=False)
+        flops += len(rows_b) * (2.0 * s.h * s.F + 2.0 * s.h * s.a_rows)  # dH and dX of those rows
+        flops += len(feats) * (2.0 * s.M * s.h * (3 if s.gated else 2))  # dA rows and dB column over all M
+        what += f"; input gradient of {len(rows_b)} rows; weight gradients of {len(feats)} ffn features over all M"
+    dt = time.perf_counter() - t0
+    return flops, dt, what
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from comm_overlap_gb300 import build as cuda_build
+    from comm_overlap_gb300 import domino as dm
+
+    if rank == 0 or not os.path.exists(cuda_build.LIB):
+        cuda_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    s = args.shape
+    sched = {"serial": dm.SCHED_SERIAL, "intra": dm.SCHED_INTRA, "inter": dm.SCHED_INTER}[args.sched]
+    inp = synth.make_inputs(s, seed=0)
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    X, A, B = dev(inp["X"]), dev(inp["A"]), dev(inp["B"])
+    gY = dev(inp["gY"]) if s.backward else None
+    h = dm.domino_create()
+    cfg = dm.make_cfg(s.M, s.h, s.F, s.t, s.p, s.q, s.act, sched=sched, layers=s.layers, ln_eps=1e-5)
+    if s.layernorm:
+        wsb = dm.domino_workspace_size(cfg, dm.PASS_STACK)
+    else:
+        wsb = max(dm.domino_workspace_size(cfg, dm.PASS_FWD),
+                  dm.domino_workspace_size(cfg, dm.PASS_BWD) if s.backward else 0)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    Y = torch.empty((s.M, s.h), dtype=torch.bfloat16, device="cuda")
+    S = torch.empty((s.M, s.a_rows), dtype=torch.bfloat16, device="cuda") if s.backward else None
+    gX = torch.empty_like(Y) if s.backward else None
+    gA = torch.zeros((s.a_rows, s.h), dtype=torch.float32, device="cuda") if s.backward else None
+    gB = torch.zeros((s.t, s.h, s.Fi), dtype=torch.float32, device="cuda") if s.backward else None
+    stream = torch.cuda.current_stream()
+
+    def step(Xin, gYin):
+        if s.layernorm:
+            dm.domino_stack_fwd(h, cfg, Xin, A, B, Y, ws, wsb, stream)
+            return
+        dm.domino_mlp_fwd(h, cfg, Xin, A, B, Y, S, ws, wsb, stream)
+        if s.backward:
+            dm.domino_mlp_bwd(h, cfg, Xin, A, B, S, gYin, gX, gA, gB, ws, wsb, stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step(X, gY)
+    barrier()
+
+    # ---- device-resident timing (the `value`), per-kernel events on their own streams
+    clocks = ClockSampler(physical_gpu(local_rank))
+    clocks.start()
+    time.sleep(0.3)
+    dm.domino_timing_reset(h)
+    dm.domino_timing_enable(h, True)
+    n_launch0 = dm.domino_launch_count(h)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(X, gY)
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    dm.domino_timing_enable(h, False)
+    launches = dm.domino_launch_count(h) - n_launch0
+    ms = e0.elapsed_time(e1)
+    kern = {}
+    for k, name in enumerate(dm.KERNEL_NAMES):
+        n, tot = dm.domino_timing_read(h, k)
+        if n:
+            kern[name] = {"launches": n, "total_ms": tot}
+    st, site = dm.domino_device_status(h)
+    if st != 0:
+        raise RuntimeError(f"device error word set during the benchmark: {site:#x}")
+
+    # ---- end to end through the C ABI: pinned host inputs in, outputs back, every step
+    hX = torch.from_numpy(inp["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hgY = torch.from_numpy(inp["gY"].view(np.int16)).view(torch.bfloat16).pin_memory() if s.backward else None
+    hY = torch.empty((s.M, s.h), dtype=torch.bfloat16).pin_memory()
+    hgX = torch.empty((s.M, s.h), dtype=torch.bfloat16).pin_memory() if s.backward else None
+    Xs = torch.empty_like(X)
+    gYs = torch.empty_like(gY) if s.backward else None
+    h2d = hX.numel() * 2 + (hgY.numel() * 2 if s.backward else 0)
+    d2h = hY.numel() * 2 + (hgX.numel() * 2 if s.backward else 0)
+
+    def e2e_step():
+        Xs.copy_(hX, non_blocking=True)
+        if s.backward:
+            gYs.copy_(hgY, non_blocking=True)
+        step(Xs, gYs)
+        hY.copy_(Y, non_blocking=True)
+        if s.backward:
+            hgX.copy_(gX, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    dm.domino_destroy(h)
+
+    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms, ms_e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    flops = s.gemm_flops()
+    value = world * args.steps * flops / (ms * 1e-3) / 1e12
+    e2e = world * args.steps * flops / (ms_e2e * 1e-3) / 1e12
+    peaks = load_peaks()
+    work = kernel_work(s)
+    dom = max(kern, key=lambda k: kern[k]["total_ms"])
+    bound, per_launch = work[dom]
+    avg_ms = kern[dom]["total_ms"] / kern[dom]["launches"]
+    sha = kernel_source_sha()
+    traffic = NCU_TRAFFIC.get((s.name, dom))
+    traffic_val = traffic["bytes_per_launch"] if traffic and traffic.get("src_sha") == sha else None
+    if bound == "tensor":
+        achieved = per_launch / (avg_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_val,
+                "peak_kind": f"bf16 sustained ({peaks['source']})", "algorithmic_flops_per_launch": per_launch,
+                "avg_launch_ms": avg_ms}
+    else:
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic_val, "peak_kind": f"hbm copy ({peaks['source']})",
+                "algorithmic_bytes_per_launch": per_launch, "avg_launch_ms": avg_ms}
+    total_k = sum(v["total_ms"] for v in kern.values())
+    for name, v in kern.items():
+        b, w = work[name]
+        v["share"] = v["total_ms"] / total_k
+        v["avg_ms"] = v["total_ms"] / v["launches"]
+        if b == "tensor":
+            v["tflops"] = w / (v["avg_ms"] * 1e-3) / 1e12
+        else:
+            v["gbs"] = w / (v["avg_ms"] * 1e-3) / 1e9
+    out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": config_json(s, args.sched, world),
+           "pct_of_peak": {"of_sustained": value / world / peaks["bf16_tflops_sustained"],
+                           "of_burst": value / world / peaks["bf16_tflops"], "peaks": peaks["source"]},
+           "roofline": roof,
+           "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+           "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
+    if world == 1 and not args.no_cpu_baseline:
+        flops_s, dt, what = oracle_sample(s, inp)
+        import oracle
+        out["cpu_baseline"] = {"value": flops_s / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                               "kind": "oracle", "sample": what, "seconds": dt}
+    return out
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    s = args.shape
+    inp = synth.make_inputs(s, seed=0)
+    import oracle
+    oracle.lib()
+    for _ in range(args.warmup):
+        oracle_sample(s, inp, scale=0.1)
+    total_f, total_t, what = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        f, dt, what = oracle_sample(s, inp, scale=0.1)
+        total_f += f
+        total_t += dt
+    value = total_f / total_t / 1e12
+    cores = oracle.num_threads()
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_json(s, args.sched, 1),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + what},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.SHAPES))
+    ap.add_argument("--sched", default="intra", choices=["serial", "intra", "inter"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pass", dest="pass_", default=None, choices=["fwd", "fwd+bwd"],
+                    help="override the workload's pass (profiling aid)")
+    ap.add_argument("--p", type=int, default=None, help="override the row-chunk count")
+    ap.add_argument("--q", type=int, default=None, help="override the column-chunk count")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    import dataclasses
+    s = synth.SHAPES[args.workload]
+    over = {}
+    if args.pass_ is not None:
+        over["backward"] = args.pass_ == "fwd+bwd"
+    if args.p is not None:
+        over["p"] = args.p
+    if args.q is not None:
+        over["q"] = args.q
+    args.shape = dataclasses.replace(s, **over) if over else s
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+    else:
+        import torch
+        torch.cuda.set_device(local_rank)
+        if world > 1:
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        try:
+            out = run_ours(args, rank, world, local_rank)
+        finally:
+            if world > 1:
+                torch.distributed.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -52,16 +52,41 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def normal_bf16(shape, mean: float, std: float, seed: int, tid: int, layer: int = 0) -> np.ndarray:
-    """bf16 bits of N(mean, std) draws, shape ``shape``."""
-    n = int(np.prod(shape))
-    g = _rng(seed, tid, layer)
+_CHUNK = 1 << 22
+
+
+def _normal_block(n: int, mean: float, std: float, g: np.random.Generator) -> np.ndarray:
     x = g.standard_normal(n, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
     if mean != 0.0:
         x += np.float32(mean)
-    return f32_to_bf16_bits(x).reshape(shape)
+    return f32_to_bf16_bits(x)
+
+
+def normal_bf16(shape, mean: float, std: float, seed: int, tid: int, layer: int = 0) -> np.ndarray:
+    """bf16 bits of N(mean, std) draws, shape ``shape``.
+
+    Tensors larger than 4 Mi elements are drawn in 4 Mi-element blocks, block ``b`` from its own
+    Philox stream keyed by (seed, tid, layer, b), on a thread pool; the values do not depend on
+    the number of threads.
+    """
+    n = int(np.prod(shape))
+    if n <= _CHUNK:
+        return _normal_block(n, mean, std, _rng(seed, tid, layer)).reshape(shape)
+    import concurrent.futures as cf
+    import os
+    out = np.empty(n, dtype=np.uint16)
+    nblk = (n + _CHUNK - 1) // _CHUNK
+
+    def work(b):
+        lo, hi = b * _CHUNK, min(n, (b + 1) * _CHUNK)
+        g = np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, tid, layer, b])))
+        out[lo:hi] = _normal_block(hi - lo, mean, std, g)
+
+    with cf.ThreadPoolExecutor(max_workers=min(nblk, os.cpu_count() or 4)) as ex:
+        list(ex.map(work, range(nblk)))
+    return out.reshape(shape)
 
 
 def ternary_bf16(shape, seed: int, tid: int, layer: int = 0, p_zero: float = 0.5) -> np.ndarray:
