@@ -363,6 +363,11 @@ domino_status weight_maps_fwd(const Plan& P, const uint16_t* A, const uint16_t* 
 
 }  // namespace
 
+namespace dm {
+// Lets other translation units of the library report a message through domino_last_error().
+void set_last_error(const std::string& msg) { t_last_error = msg; }
+}  // namespace dm
+
 // =============================================================================================
 
 extern "C" {

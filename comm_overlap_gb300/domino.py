@@ -53,6 +53,7 @@ _SIGS = {
     "domino_workspace_size": [ctypes.POINTER(domino_cfg), ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
     "domino_mlp_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "domino_mlp_bwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "domino_mlp_fwd_noalloc": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P],
     "domino_stack_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "domino_shard_sum": [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int64, _P,
                          ctypes.c_int64, _P],
@@ -142,6 +143,13 @@ def domino_mlp_bwd(handle, cfg, X, A, B, act_save, gY, gX, gA, gB, workspace, wo
         workspace_bytes or 0)
     _check(lib().domino_mlp_bwd(handle, ctypes.byref(cfg), _ptr(X), _ptr(A), _ptr(B), _ptr(act_save), _ptr(gY),
                                 _ptr(gX), _ptr(gA), _ptr(gB), _ptr(workspace), wb, _stream(stream)))
+
+
+def domino_mlp_fwd_noalloc(handle, cfg, X, A, B, Y, act_save, stream=None) -> None:
+    """domino_mlp_fwd without a workspace argument: the scratch is the library's fixed 64 MiB
+    device array (for callers that cannot allocate); see include/domino.h."""
+    _check(lib().domino_mlp_fwd_noalloc(handle, ctypes.byref(cfg), _ptr(X), _ptr(A), _ptr(B), _ptr(Y),
+                                        _ptr(act_save), _stream(stream)))
 
 
 def domino_stack_fwd(handle, cfg, Z_in, A, B, Z_out, workspace, workspace_bytes=None, stream=None) -> None:

@@ -129,6 +129,24 @@ DOMINO_API domino_status domino_mlp_bwd(domino_handle handle, const domino_cfg* 
                              const uint16_t* gY, uint16_t* gX, float* gA, float* gB,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/* Forward of one MLP, exactly as domino_mlp_fwd, for callers that cannot allocate device memory
+ * when they run the layer (a plugin inside a framework that owns the whole memory pool and gives
+ * out no workspace, a serving loop that forbids allocations after warm-up, code that must avoid
+ * the device-wide synchronisation cudaMalloc/cudaFree may cause).  Not part of the method on the
+ * pages: it has no counterpart there.
+ * The scratch comes from a fixed 64 MiB array compiled into the library, which every GPU that
+ * loads the library holds until the process exits; nothing is allocated.  Problems whose
+ * domino_workspace_size(cfg, DOMINO_PASS_FWD) exceeds 64 MiB are rejected with
+ * DOMINO_ERR_WORKSPACE and nothing is launched.
+ * The first call on each device looks up the array's device address (the device current at the
+ * call); make that first call before any stream capture.  All calls share the one array: calls
+ * whose work overlaps on the GPU (other streams, other host threads, other handles on the same
+ * device) race on it and must be serialised by the caller.  The array keeps the last call's
+ * contents; the forward overwrites every scratch byte it reads, so nothing needs clearing. */
+DOMINO_API domino_status domino_mlp_fwd_noalloc(domino_handle handle, const domino_cfg* cfg,
+                                                const uint16_t* X, const uint16_t* A, const uint16_t* B,
+                                                uint16_t* Y, uint16_t* act_save, void* stream);
+
 /* Pre-LN residual stack of cfg->layers layers ("实现与优化": LayerNorm, GeMM + act + GeMM,
  * residual):  Z_{l+1} = bf16(Z_l + sum_i act(LN(Z_l) . A_{l,i}^T) . B_{l,i}^T).
  * LN has no affine parameters and eps = cfg->ln_eps; its output is rounded to bf16 before
