@@ -389,6 +389,7 @@ def main():
                     help="override the workload's pass (profiling aid)")
     ap.add_argument("--p", type=int, default=None, help="override the row-chunk count")
     ap.add_argument("--q", type=int, default=None, help="override the column-chunk count")
+    ap.add_argument("--M", type=int, default=None, help="override the token count (profiling aid)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -402,6 +403,8 @@ def main():
         over["p"] = args.p
     if args.q is not None:
         over["q"] = args.q
+    if args.M is not None:
+        over["M"] = args.M
     args.shape = dataclasses.replace(s, **over) if over else s
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

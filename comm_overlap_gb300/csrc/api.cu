@@ -210,7 +210,7 @@ GemmArgs gemm_args(int variant, int batches, int64_t M, int64_t N, int64_t K, in
   a.batches = batches;
   a.M = int32_t(M);
   a.N = int32_t(N);
-  a.m_tiles = int32_t(cdiv(M, dm::kBM));
+  a.m_tiles = int32_t(cdiv(M, dm::kTileM));
   a.n_tiles = int32_t(cdiv(N, dm::gemm_out_tile_n(variant)));
   a.k_blocks = int32_t(cdiv(K, dm::kBK));
   a.err_site = site << 4;
@@ -221,10 +221,9 @@ domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap
                        const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st) {
   const int64_t tiles = int64_t(a.batches) * a.m_tiles * a.n_tiles;
   if (tiles == 0) return DOMINO_OK;
-  const int grid = int(std::min<int64_t>(tiles, H->num_sms));
   return launch(H, kind, st, "GEMM launch", [&] {
-    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, a, grid, st)
-                                         : dm::launch_gemm_bwd(variant, ta, tb, a, grid, st);
+    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, a, st)
+                                         : dm::launch_gemm_bwd(variant, ta, tb, a, st);
   });
 }
 
@@ -354,10 +353,10 @@ domino_status weight_maps_fwd(const Plan& P, const uint16_t* A, const uint16_t* 
     std::string err;
     if (!dm::make_map_bf16(mapA, A, 4, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
   } else {
-    DM_TRY(map_k(mapA, A, P.h, P.F, 1, P.h, 0, 256));
+    DM_TRY(map_k(mapA, A, P.h, P.F, 1, P.h, 0, dm::kBBoxRows));
   }
   // B shard i is h x F_i: K-major over F_i, rows h, batch t
-  DM_TRY(map_k(mapB, B, P.Fi, P.h, P.t, P.Fi, P.h * P.Fi, 256));
+  DM_TRY(map_k(mapB, B, P.Fi, P.h, P.t, P.Fi, P.h * P.Fi, dm::kBBoxRows));
   return DOMINO_OK;
 }
 

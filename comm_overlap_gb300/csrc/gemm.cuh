@@ -24,21 +24,25 @@ namespace dm {
 // Device error word of the GEMM kernels of the including translation unit.
 static __device__ int g_gemm_err;
 
-constexpr int kABytes = kBM * kBK * 2;        // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;        // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+// Shared-memory ring geometry.  PAIR: a CTA pair computes a 256 x 256 tile with
+// tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and its half (128 rows) of B,
+// 32 KiB per stage, 6 stages.  Single CTA: 128 x 256 tiles, 48 KiB stages, 4 stages.
+template <bool PAIR>
+struct Ring {
+  static constexpr int kBRows = PAIR ? 128 : 256;        // B rows staged by one CTA
+  static constexpr int kABytes = kBM * kBK * 2;           // 16 KiB
+  static constexpr int kBBytes = kBRows * kBK * 2;        // 16 or 32 KiB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kTileM = PAIR ? 2 * kBM : kBM;     // rows of D per tile
+};
 constexpr int kCtrlBytes = 1024;
-constexpr int kSmemBytes = 1024 /* alignment slack */ + kCtrlBytes + kStages * kStageBytes;
+template <bool PAIR>
+constexpr int smem_bytes() { return 1024 /* alignment slack */ + kCtrlBytes + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes; }
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kGroupM = 8;  // tiles are visited in groups of 8 M-tiles for L2 reuse of B tiles
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;
-
-// Barrier indices in the control block.
-constexpr int kBarFull = 0;                 // [kStages]
-constexpr int kBarEmpty = kStages;          // [kStages]
-constexpr int kBarTmemFull = 2 * kStages;   // [2]
-constexpr int kBarTmemEmpty = 2 * kStages + 2;  // [2]
-constexpr int kBarDrain = 2 * kStages + 4;
+constexpr uint64_t kPeerCopyGraceNs = 100000ull;  // time given to in-flight copies after an abort
 
 __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, int& g, int& mt, int& nt) {
   const int per_batch = a.m_tiles * a.n_tiles;
@@ -191,13 +195,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, uint32_t tacc, 
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs args) {
+  using R = Ring<PAIR>;
+  constexpr int S = R::kStages;
   constexpr bool kGatedB = (EPI == EPI_GLU_BF16);
   constexpr int kOutN = kGatedB ? 128 : kBN;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
+  constexpr uint32_t kIdesc = idesc_bf16_f32(R::kTileM, kBN, A_MN, B_MN);
+  // barrier indices in the control block
+  constexpr int kBarFull = 0, kBarEmpty = S, kBarTmemFull = 2 * S, kBarTmemEmpty = 2 * S + 2,
+                kBarDrain = 2 * S + 4;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -210,16 +219,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = leader of the pair
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   int* err = &g_gemm_err;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarTmemFull + i), 1);
-      mbar_init(bar(kBarTmemEmpty + i), 4);
+      mbar_init(bar(kBarTmemEmpty + i), PAIR ? 8 : 4);
     }
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
@@ -230,70 +243,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // barrier initialisation visible to the peer before any remote signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = args.batches * args.m_tiles * args.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs of a pair load their own halves)
       uint32_t s = 0, ph = 0, armed = 0, armed_ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total && ok; tile += units) {
         int g, mt, nt;
         decode_tile(tile, args, g, mt, nt);
-        const int m0 = mt * kBM + args.a_row_off;
-        const int n0 = nt * kOutN + args.b_row_off;
+        const int m0 = mt * R::kTileM + static_cast<int>(rank) * kBM + args.a_row_off;
+        const int n0 = nt * kOutN + args.b_row_off + ((PAIR && !kGatedB) ? static_cast<int>(rank) * 128 : 0);
         const int ga = g * args.a_bmul, gb = g * args.b_bmul;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, err, args.err_site + 1)) {
             ok = false;
             break;
           }
-          const uint32_t sa = stage0 + s * kStageBytes, sb = sa + kABytes, fb = bar(kBarFull + s);
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          const uint32_t sa = stage0 + s * R::kStageBytes, sb = sa + R::kABytes;
+          const uint32_t fb_local = bar(kBarFull + s);
           const int k0 = kb * kBK;
-          if constexpr (!A_MN) {
-            tma_load_3d(sa, &tmA, fb, k0, m0, ga);
+          if constexpr (PAIR) {
+            // the leader's full barrier counts the bytes of both CTAs
+            const uint32_t fb = mapa_shared(fb_local, 0);
+            if (leader) mbar_arrive_expect_tx(fb_local, 2u * R::kStageBytes);
+            if constexpr (!A_MN) {
+              tma_load_3d_pair(sa, &tmA, fb, k0, m0, ga);
+            } else {
+              tma_load_3d_pair(sa, &tmA, fb, m0, k0, ga);
+              tma_load_3d_pair(sa + 8192, &tmA, fb, m0 + 64, k0, ga);
+            }
+            if constexpr (kGatedB) {
+              tma_load_4d_pair(sb, &tmB, fb, k0, n0, static_cast<int>(rank), g);
+            } else if constexpr (!B_MN) {
+              tma_load_3d_pair(sb, &tmB, fb, k0, n0, gb);
+            } else {
+              tma_load_3d_pair(sb, &tmB, fb, n0, k0, gb);
+              tma_load_3d_pair(sb + 8192, &tmB, fb, n0 + 64, k0, gb);
+            }
           } else {
-            tma_load_3d(sa, &tmA, fb, m0, k0, ga);
-            tma_load_3d(sa + 8192, &tmA, fb, m0 + 64, k0, ga);
-          }
-          if constexpr (kGatedB) {
-            tma_load_4d(sb, &tmB, fb, k0, n0, 0, g);
-            tma_load_4d(sb + 16384, &tmB, fb, k0, n0, 1, g);
-          } else if constexpr (!B_MN) {
-            tma_load_3d(sb, &tmB, fb, k0, n0, gb);
-          } else {
+            mbar_arrive_expect_tx(fb_local, R::kStageBytes);
+            armed |= 1u << s;
+            armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+            if constexpr (!A_MN) {
+              tma_load_3d(sa, &tmA, fb_local, k0, m0, ga);
+            } else {
+              tma_load_3d(sa, &tmA, fb_local, m0, k0, ga);
+              tma_load_3d(sa + 8192, &tmA, fb_local, m0 + 64, k0, ga);
+            }
+            if constexpr (kGatedB) {
+              tma_load_4d(sb, &tmB, fb_local, k0, n0, 0, g);
+              tma_load_4d(sb + 16384, &tmB, fb_local, k0, n0, 1, g);
+            } else if constexpr (!B_MN) {
+              tma_load_3d(sb, &tmB, fb_local, k0, n0, gb);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_3d(sb + 8192 * j, &tmB, fb, n0 + 64 * j, k0, gb);
+              for (int j = 0; j < 4; ++j) tma_load_3d(sb + 8192 * j, &tmB, fb_local, n0 + 64 * j, k0, gb);
+            }
           }
-          if (++s == kStages) {
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
       if (!ok) {
-        // wait for this CTA's copies still in flight before the CTA exits
-        for (int i = 0; i < kStages; ++i)
-          if ((armed >> i) & 1u) mbar_wait_drain(bar(kBarFull + i), (armed_ph >> i) & 1u);
+        // let this CTA's copies still in flight land before the CTA leaves
+        if constexpr (PAIR) {
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < kPeerCopyGraceNs) {
+          }
+        } else {
+          for (int i = 0; i < S; ++i)
+            if ((armed >> i) & 1u) mbar_wait_drain(bar(kBarFull + i), (armed_ph >> i) & 1u);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (the leader CTA of a pair issues for both)
       uint32_t s = 0, ph = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      for (int tile = unit; tile < total && ok; tile += units, ++it) {
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait(bar(kBarTmemEmpty + acc), use ^ 1u, abort_flag, err, args.err_site + 2)) break;
@@ -305,34 +353,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = stage0 + s * kStageBytes, sb = sa + kABytes;
+          const uint32_t sa = stage0 + s * R::kStageBytes, sb = sa + R::kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
+            if constexpr (PAIR)
+              umma_bf16_pair(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
+            else
+              umma_bf16(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
           }
-          umma_commit(bar(kBarEmpty + s));
-          if (++s == kStages) {
+          if constexpr (PAIR)
+            umma_commit_pair_multicast(bar(kBarEmpty + s), 0x3);
+          else
+            umma_commit(bar(kBarEmpty + s));
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(bar(kBarTmemFull + acc));
+        if constexpr (PAIR)
+          umma_commit_pair_multicast(bar(kBarTmemFull + acc), 0x3);
+        else
+          umma_commit(bar(kBarTmemFull + acc));
       }
       // all MMAs this thread issued have completed once the drain barrier flips
-      umma_commit(bar(kBarDrain));
+      if constexpr (PAIR)
+        umma_commit_pair(bar(kBarDrain));
+      else
+        umma_commit(bar(kBarDrain));
       mbar_wait_drain(bar(kBarDrain), 0);
     }
   } else {
     // ---------------- epilogue warps 2..5; TMEM lane quarter = warp % 4
     const int quarter = warp & 3;
-    const int row_in_tile = quarter * 32 + lane;
+    const int row_in_tile = static_cast<int>(rank) * kBM + quarter * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int tile = unit; tile < total; tile += units, ++it) {
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
       const bool ok = mbar_wait(bar(kBarTmemFull + acc), use, abort_flag, err, args.err_site + 4);
@@ -342,35 +402,90 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_tile(tile, args, g, mt, nt);
       const uint32_t tacc =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      epilogue_tile<EPI>(args, tacc, g, mt * kBM + row_in_tile, nt * kOutN);
+      epilogue_tile<EPI>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarTmemEmpty + acc));
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(bar(kBarTmemEmpty + acc), 0));
+        else
+          mbar_arrive(bar(kBarTmemEmpty + acc));
+      }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // no CTA of the pair leaves while the other may still touch its memory
+  else
+    __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
+// Launches one GEMM: one CTA (or CTA pair) per SM (pair), persistent over the tiles.
 template <int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                          int grid, cudaStream_t st) {
-  auto fn = gemm_kernel<EPI, A_MN, B_MN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                          cudaStream_t st) {
+  constexpr bool P = kPairMma;
+  auto fn = gemm_kernel<EPI, A_MN, B_MN, P>;
+  constexpr int smem = smem_bytes<P>();
+  static int max_units = 0;  // co-resident CTAs (single) or clusters (pair)
+  if (max_units == 0) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if constexpr (P) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorInvalidConfiguration;
+      max_units = n;
+    } else {
+      int dev = 0, sms = 0;
+      e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      max_units = sms;
+    }
   }
-  fn<<<grid, kThreads, kSmemBytes, st>>>(ta, tb, args);
-  return cudaGetLastError();
+  const int64_t tiles = int64_t(args.batches) * args.m_tiles * args.n_tiles;
+  if (tiles == 0) return cudaSuccess;
+  const int units = static_cast<int>(tiles < max_units ? tiles : max_units);
+  if constexpr (P) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, ta, tb, args);
+  } else {
+    fn<<<units, kThreads, smem, st>>>(ta, tb, args);
+    return cudaGetLastError();
+  }
 }
 
 static inline cudaError_t take_error_word(int* code) {

@@ -5,14 +5,13 @@
 namespace dm {
 
 int gemm_out_tile_n(int variant) { return variant == GV_FWD_GLU ? 128 : kBN; }
-size_t gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
-                            const GemmArgs& args, int grid, cudaStream_t st) {
+                            const GemmArgs& args, cudaStream_t st) {
   switch (variant) {
-    case GV_FWD_ACT: return launch_gemm_t<EPI_ACT_BF16, false, false>(ta, tb, args, grid, st);
-    case GV_FWD_GLU: return launch_gemm_t<EPI_GLU_BF16, false, false>(ta, tb, args, grid, st);
-    case GV_FWD_PARTIAL: return launch_gemm_t<EPI_F32_STORE, false, false>(ta, tb, args, grid, st);
+    case GV_FWD_ACT: return launch_gemm_t<EPI_ACT_BF16, false, false>(ta, tb, args, st);
+    case GV_FWD_GLU: return launch_gemm_t<EPI_GLU_BF16, false, false>(ta, tb, args, st);
+    case GV_FWD_PARTIAL: return launch_gemm_t<EPI_F32_STORE, false, false>(ta, tb, args, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -11,9 +11,14 @@ namespace dm {
 // Activation codes (same values as domino_act).
 enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2, ACT_SWIGLU = 3, ACT_BILINEAR = 4 };
 
-// GEMM tile shape: one CTA computes a 128 x 256 fp32 accumulator in TMEM per tile; the K loop
-// moves 64 bf16 (128 bytes, one swizzle atom) per pipeline stage.
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4, kThreads = 192;
+// GEMM tile shape: each CTA holds a 128 x 256 fp32 accumulator in TMEM per tile; the K loop
+// moves 64 bf16 (128 bytes, one swizzle atom) per pipeline stage.  With kPairMma a CTA pair
+// (cluster of 2) computes a 256 x 256 tile with tcgen05.mma.cta_group::2, each CTA staging
+// its own 128 rows of A and 128 rows of B.
+constexpr int kBM = 128, kBN = 256, kBK = 64, kThreads = 192;
+constexpr bool kPairMma = true;
+constexpr int kTileM = kPairMma ? 2 * kBM : kBM;   // rows of D per tile
+constexpr int kBBoxRows = kPairMma ? 128 : 256;     // TMA box height of a K-major B operand
 
 // Epilogues (what happens to the fp32 accumulator tile D).
 enum GemmEpi : int {
@@ -57,12 +62,12 @@ struct GemmArgs {
 };
 
 int gemm_out_tile_n(int variant);  // 128 for GV_FWD_GLU, else 256
-size_t gemm_smem_bytes();
 
+// Launch one GEMM; the grid (persistent: one CTA or CTA pair per SM or SM pair) is chosen here.
 cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
-                            const GemmArgs& args, int grid, cudaStream_t st);
+                            const GemmArgs& args, cudaStream_t st);
 cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
-                            const GemmArgs& args, int grid, cudaStream_t st);
+                            const GemmArgs& args, cudaStream_t st);
 // Reads and clears the device error word of the GEMM kernels in each translation unit.
 cudaError_t take_gemm_fwd_error(int* code);
 cudaError_t take_gemm_bwd_error(int* code);
