@@ -173,6 +173,16 @@ domino_status map_mn(CUtensorMap* m, const void* base, int64_t MN, int64_t K, in
   return map3(m, base, MN, K, batch, k_stride, batch_stride, 64, 64);
 }
 
+// fp32 output map of a partial slot: t contiguous rows x cols blocks, TMA-store box 32 x 32.
+domino_status map_f32_out(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, int64_t batch) {
+  const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(batch)};
+  const uint64_t strides[2] = {uint64_t(cols) * 4, uint64_t(cols * rows) * 4};
+  const uint32_t box[3] = {32, 32, 1};
+  std::string err;
+  if (!dm::make_map(m, 4, base, 3, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
+  return DOMINO_OK;
+}
+
 // ---- launches -----------------------------------------------------------------------------
 
 cudaEvent_t timing_event(domino_handle H) {
@@ -217,13 +227,18 @@ GemmArgs gemm_args(int variant, int batches, int64_t M, int64_t N, int64_t K, in
   return a;
 }
 
+// `tc`: the fp32 output map for the partial variants; other variants ignore it.
 domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap& ta,
-                       const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st) {
+                       const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st,
+                       const CUtensorMap* tc = nullptr) {
   const int64_t tiles = int64_t(a.batches) * a.m_tiles * a.n_tiles;
   if (tiles == 0) return DOMINO_OK;
+  if ((variant == dm::GV_FWD_PARTIAL || variant == dm::GV_BWD_PARTIAL) && tc == nullptr)
+    return fail(DOMINO_ERR_INVALID_ARG, "internal: partial GEMM without an output map");
+  const CUtensorMap& c = tc ? *tc : ta;
   return launch(H, kind, st, "GEMM launch", [&] {
-    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, a, st)
-                                         : dm::launch_gemm_bwd(variant, ta, tb, a, st);
+    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, c, a, st)
+                                         : dm::launch_gemm_bwd(variant, ta, tb, c, a, st);
   });
 }
 
@@ -334,7 +349,9 @@ domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, Sl
     a.out0 = part;
     a.ld0 = P.n;
     a.bs0 = P.m * P.n;
-    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp));
+    CUtensorMap mapP;
+    DM_TRY(map_f32_out(&mapP, part, P.n, P.m, P.t));
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp, &mapP));
     DM_TRY(slot_handoff(H, S, slot));
     DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, res_c ? res_c + qc * P.n : nullptr, P.h,
                          Yc + qc * P.n, P.h, S.red));
@@ -609,7 +626,9 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
       a.out0 = part;
       a.ld0 = P.n;
       a.bs0 = P.m * P.n;
-      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, mapDZk, mapAmn, a, S.comp));
+      CUtensorMap mapP;
+      DM_TRY(map_f32_out(&mapP, part, P.n, P.m, P.t));
+      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, mapDZk, mapAmn, a, S.comp, &mapP));
       DM_TRY(slot_handoff(H, S, slot));
       DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, nullptr, 0, gX + r0 * P.h + qc * P.n, P.h, S.red));
       DM_TRY(slot_release(H, S, R, slot));

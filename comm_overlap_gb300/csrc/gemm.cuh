@@ -37,8 +37,22 @@ struct Ring {
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;     // rows of D per tile
 };
 constexpr int kCtrlBytes = 1024;
-template <bool PAIR>
-constexpr int smem_bytes() { return 1024 /* alignment slack */ + kCtrlBytes + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes; }
+
+// Epilogue warps: 4 (one per TMEM lane quarter, all columns) or, for the activation-backward
+// epilogues whose per-element work and saved-input loads dominate, 8 (two per lane quarter,
+// half the columns each).  Block = TMA warp + MMA warp + epilogue warps.
+template <int EPI>
+constexpr int epi_warps() { return (EPI == EPI_ACT_BWD || EPI == EPI_GLU_BWD) ? 8 : 4; }
+template <int EPI>
+constexpr int block_threads() { return 64 + 32 * epi_warps<EPI>(); }
+// The fp32-partial epilogue stages its output in shared memory for TMA stores: per epilogue warp
+// two 4 KiB buffers (32 rows x 32 fp32, 128-byte swizzle).
+template <int EPI>
+constexpr int staging_bytes() { return EPI == EPI_F32_STORE ? 4 * 2 * 4096 : 0; }
+template <bool PAIR, int EPI>
+constexpr int smem_bytes() {
+  return 1024 /* alignment slack */ + kCtrlBytes + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes + staging_bytes<EPI>();
+}
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kGroupM = 8;  // tiles are visited in groups of 8 M-tiles for L2 reuse of B tiles
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;
@@ -82,25 +96,26 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* p, float* v) {
   v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
 }
 
-// Epilogue of one 128 x kOutN tile for the calling thread's row.  `tacc` addresses this warp's
-// TMEM lane quarter at column 0 of the accumulator.  Every lane executes the TMEM loads;
-// only stores are masked.
-template <int EPI>
-__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, uint32_t tacc, int g, int row,
-                                              int col0) {
+// Epilogue of NC accumulator columns of one tile for the calling thread's row.  `tacc` addresses
+// this warp's TMEM lane quarter at the first of those columns (for the gated forward: at the
+// first gate column; the matching up columns sit 128 columns further).  Every lane executes the
+// TMEM loads; only global accesses are masked.  Inputs of the next 32-column chunk are loaded
+// before the current chunk's TMEM load is awaited.
+template <int EPI, int NC>
+__device__ __forceinline__ void epilogue_cols(const GemmArgs& a, uint32_t tacc, int g, int row, int col0) {
   const bool row_ok = row < a.M;
+  const int64_t rowoff = static_cast<int64_t>(row);
   if constexpr (EPI == EPI_GLU_BF16) {
 #pragma unroll 1
-    for (int cc = 0; cc < 128; cc += 32) {
+    for (int cc = 0; cc < NC; cc += 32) {
       uint32_t rg[32], ru[32];
       tmem_ld32(tacc + cc, rg);
       tmem_ld32(tacc + 128 + cc, ru);
       tmem_ld_wait();
       const int col = col0 + cc;
       if (!row_ok) continue;
-      uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + static_cast<int64_t>(row) * a.ld0 + col;
-      uint16_t* o1 = a.out1 ? static_cast<uint16_t*>(a.out1) + g * a.bs1 + static_cast<int64_t>(row) * a.ld1 + col
-                            : nullptr;
+      uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
+      uint16_t* o1 = a.out1 ? static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col : nullptr;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         if (col + 8 * s >= a.N) break;
@@ -118,15 +133,68 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, uint32_t tacc, 
         }
       }
     }
+  } else if constexpr (EPI == EPI_ACT_BWD || EPI == EPI_GLU_BWD) {
+    // saved first-linear output of the chunk: Z (act) or G and U (gated)
+    constexpr bool kGlu = EPI == EPI_GLU_BWD;
+    const uint16_t* in = static_cast<const uint16_t*>(a.in0) + g * a.bsi + rowoff * a.ldi;
+    uint4 cz[4], cu[4], nz[4], nu[4];
+    auto fetch = [&](int col, uint4* z, uint4* u) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        if (row_ok && col + 8 * s < a.N) {
+          z[s] = *reinterpret_cast<const uint4*>(in + col + 8 * s);
+          if (kGlu) u[s] = *reinterpret_cast<const uint4*>(in + a.offi + col + 8 * s);
+        }
+      }
+    };
+    fetch(col0, cz, cu);
+#pragma unroll 1
+    for (int cc = 0; cc < NC; cc += 32) {
+      uint32_t r[32];
+      tmem_ld32(tacc + cc, r);
+      const int col = col0 + cc;
+      if (cc + 32 < NC) fetch(col + 32, nz, nu);
+      tmem_ld_wait();
+      if (row_ok && col < a.N) {
+        uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
+        uint16_t* o1 = static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          if (col + 8 * s >= a.N) break;
+          const uint32_t zw[4] = {cz[s].x, cz[s].y, cz[s].z, cz[s].w};
+          float d1[8], d2[8], hv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float z = (e & 1) ? bf16hi(zw[e >> 1]) : bf16lo(zw[e >> 1]);
+            const float dh = __uint_as_float(r[8 * s + e]);
+            if constexpr (kGlu) {
+              const uint32_t uw[4] = {cu[s].x, cu[s].y, cu[s].z, cu[s].w};
+              const float u = (e & 1) ? bf16hi(uw[e >> 1]) : bf16lo(uw[e >> 1]);
+              glu_bwd(a.act, z, u, dh, d1[e], d2[e], hv[e]);
+            } else {
+              d1[e] = dh * act_grad(a.act, z);
+              hv[e] = act_fwd(a.act, z);
+            }
+          }
+          store8_bf16(o0 + 8 * s, d1);
+          if constexpr (kGlu) store8_bf16(o0 + a.off0 + 8 * s, d2);
+          store8_bf16(o1 + 8 * s, hv);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        cz[s] = nz[s];
+        if (kGlu) cu[s] = nu[s];
+      }
+    }
   } else {
 #pragma unroll 1
-    for (int cc = 0; cc < kBN; cc += 32) {
+    for (int cc = 0; cc < NC; cc += 32) {
       uint32_t r[32];
       tmem_ld32(tacc + cc, r);
       tmem_ld_wait();
       const int col = col0 + cc;
       if (!row_ok || col >= a.N) continue;
-      const int64_t rowoff = static_cast<int64_t>(row);
       if constexpr (EPI == EPI_ACT_BF16) {
         uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
         uint16_t* o1 = a.out1 ? static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col : nullptr;
@@ -142,7 +210,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, uint32_t tacc, 
           store8_bf16(o0 + 8 * s, v);
           if (o1) store8_bf16(o1 + 8 * s, z);
         }
-      } else if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_ACCUM) {
+      } else {  // EPI_F32_STORE / EPI_F32_ACCUM
         float* o0 = static_cast<float*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
@@ -156,49 +224,49 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, uint32_t tacc, 
           }
           *dst = v;
         }
-      } else if constexpr (EPI == EPI_ACT_BWD) {
-        const uint16_t* zi = static_cast<const uint16_t*>(a.in0) + g * a.bsi + rowoff * a.ldi + col;
-        uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
-        uint16_t* o1 = static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          if (col + 8 * s >= a.N) break;
-          float z[8], dz[8], hv[8];
-          load8_bf16(zi + 8 * s, z);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            dz[e] = __uint_as_float(r[8 * s + e]) * act_grad(a.act, z[e]);
-            hv[e] = act_fwd(a.act, z[e]);
-          }
-          store8_bf16(o0 + 8 * s, dz);
-          store8_bf16(o1 + 8 * s, hv);
-        }
-      } else if constexpr (EPI == EPI_GLU_BWD) {
-        const uint16_t* gi = static_cast<const uint16_t*>(a.in0) + g * a.bsi + rowoff * a.ldi + col;
-        uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
-        uint16_t* o1 = static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          if (col + 8 * s >= a.N) break;
-          float gv[8], uv[8], dg[8], du[8], hv[8];
-          load8_bf16(gi + 8 * s, gv);
-          load8_bf16(gi + a.offi + 8 * s, uv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            glu_bwd(a.act, gv[e], uv[e], __uint_as_float(r[8 * s + e]), dg[e], du[e], hv[e]);
-          store8_bf16(o0 + 8 * s, dg);
-          store8_bf16(o0 + a.off0 + 8 * s, du);
-          store8_bf16(o1 + 8 * s, hv);
-        }
       }
     }
   }
 }
 
+// fp32 epilogue through TMA stores: each 32-column chunk of the warp's 32 rows is written to one
+// of the warp's two staging buffers (row `lane`, 16-byte chunk j at position j ^ (lane % 8), the
+// 128-byte swizzle pattern) and stored by one lane with a bulk tensor copy; TMA clips rows and
+// columns outside the output.  A buffer is rewritten only after the store issued from it two
+// chunks earlier has finished reading it.
+template <int NC>
+__device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtensorMap* tmC, uint32_t tacc, int g,
+                                                 int row0, int col0, uint32_t staging, uint32_t& nchunk,
+                                                 int lane) {
+  if (row0 >= a.M) return;
+#pragma unroll 1
+  for (int cc = 0; cc < NC; cc += 32) {
+    if (col0 + cc >= a.N) break;
+    const uint32_t buf = staging + (nchunk & 1u) * 4096u;
+    if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
+    __syncwarp();
+    uint32_t r[32];
+    tmem_ld32(tacc + cc, r);
+    tmem_ld_wait();
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u)) << 4), r[4 * j],
+                   r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmC, buf, col0 + cc, row0, g);
+      bulk_commit_group();
+    }
+    ++nchunk;
+  }
+}
+
 template <int EPI, bool A_MN, bool B_MN, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(block_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   using R = Ring<PAIR>;
   constexpr int S = R::kStages;
   constexpr bool kGatedB = (EPI == EPI_GLU_BF16);
@@ -232,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarTmemFull + i), 1);
-      mbar_init(bar(kBarTmemEmpty + i), PAIR ? 8 : 4);
+      mbar_init(bar(kBarTmemEmpty + i), (PAIR ? 2 : 1) * epi_warps<EPI>());
     }
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
@@ -241,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if constexpr (EPI == EPI_F32_STORE) tma_prefetch_map(&tmC);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -388,9 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(kBarDrain), 0);
     }
   } else {
-    // ---------------- epilogue warps 2..5; TMEM lane quarter = warp % 4
+    // ---------------- epilogue warps 2..: TMEM lane quarter = warp % 4; with 8 epilogue warps,
+    // warps 2-5 take the first half of the accumulator's columns and warps 6-9 the second
+    constexpr int kParts = epi_warps<EPI>() / 4;
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    constexpr int kHalfOut = kOutN / kParts;
     const int row_in_tile = static_cast<int>(rank) * kBM + quarter * 32 + lane;
+    const uint32_t staging = stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * 8192u;
+    uint32_t nchunk = 0;
     int it = 0;
     for (int tile = unit; tile < total; tile += units, ++it) {
       const int acc = it & 1;
@@ -400,17 +475,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int g, mt, nt;
       decode_tile(tile, args, g, mt, nt);
-      const uint32_t tacc =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      epilogue_tile<EPI>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                            static_cast<uint32_t>(acc * kBN + half * kHalfOut);
+      if constexpr (EPI == EPI_F32_STORE)
+        epilogue_f32_tma<kHalfOut>(args, &tmC, tacc, g, mt * R::kTileM + row_in_tile - lane,
+                                   nt * kOutN + half * kHalfOut, staging, nchunk, lane);
+      else
+        epilogue_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if constexpr (PAIR)
-          mbar_arrive_cluster(mapa_shared(bar(kBarTmemEmpty + acc), 0));
+          mbar_arrive_cluster_relaxed(mapa_shared(bar(kBarTmemEmpty + acc), 0));
         else
           mbar_arrive(bar(kBarTmemEmpty + acc));
       }
+    }
+    if constexpr (EPI == EPI_F32_STORE) {
+      if (lane == 0) bulk_wait_group_all();  // stores done before the staging memory goes away
+      __syncwarp();
     }
   }
 
@@ -431,11 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Launches one GEMM: one CTA (or CTA pair) per SM (pair), persistent over the tiles.
 template <int EPI, bool A_MN, bool B_MN>
-cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                          cudaStream_t st) {
+cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                          const GemmArgs& args, cudaStream_t st) {
   constexpr bool P = kPairMma;
   auto fn = gemm_kernel<EPI, A_MN, B_MN, P>;
-  constexpr int smem = smem_bytes<P>();
+  constexpr int smem = smem_bytes<P, EPI>();
+  static_assert(smem <= 232448, "shared memory beyond the per-CTA limit");
   static int max_units = 0;  // co-resident CTAs (single) or clusters (pair)
   if (max_units == 0) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -448,7 +532,7 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(2);
-      cfg.blockDim = dim3(kThreads);
+      cfg.blockDim = dim3(block_threads<EPI>());
       cfg.dynamicSmemBytes = smem;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
@@ -476,14 +560,14 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * units);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(block_threads<EPI>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, ta, tb, args);
+    return cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, args);
   } else {
-    fn<<<units, kThreads, smem, st>>>(ta, tb, args);
+    fn<<<units, block_threads<EPI>(), smem, st>>>(ta, tb, tc, args);
     return cudaGetLastError();
   }
 }

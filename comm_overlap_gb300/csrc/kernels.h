@@ -15,7 +15,7 @@ enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2, ACT_SWIGLU = 3, ACT_BILIN
 // moves 64 bf16 (128 bytes, one swizzle atom) per pipeline stage.  With kPairMma a CTA pair
 // (cluster of 2) computes a 256 x 256 tile with tcgen05.mma.cta_group::2, each CTA staging
 // its own 128 rows of A and 128 rows of B.
-constexpr int kBM = 128, kBN = 256, kBK = 64, kThreads = 192;
+constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr bool kPairMma = true;
 constexpr int kTileM = kPairMma ? 2 * kBM : kBM;   // rows of D per tile
 constexpr int kBBoxRows = kPairMma ? 128 : 256;     // TMA box height of a K-major B operand
@@ -64,9 +64,12 @@ struct GemmArgs {
 int gemm_out_tile_n(int variant);  // 128 for GV_FWD_GLU, else 256
 
 // Launch one GEMM; the grid (persistent: one CTA or CTA pair per SM or SM pair) is chosen here.
-cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
+// `tc` is the output map of the fp32-partial variants (GV_FWD_PARTIAL, GV_BWD_PARTIAL), whose
+// epilogue writes through TMA stores: fp32, (N, M, batches), box 32 x 32, 128-byte swizzle.  Other
+// variants ignore it.
+cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                             const GemmArgs& args, cudaStream_t st);
-cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                             const GemmArgs& args, cudaStream_t st);
 // Reads and clears the device error word of the GEMM kernels in each translation unit.
 cudaError_t take_gemm_fwd_error(int* code);
@@ -79,10 +82,14 @@ cudaError_t launch_shard_sum(const float* P, int t, int64_t rows, int64_t cols,
 cudaError_t launch_layernorm(const uint16_t* Z, int64_t rows, int64_t h, float eps, uint16_t* out,
                              cudaStream_t st);
 
-// Tensor maps (bf16, 128-byte swizzle, zero fill out of bounds).  dims[0] is innermost;
-// strides_bytes[i] is the stride of dims[i+1].
+// Tensor maps (128-byte swizzle, zero fill out of bounds).  dims[0] is innermost;
+// strides_bytes[i] is the stride of dims[i+1].  elem_bytes: 2 = bf16, 4 = fp32.
 bool tma_encoder_ready(std::string* err);
-bool make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                   const uint64_t* strides_bytes, const uint32_t* box, std::string* err);
+bool make_map(CUtensorMap* map, int elem_bytes, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides_bytes, const uint32_t* box, std::string* err);
+inline bool make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides_bytes, const uint32_t* box, std::string* err) {
+  return make_map(map, 2, base, rank, dims, strides_bytes, box, err);
+}
 
 }  // namespace dm
