@@ -38,7 +38,18 @@ ACT_NAMES = {0: "none", 1: "relu", 2: "gelu", 3: "swiglu", 4: "bilinear"}
 # DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by workload and
 # kernel, with the SHA-256 of the GEMM kernel source at capture time; reported only while the
 # source is unchanged.  See profiles/ for the capture commands and summaries.
-NCU_TRAFFIC = {}
+_SHA_PAIR_V1 = "d910d6463b9c3af7"
+NCU_TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full-size
+    # forward+backward workload; bytes per launch, mean of the captured launches
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.139e9, "src_sha": _SHA_PAIR_V1},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.860e9, "src_sha": _SHA_PAIR_V1},
+    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2.262e9, "src_sha": _SHA_PAIR_V1},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 5.182e9, "src_sha": _SHA_PAIR_V1},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 4.315e9, "src_sha": _SHA_PAIR_V1},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.846e9, "src_sha": _SHA_PAIR_V1},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 10.763e9, "src_sha": _SHA_PAIR_V1},
+}
 
 
 def kernel_source_sha() -> str:
@@ -343,7 +354,7 @@ def run_ours(args, rank, world, local_rank):
            "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
            "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
     if world == 1 and not args.no_cpu_baseline:
-        flops_s, dt, what = oracle_sample(s, inp)
+        flops_s, dt, what = oracle_sample(s, inp, scale=5.0)
         import oracle
         out["cpu_baseline"] = {"value": flops_s / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                                "kind": "oracle", "sample": what, "seconds": dt}

@@ -133,60 +133,6 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, uint32_t tacc, 
         }
       }
     }
-  } else if constexpr (EPI == EPI_ACT_BWD || EPI == EPI_GLU_BWD) {
-    // saved first-linear output of the chunk: Z (act) or G and U (gated)
-    constexpr bool kGlu = EPI == EPI_GLU_BWD;
-    const uint16_t* in = static_cast<const uint16_t*>(a.in0) + g * a.bsi + rowoff * a.ldi;
-    uint4 cz[4], cu[4], nz[4], nu[4];
-    auto fetch = [&](int col, uint4* z, uint4* u) {
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        if (row_ok && col + 8 * s < a.N) {
-          z[s] = *reinterpret_cast<const uint4*>(in + col + 8 * s);
-          if (kGlu) u[s] = *reinterpret_cast<const uint4*>(in + a.offi + col + 8 * s);
-        }
-      }
-    };
-    fetch(col0, cz, cu);
-#pragma unroll 1
-    for (int cc = 0; cc < NC; cc += 32) {
-      uint32_t r[32];
-      tmem_ld32(tacc + cc, r);
-      const int col = col0 + cc;
-      if (cc + 32 < NC) fetch(col + 32, nz, nu);
-      tmem_ld_wait();
-      if (row_ok && col < a.N) {
-        uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
-        uint16_t* o1 = static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          if (col + 8 * s >= a.N) break;
-          const uint32_t zw[4] = {cz[s].x, cz[s].y, cz[s].z, cz[s].w};
-          float d1[8], d2[8], hv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float z = (e & 1) ? bf16hi(zw[e >> 1]) : bf16lo(zw[e >> 1]);
-            const float dh = __uint_as_float(r[8 * s + e]);
-            if constexpr (kGlu) {
-              const uint32_t uw[4] = {cu[s].x, cu[s].y, cu[s].z, cu[s].w};
-              const float u = (e & 1) ? bf16hi(uw[e >> 1]) : bf16lo(uw[e >> 1]);
-              glu_bwd(a.act, z, u, dh, d1[e], d2[e], hv[e]);
-            } else {
-              d1[e] = dh * act_grad(a.act, z);
-              hv[e] = act_fwd(a.act, z);
-            }
-          }
-          store8_bf16(o0 + 8 * s, d1);
-          if constexpr (kGlu) store8_bf16(o0 + a.off0 + 8 * s, d2);
-          store8_bf16(o1 + 8 * s, hv);
-        }
-      }
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        cz[s] = nz[s];
-        if (kGlu) cu[s] = nu[s];
-      }
-    }
   } else {
 #pragma unroll 1
     for (int cc = 0; cc < NC; cc += 32) {
@@ -225,6 +171,116 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, uint32_t tacc, 
           *dst = v;
         }
       }
+    }
+  }
+}
+
+// Activation-backward epilogue (EPI_ACT_BWD / EPI_GLU_BWD) for all tiles of one warp, as a software
+// pipeline: the saved first-linear output (Z, or G and U) that chunk k needs is loaded while chunk
+// k-2 is processed, across tile boundaries, so the loads' latency overlaps TMEM reads, arithmetic
+// and stores.  dZ (or dG, dU) and the recomputed activation H go straight to global memory.
+template <int EPI, int NC, int kTileM, int kOutN>
+__device__ __forceinline__ void epilogue_act_bwd_loop(const GemmArgs& a, uint32_t tmem_col0, uint32_t full_bar0,
+                                                      uint32_t empty_addr0, bool pair, int unit, int units,
+                                                      int total, int row_in_tile, int col_in_tile, int lane,
+                                                      volatile int* abort_flag, int* err) {
+  constexpr bool kGlu = EPI == EPI_GLU_BWD;
+  struct Cursor {
+    int tile, cc;
+  };
+  auto advance = [&](Cursor& c) {
+    c.cc += 32;
+    if (c.cc >= NC) {
+      c.cc = 0;
+      c.tile += units;
+    }
+  };
+  auto fetch = [&](const Cursor& c, uint4* z, uint4* u) {
+    if (c.tile >= total) return;
+    int g, mt, nt;
+    decode_tile(c.tile, a, g, mt, nt);
+    const int row = mt * kTileM + row_in_tile;
+    const int col = nt * kOutN + col_in_tile + c.cc;
+    if (row >= a.M) return;
+    const uint16_t* in = static_cast<const uint16_t*>(a.in0) + g * a.bsi + static_cast<int64_t>(row) * a.ldi + col;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (col + 8 * s < a.N) {
+        z[s] = *reinterpret_cast<const uint4*>(in + 8 * s);
+        if (kGlu) u[s] = *reinterpret_cast<const uint4*>(in + a.offi + 8 * s);
+      }
+    }
+  };
+  uint4 cz[4], cu[4], az[4], au[4], bz[4], bu[4];
+  Cursor pf{unit, 0};
+  fetch(pf, cz, cu);
+  advance(pf);
+  fetch(pf, az, au);
+  advance(pf);
+  int it = 0;
+  for (int tile = unit; tile < total; tile += units, ++it) {
+    const int acc = it & 1;
+    const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+    const bool ok = mbar_wait(full_bar0 + 8u * acc, use, abort_flag, err, a.err_site + 4);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    tc_fence_after();
+    int g, mt, nt;
+    decode_tile(tile, a, g, mt, nt);
+    const int row = mt * kTileM + row_in_tile;
+    const bool row_ok = row < a.M;
+    const int64_t rowoff = static_cast<int64_t>(row);
+    const uint32_t tacc = tmem_col0 + static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+    for (int cc = 0; cc < NC; cc += 32) {
+      fetch(pf, bz, bu);
+      advance(pf);
+      uint32_t r[32];
+      tmem_ld32(tacc + cc, r);
+      tmem_ld_wait();
+      const int col = nt * kOutN + col_in_tile + cc;
+      if (row_ok && col < a.N) {
+        uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
+        uint16_t* o1 = static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          if (col + 8 * s >= a.N) break;
+          const uint32_t zw[4] = {cz[s].x, cz[s].y, cz[s].z, cz[s].w};
+          float d1[8], d2[8], hv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float z = (e & 1) ? bf16hi(zw[e >> 1]) : bf16lo(zw[e >> 1]);
+            const float dh = __uint_as_float(r[8 * s + e]);
+            if constexpr (kGlu) {
+              const uint32_t uw[4] = {cu[s].x, cu[s].y, cu[s].z, cu[s].w};
+              const float u = (e & 1) ? bf16hi(uw[e >> 1]) : bf16lo(uw[e >> 1]);
+              glu_bwd(a.act, z, u, dh, d1[e], d2[e], hv[e]);
+            } else {
+              d1[e] = dh * act_grad(a.act, z);
+              hv[e] = act_fwd(a.act, z);
+            }
+          }
+          store8_bf16(o0 + 8 * s, d1);
+          if constexpr (kGlu) store8_bf16(o0 + a.off0 + 8 * s, d2);
+          store8_bf16(o1 + 8 * s, hv);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        cz[s] = az[s];
+        az[s] = bz[s];
+        if (kGlu) {
+          cu[s] = au[s];
+          au[s] = bu[s];
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (pair)
+        mbar_arrive_cluster_relaxed(mapa_shared(empty_addr0 + 8u * acc, 0));
+      else
+        mbar_arrive(empty_addr0 + 8u * acc);
     }
   }
 }
@@ -466,29 +522,36 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     const int row_in_tile = static_cast<int>(rank) * kBM + quarter * 32 + lane;
     const uint32_t staging = stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * 8192u;
     uint32_t nchunk = 0;
-    int it = 0;
-    for (int tile = unit; tile < total; tile += units, ++it) {
-      const int acc = it & 1;
-      const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-      const bool ok = mbar_wait(bar(kBarTmemFull + acc), use, abort_flag, err, args.err_site + 4);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      tc_fence_after();
-      int g, mt, nt;
-      decode_tile(tile, args, g, mt, nt);
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                            static_cast<uint32_t>(acc * kBN + half * kHalfOut);
-      if constexpr (EPI == EPI_F32_STORE)
-        epilogue_f32_tma<kHalfOut>(args, &tmC, tacc, g, mt * R::kTileM + row_in_tile - lane,
-                                   nt * kOutN + half * kHalfOut, staging, nchunk, lane);
-      else
-        epilogue_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR)
-          mbar_arrive_cluster_relaxed(mapa_shared(bar(kBarTmemEmpty + acc), 0));
+    if constexpr (EPI == EPI_ACT_BWD || EPI == EPI_GLU_BWD) {
+      epilogue_act_bwd_loop<EPI, kHalfOut, R::kTileM, kOutN>(
+          args, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * kHalfOut),
+          bar(kBarTmemFull), bar(kBarTmemEmpty), PAIR, unit, units, total, row_in_tile, half * kHalfOut, lane,
+          abort_flag, err);
+    } else {
+      int it = 0;
+      for (int tile = unit; tile < total; tile += units, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+        const bool ok = mbar_wait(bar(kBarTmemFull + acc), use, abort_flag, err, args.err_site + 4);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        tc_fence_after();
+        int g, mt, nt;
+        decode_tile(tile, args, g, mt, nt);
+        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>(acc * kBN + half * kHalfOut);
+        if constexpr (EPI == EPI_F32_STORE)
+          epilogue_f32_tma<kHalfOut>(args, &tmC, tacc, g, mt * R::kTileM + row_in_tile - lane,
+                                     nt * kOutN + half * kHalfOut, staging, nchunk, lane);
         else
-          mbar_arrive(bar(kBarTmemEmpty + acc));
+          epilogue_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster_relaxed(mapa_shared(bar(kBarTmemEmpty + acc), 0));
+          else
+            mbar_arrive(bar(kBarTmemEmpty + acc));
+        }
       }
     }
     if constexpr (EPI == EPI_F32_STORE) {
