@@ -229,13 +229,16 @@ def run_ours(args, rank, world, local_rank):
     gB = torch.zeros((s.t, s.h, s.Fi), dtype=torch.float32, device="cuda") if s.backward else None
     stream = torch.cuda.current_stream()
 
-    def step(Xin, gYin):
+    def step_on(st, Xin, gYin):
         if s.layernorm:
-            dm.domino_stack_fwd(h, cfg, Xin, A, B, Y, ws, wsb, stream)
+            dm.domino_stack_fwd(h, cfg, Xin, A, B, Y, ws, wsb, st)
             return
-        dm.domino_mlp_fwd(h, cfg, Xin, A, B, Y, S, ws, wsb, stream)
+        dm.domino_mlp_fwd(h, cfg, Xin, A, B, Y, S, ws, wsb, st)
         if s.backward:
-            dm.domino_mlp_bwd(h, cfg, Xin, A, B, S, gYin, gX, gA, gB, ws, wsb, stream)
+            dm.domino_mlp_bwd(h, cfg, Xin, A, B, S, gYin, gX, gA, gB, ws, wsb, st)
+
+    def step(Xin, gYin):
+        step_on(stream, Xin, gYin)
 
     def barrier():
         torch.cuda.synchronize()
@@ -265,6 +268,24 @@ def run_ours(args, rank, world, local_rank):
     dm.domino_timing_enable(h, False)
     launches = dm.domino_launch_count(h) - n_launch0
     ms = e0.elapsed_time(e1)
+    ms_eager = ms
+    if args.graph:
+        # one step captured as a CUDA graph (the eager steps above did the one-time set-up),
+        # replayed `steps` times; the per-kernel timings come from the eager pass above
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step_on(side, X, gY)
+        for _ in range(args.warmup):
+            graph.replay()
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+        barrier()
+        ms = e0.elapsed_time(e1)
     kern = {}
     for k, name in enumerate(dm.KERNEL_NAMES):
         n, tot = dm.domino_timing_read(h, k)
@@ -353,6 +374,9 @@ def run_ours(args, rank, world, local_rank):
            "roofline": roof,
            "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
            "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
+    if args.graph:
+        out["config"]["graph"] = True
+        out["eager_value"] = world * args.steps * flops / (ms_eager * 1e-3) / 1e12
     if world == 1 and not args.no_cpu_baseline:
         flops_s, dt, what = oracle_sample(s, inp, scale=5.0)
         import oracle
@@ -402,6 +426,7 @@ def main():
     ap.add_argument("--q", type=int, default=None, help="override the column-chunk count")
     ap.add_argument("--M", type=int, default=None, help="override the token count (profiling aid)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="time replays of one step captured as a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
