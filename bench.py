@@ -131,6 +131,22 @@ def physical_gpu(local_rank: int) -> int:
     return local_rank
 
 
+# ------------------------------------------------------------------------------ multi-rank timing
+
+def max_over_ranks(values, world: int, device: str):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the job's time)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of `flops_per_step` in `ms` (max over ranks)."""
+    return world * steps * flops_per_step / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------------------ workload
 
 def kernel_work(s: synth.MlpShape):
@@ -325,16 +341,13 @@ def run_ours(args, rank, world, local_rank):
     ms_e2e = e0.elapsed_time(e1)
     dm.domino_destroy(h)
 
-    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, "cuda")
     if rank != 0:
         return None
 
     flops = s.gemm_flops()
-    value = world * args.steps * flops / (ms * 1e-3) / 1e12
-    e2e = world * args.steps * flops / (ms_e2e * 1e-3) / 1e12
+    value = job_tflops(flops, args.steps, world, ms)
+    e2e = job_tflops(flops, args.steps, world, ms_e2e)
     peaks = load_peaks()
     work = kernel_work(s)
     dom = max(kern, key=lambda k: kern[k]["total_ms"])

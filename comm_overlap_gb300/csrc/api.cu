@@ -32,6 +32,7 @@ struct domino_handle_s {
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> timing_pool;
   int64_t launches = 0;
+  int64_t fail_countdown = 0;  // > 0: the launch attempt that brings it to 0 fails (test hook)
 };
 
 namespace {
@@ -198,6 +199,8 @@ cudaEvent_t timing_event(domino_handle H) {
 
 template <class Fn>
 domino_status launch(domino_handle H, int kind, cudaStream_t st, const char* what, Fn&& fn) {
+  if (H->fail_countdown > 0 && --H->fail_countdown == 0)
+    return fail(DOMINO_ERR_CUDA, std::string(what) + ": injected launch failure");
   cudaEvent_t a = nullptr, b = nullptr;
   if (H->timing) {
     a = timing_event(H);
@@ -278,6 +281,16 @@ domino_status join(domino_handle H, const Streams& S, cudaStream_t caller) {
   DM_CUDA(cudaStreamWaitEvent(caller, H->ev_join_c, 0), "cudaStreamWaitEvent");
   DM_CUDA(cudaStreamWaitEvent(caller, H->ev_join_r, 0), "cudaStreamWaitEvent");
   return DOMINO_OK;
+}
+
+// Joins the internal streams back into the caller's stream whatever the outcome of the schedule,
+// so a failed call leaves no dangling work ordering behind; the first error wins.
+domino_status finish(domino_handle H, const Streams& S, cudaStream_t caller, domino_status st) {
+  if (st == DOMINO_OK) return join(H, S, caller);
+  const std::string msg = t_last_error;
+  join(H, S, caller);
+  t_last_error = msg;
+  return st;
 }
 
 // Chunk k writes partial slot k % nslots on the compute stream and is reduced on the reduction
@@ -483,13 +496,16 @@ domino_status domino_mlp_fwd(domino_handle H, const domino_cfg* cfg, const uint1
   float* parts = reinterpret_cast<float*>(w + P.off_part);
   Streams S;
   DM_TRY(fork(H, P, caller, &S));
-  SlotRing R;
-  for (int pc = 0; pc < P.p; ++pc) {
-    const int64_t r0 = pc * P.m;
-    DM_TRY(mlp_chunk_fwd(H, P, S, R, X + r0 * P.h, mapA, mapB, Hbuf, parts,
-                         act_save ? act_save + r0 * P.a_rows : nullptr, nullptr, Y + r0 * P.h, 1));
-  }
-  return join(H, S, caller);
+  const domino_status st = [&]() -> domino_status {
+    SlotRing R;
+    for (int pc = 0; pc < P.p; ++pc) {
+      const int64_t r0 = pc * P.m;
+      DM_TRY(mlp_chunk_fwd(H, P, S, R, X + r0 * P.h, mapA, mapB, Hbuf, parts,
+                           act_save ? act_save + r0 * P.a_rows : nullptr, nullptr, Y + r0 * P.h, 1));
+    }
+    return DOMINO_OK;
+  }();
+  return finish(H, S, caller, st);
 }
 
 domino_status domino_stack_fwd(domino_handle H, const domino_cfg* cfg, const uint16_t* Z_in,
@@ -516,6 +532,7 @@ domino_status domino_stack_fwd(domino_handle H, const domino_cfg* cfg, const uin
   float* parts = reinterpret_cast<float*>(w + P.off_part);
   Streams S;
   DM_TRY(fork(H, P, caller, &S));
+  const domino_status st = [&]() -> domino_status {
   SlotRing R;
   const int64_t a_layer = P.a_rows * P.h, b_layer = P.h * P.F;
   for (int l = 0; l < P.layers; ++l) {
@@ -543,7 +560,9 @@ domino_status domino_stack_fwd(domino_handle H, const domino_cfg* cfg, const uin
         DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
     }
   }
-  return join(H, S, caller);
+  return DOMINO_OK;
+  }();
+  return finish(H, S, caller, st);
 }
 
 domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint16_t* X,
@@ -578,6 +597,7 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
   DM_TRY(map_mn(&mapHmn, Hb, P.Fi, P.m, P.t, P.F, P.Fi));
   Streams S;
   DM_TRY(fork(H, P, caller, &S));
+  const domino_status st = [&]() -> domino_status {
   SlotRing R;
   // row chunks in reverse order, as the backward pass runs the forward schedule backwards
   for (int pc = P.p - 1; pc >= 0; --pc) {
@@ -643,7 +663,9 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
       DM_TRY(run_gemm(H, DOMINO_K_GEMM_WGRAD_A, dm::GV_WGRAD, mapDZmn, mapXmn, a, S.comp));
     }
   }
-  return join(H, S, caller);
+  return DOMINO_OK;
+  }();
+  return finish(H, S, caller, st);
 }
 
 domino_status domino_shard_sum(const float* Pp, int32_t t, int64_t rows, int64_t cols,
@@ -712,6 +734,23 @@ domino_status domino_timing_read(domino_handle H, int32_t kind, int64_t* launche
   }
   *launches = n;
   *total_ms = ms;
+  return DOMINO_OK;
+}
+
+domino_status domino_selftest_wait_timeout(domino_handle H, uint32_t timeout_us, void* stream) {
+  DM_TRY(ready(H));
+  if (timeout_us < 1 || timeout_us > 1000000u)
+    return fail(DOMINO_ERR_INVALID_ARG, "timeout_us must be in [1, 1000000]");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return launch(H, DOMINO_K_COUNT, st, "self-test launch", [&] {
+    return dm::launch_wait_selftest(uint64_t(timeout_us) * 1000u, DOMINO_SELFTEST_SITE, st);
+  });
+}
+
+domino_status domino_debug_fail_launch(domino_handle H, int32_t nth) {
+  if (!H) return fail(DOMINO_ERR_INVALID_ARG, "handle is NULL");
+  if (nth < 0) return fail(DOMINO_ERR_INVALID_ARG, "nth must be >= 0");
+  H->fail_countdown = nth;
   return DOMINO_OK;
 }
 

@@ -18,4 +18,24 @@ cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMa
 
 cudaError_t take_gemm_fwd_error(int* code) { return take_error_word(code); }
 
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait gives up after
+// `timeout_ns`, records `site` in the error word and the kernel returns.
+__global__ void wait_selftest_kernel(uint64_t timeout_ns, int site) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(b, 0, &abort_flag, &g_gemm_err, site, timeout_ns);
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, int site, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns, site);
+  return cudaGetLastError();
+}
+
 }  // namespace dm

@@ -71,6 +71,8 @@ cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMa
                             const GemmArgs& args, cudaStream_t st);
 cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                             const GemmArgs& args, cudaStream_t st);
+// Self-test of the bounded-wait failure path (see domino_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, int site, cudaStream_t st);
 // Reads and clears the device error word of the GEMM kernels in each translation unit.
 cudaError_t take_gemm_fwd_error(int* code);
 cudaError_t take_gemm_bwd_error(int* code);

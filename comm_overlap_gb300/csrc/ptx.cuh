@@ -57,7 +57,7 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 // abort flag is raised or the wait exceeds kWaitTimeoutNs (then the flag is raised and the
 // error word set to `site`).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err_word, int site) {
+                                          int* err_word, int site, uint64_t timeout_ns = kWaitTimeoutNs) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -66,7 +66,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       const uint64_t now = global_timer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitTimeoutNs) {
+      } else if (now - t0 > timeout_ns) {
         *abort_flag = 1;
         atomicCAS(err_word, 0, site);
         return false;

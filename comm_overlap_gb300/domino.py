@@ -62,6 +62,8 @@ _SIGS = {
     "domino_timing_reset": [_P],
     "domino_timing_read": [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)],
     "domino_launch_count": [_P, ctypes.POINTER(ctypes.c_int64)],
+    "domino_selftest_wait_timeout": [_P, ctypes.c_uint32, _P],
+    "domino_debug_fail_launch": [_P, ctypes.c_int32],
     "domino_status_string": [ctypes.c_int32],
     "domino_last_error": [],
 }
@@ -181,6 +183,17 @@ def domino_timing_read(handle, kind: int) -> tuple[int, float]:
     n, ms = ctypes.c_int64(), ctypes.c_double()
     _check(lib().domino_timing_read(handle, kind, ctypes.byref(n), ctypes.byref(ms)))
     return n.value, ms.value
+
+
+SELFTEST_SITE = 0x7F0
+
+
+def domino_selftest_wait_timeout(handle, timeout_us: int, stream=None) -> None:
+    _check(lib().domino_selftest_wait_timeout(handle, timeout_us, _stream(stream)))
+
+
+def domino_debug_fail_launch(handle, nth: int) -> None:
+    _check(lib().domino_debug_fail_launch(handle, nth))
 
 
 def domino_launch_count(handle) -> int:

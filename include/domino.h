@@ -189,6 +189,18 @@ DOMINO_API domino_status domino_timing_reset(domino_handle handle);
 DOMINO_API domino_status domino_timing_read(domino_handle handle, int32_t kind, int64_t* launches,
                                  double* total_ms);
 
+/* Failure-path self-test: launches a one-CTA kernel whose mbarrier wait can never complete.
+ * After timeout_us (1 .. 1,000,000 microseconds) the bounded wait gives up, records
+ * DOMINO_ERR_TIMEOUT with site DOMINO_SELFTEST_SITE in the device error word and the kernel
+ * returns; the GPU context stays usable.  Read the result with domino_device_status(). */
+#define DOMINO_SELFTEST_SITE 0x7F0
+DOMINO_API domino_status domino_selftest_wait_timeout(domino_handle handle, uint32_t timeout_us, void* stream);
+
+/* Test hook: the nth launch attempt from now (1-based) through `handle` fails with
+ * DOMINO_ERR_CUDA ("injected launch failure") instead of launching; 0 disables.  A call that
+ * fails this way returns after joining its internal streams back into the caller's stream. */
+DOMINO_API domino_status domino_debug_fail_launch(domino_handle handle, int32_t nth);
+
 /* Number of kernels this library has launched through `handle` since creation. */
 DOMINO_API domino_status domino_launch_count(domino_handle handle, int64_t* launches);
 

@@ -1,0 +1,76 @@
+"""Host logic of bench.py that needs no GPU: multi-rank timing aggregation over gloo (2 CPU
+ranks), whole-job throughput, the CPU-baseline sample accounting and the reference arm's rank
+handling."""
+import os
+import socket
+
+import pytest
+
+import bench
+from comm_overlap_gb300 import synth
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = [10.0 + rank, 20.0 - rank]   # rank 1 is slower in the first entry, faster in the second
+        q.put((rank, bench.max_over_ranks(local, world, "cpu")))
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0] == [11.0, 20.0] and res[1] == [11.0, 20.0]
+
+
+def test_job_throughput_counts_all_ranks():
+    s = synth.SHAPES["llama3_8b_swiglu_fwdbwd"]
+    one = bench.job_tflops(s.gemm_flops(), 10, 1, 250.0)
+    assert abs(one - 10 * s.gemm_flops() / 0.25 / 1e12) < 1e-9
+    assert abs(bench.job_tflops(s.gemm_flops(), 10, 4, 250.0) - 4 * one) < 1e-9
+
+
+def test_gemm_flops_of_the_workloads():
+    # forward: 2 M h R + 2 M F h (R = 2F gated); backward = 2 x forward
+    s = synth.SHAPES["llama3_8b_swiglu_fwdbwd"]
+    fwd = 2 * 32768 * 4096 * 2 * 14336 + 2 * 32768 * 14336 * 4096
+    assert s.gemm_flops() == 3 * fwd
+    s = synth.SHAPES["gpt3_6.7b_stack4"]
+    assert s.gemm_flops() == 4 * (2 * 32768 * 4096 * 16384 * 2)
+
+
+def test_kernel_work_sums_to_step_flops():
+    # the per-launch algorithmic flops of the GEMM kinds, times their launches per step, add up to
+    # the step's GEMM flops (p launches of each kind per step, q of the column-chunked ones)
+    s = synth.SHAPES["llama3_8b_swiglu_fwdbwd"]
+    w = bench.kernel_work(s)
+    per_step = (s.p * (w["gemm_fwd1"][1] + w["gemm_dgrad_h"][1] + w["gemm_wgrad_b"][1] + w["gemm_wgrad_a"][1])
+                + s.p * s.q * (w["gemm_fwd2"][1] + w["gemm_dgrad_x"][1]))
+    assert abs(per_step - s.gemm_flops()) / s.gemm_flops() < 1e-12
+
+
+def test_reference_arm_only_rank0_reports():
+    class A:
+        pass
+    a = A()
+    a.shape = synth.SHAPES["tiny_gelu"]
+    assert bench.run_reference(a, rank=1) is None
