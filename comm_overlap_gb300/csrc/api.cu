@@ -174,6 +174,18 @@ domino_status map_mn(CUtensorMap* m, const void* base, int64_t MN, int64_t K, in
   return map3(m, base, MN, K, batch, k_stride, batch_stride, 64, 64);
 }
 
+// bf16 (cols, rows, batch) map with a 32 x 32 box and 64-byte swizzle, for the activation-backward
+// epilogue's TMA loads and stores; row and batch strides in elements.
+domino_status map_epi_bf16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t batch,
+                           int64_t row_stride, int64_t batch_stride) {
+  const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(batch)};
+  const uint64_t strides[2] = {uint64_t(row_stride) * 2, uint64_t(batch > 1 ? batch_stride : row_stride * rows) * 2};
+  const uint32_t box[3] = {32, 32, 1};
+  std::string err;
+  if (!dm::make_map(m, 2, base, 3, dims, strides, box, &err, 64)) return fail(DOMINO_ERR_CUDA, err);
+  return DOMINO_OK;
+}
+
 // fp32 output map of a partial slot: t contiguous rows x cols blocks, TMA-store box 32 x 32.
 domino_status map_f32_out(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, int64_t batch) {
   const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(batch)};
@@ -230,18 +242,20 @@ GemmArgs gemm_args(int variant, int batches, int64_t M, int64_t N, int64_t K, in
   return a;
 }
 
-// `tc`: the fp32 output map for the partial variants; other variants ignore it.
+// `em`: the epilogue's tensor maps (fp32-partial and activation-backward variants); others ignore it.
 domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap& ta,
                        const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st,
-                       const CUtensorMap* tc = nullptr) {
+                       const dm::EpiMaps* em = nullptr) {
   const int64_t tiles = int64_t(a.batches) * a.m_tiles * a.n_tiles;
   if (tiles == 0) return DOMINO_OK;
-  if ((variant == dm::GV_FWD_PARTIAL || variant == dm::GV_BWD_PARTIAL) && tc == nullptr)
-    return fail(DOMINO_ERR_INVALID_ARG, "internal: partial GEMM without an output map");
-  const CUtensorMap& c = tc ? *tc : ta;
+  const bool needs = variant == dm::GV_FWD_PARTIAL || variant == dm::GV_BWD_PARTIAL ||
+                     variant == dm::GV_BWD_ACT || variant == dm::GV_BWD_GLU;
+  if (needs && em == nullptr) return fail(DOMINO_ERR_INVALID_ARG, "internal: GEMM epilogue without its maps");
+  static const dm::EpiMaps kNone = {};
+  const dm::EpiMaps& e = em ? *em : kNone;
   return launch(H, kind, st, "GEMM launch", [&] {
-    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, c, a, st)
-                                         : dm::launch_gemm_bwd(variant, ta, tb, c, a, st);
+    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, e, a, st)
+                                         : dm::launch_gemm_bwd(variant, ta, tb, e, a, st);
   });
 }
 
@@ -362,9 +376,9 @@ domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, Sl
     a.out0 = part;
     a.ld0 = P.n;
     a.bs0 = P.m * P.n;
-    CUtensorMap mapP;
-    DM_TRY(map_f32_out(&mapP, part, P.n, P.m, P.t));
-    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp, &mapP));
+    dm::EpiMaps em = {};
+    DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp, &em));
     DM_TRY(slot_handoff(H, S, slot));
     DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, res_c ? res_c + qc * P.n : nullptr, P.h,
                          Yc + qc * P.n, P.h, S.red));
@@ -623,7 +637,18 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
       a.out1 = Hb;
       a.ld1 = P.F;
       a.bs1 = P.Fi;
-      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_H, variant, mapGYk, mapBmn, a, S.comp));
+      // epilogue maps: saved Z (or G, U) of the chunk in, dZ (or dG, dU) and H out; each branch has
+      // its own base so a column tail is clipped at F_i
+      dm::EpiMaps em = {};
+      const uint16_t* save_c = act_save + r0 * P.a_rows;
+      DM_TRY(map_epi_bf16(&em.m[0], save_c, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+      DM_TRY(map_epi_bf16(&em.m[2], dZ, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+      if (P.gated) {
+        DM_TRY(map_epi_bf16(&em.m[1], save_c + P.Fi, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+        DM_TRY(map_epi_bf16(&em.m[3], dZ + P.Fi, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+      }
+      DM_TRY(map_epi_bf16(&em.m[4], Hb, P.Fi, P.m, P.t, P.F, P.Fi));
+      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_H, variant, mapGYk, mapBmn, a, S.comp, &em));
     }
     // gB_i += gY_c^T . H_i   (D = h x F_i, K = tokens of the chunk)
     {
@@ -646,9 +671,9 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
       a.out0 = part;
       a.ld0 = P.n;
       a.bs0 = P.m * P.n;
-      CUtensorMap mapP;
-      DM_TRY(map_f32_out(&mapP, part, P.n, P.m, P.t));
-      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, mapDZk, mapAmn, a, S.comp, &mapP));
+      dm::EpiMaps em = {};
+      DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
+      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, mapDZk, mapAmn, a, S.comp, &em));
       DM_TRY(slot_handoff(H, S, slot));
       DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, nullptr, 0, gX + r0 * P.h + qc * P.n, P.h, S.red));
       DM_TRY(slot_release(H, S, R, slot));

@@ -24,34 +24,42 @@ namespace dm {
 // Device error word of the GEMM kernels of the including translation unit.
 static __device__ int g_gemm_err;
 
+constexpr bool is_act_bwd(int epi) { return epi == EPI_ACT_BWD || epi == EPI_GLU_BWD; }
+
 // Shared-memory ring geometry.  PAIR: a CTA pair computes a 256 x 256 tile with
 // tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and its half (128 rows) of B,
-// 32 KiB per stage, 6 stages.  Single CTA: 128 x 256 tiles, 48 KiB stages, 4 stages.
-template <bool PAIR>
+// 32 KiB per stage, 6 stages (5 when the activation-backward epilogue needs its staging space).
+// Single CTA: 128 x 256 tiles, 48 KiB stages, 4 stages.
+template <bool PAIR, int EPI>
 struct Ring {
   static constexpr int kBRows = PAIR ? 128 : 256;        // B rows staged by one CTA
   static constexpr int kABytes = kBM * kBK * 2;           // 16 KiB
   static constexpr int kBBytes = kBRows * kBK * 2;        // 16 or 32 KiB
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kStages = PAIR ? (is_act_bwd(EPI) ? 5 : 6) : (is_act_bwd(EPI) ? 3 : 4);
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;     // rows of D per tile
 };
 constexpr int kCtrlBytes = 1024;
 
-// Epilogue warps: 4 (one per TMEM lane quarter, all columns) or, for the activation-backward
-// epilogues whose per-element work and saved-input loads dominate, 8 (two per lane quarter,
-// half the columns each).  Block = TMA warp + MMA warp + epilogue warps.
+// Four epilogue warps, one per TMEM lane quarter (32 rows), all accumulator columns.
+// Block = TMA warp + MMA warp + epilogue warps.
 template <int EPI>
-constexpr int epi_warps() { return (EPI == EPI_ACT_BWD || EPI == EPI_GLU_BWD) ? 8 : 4; }
+constexpr int epi_warps() { return 4; }
 template <int EPI>
 constexpr int block_threads() { return 64 + 32 * epi_warps<EPI>(); }
-// The fp32-partial epilogue stages its output in shared memory for TMA stores: per epilogue warp
-// two 4 KiB buffers (32 rows x 32 fp32, 128-byte swizzle).
+// Epilogues that move data with TMA stage it in shared memory, per epilogue warp:
+//  fp32 partials: two 4 KiB buffers (32 rows x 32 fp32, 128-byte swizzle);
+//  activation backward: 4 KiB of inputs (Z or G, U) and 6 KiB of outputs (dZ or dG, dU; H), as
+//  32 rows x 32 bf16 boxes with 64-byte swizzle.
+constexpr int kActBwdWarpBytes = 10240;
 template <int EPI>
-constexpr int staging_bytes() { return EPI == EPI_F32_STORE ? 4 * 2 * 4096 : 0; }
+constexpr int staging_bytes() {
+  return EPI == EPI_F32_STORE ? 4 * 2 * 4096 : (is_act_bwd(EPI) ? 4 * kActBwdWarpBytes : 0);
+}
 template <bool PAIR, int EPI>
 constexpr int smem_bytes() {
-  return 1024 /* alignment slack */ + kCtrlBytes + Ring<PAIR>::kStages * Ring<PAIR>::kStageBytes + staging_bytes<EPI>();
+  return 1024 /* alignment slack */ + kCtrlBytes + Ring<PAIR, EPI>::kStages * Ring<PAIR, EPI>::kStageBytes +
+         staging_bytes<EPI>();
 }
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kGroupM = 8;  // tiles are visited in groups of 8 M-tiles for L2 reuse of B tiles
@@ -175,48 +183,60 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, uint32_t tacc, 
   }
 }
 
-// Activation-backward epilogue (EPI_ACT_BWD / EPI_GLU_BWD) for all tiles of one warp, as a software
-// pipeline: the saved first-linear output (Z, or G and U) that chunk k needs is loaded while chunk
-// k-2 is processed, across tile boundaries, so the loads' latency overlaps TMEM reads, arithmetic
-// and stores.  dZ (or dG, dU) and the recomputed activation H go straight to global memory.
-template <int EPI, int NC, int kTileM, int kOutN>
-__device__ __forceinline__ void epilogue_act_bwd_loop(const GemmArgs& a, uint32_t tmem_col0, uint32_t full_bar0,
-                                                      uint32_t empty_addr0, bool pair, int unit, int units,
-                                                      int total, int row_in_tile, int col_in_tile, int lane,
-                                                      volatile int* abort_flag, int* err) {
+// Activation-backward epilogue (EPI_ACT_BWD / EPI_GLU_BWD) for all tiles of one warp (32 rows x 256
+// columns of each tile, in 32-column chunks), with every global access a TMA box:
+//  * the saved first-linear output of the chunk (Z, or G and U) is loaded into the warp's input
+//    buffer; the next chunk's load is issued as soon as the lanes have read the current one, so it
+//    overlaps the current chunk's TMEM read, arithmetic and stores;
+//  * dZ (or dG, dU) and the recomputed activation H are written into the warp's output buffer and
+//    stored with bulk tensor copies (clipped at the tensor edges).
+// Shared-memory boxes are 32 rows x 64 bytes with 64-byte swizzle: 16-byte chunk j of row r sits at
+// position j ^ ((r >> 1) & 3) of the row.
+template <int EPI, int kTileM, int kOutN>
+__device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const EpiMaps& em, uint32_t tmem_q,
+                                                     uint32_t full_bar0, uint32_t empty_addr0, uint32_t in_bar,
+                                                     uint32_t buf, bool pair, int unit, int units, int total,
+                                                     int row_off, int lane, volatile int* abort_flag, int* err) {
   constexpr bool kGlu = EPI == EPI_GLU_BWD;
+  constexpr uint32_t kInBytes = kGlu ? 4096u : 2048u;
+  const uint32_t ibuf = buf, obuf = buf + 4096u;
+  const uint32_t rsw = static_cast<uint32_t>(lane) * 64u;          // this lane's row in a box
+  const uint32_t rx = (static_cast<uint32_t>(lane) >> 1) & 3u;      // its 64-byte swizzle key
   struct Cursor {
     int tile, cc;
   };
   auto advance = [&](Cursor& c) {
     c.cc += 32;
-    if (c.cc >= NC) {
+    if (c.cc >= kOutN) {
       c.cc = 0;
       c.tile += units;
     }
   };
-  auto fetch = [&](const Cursor& c, uint4* z, uint4* u) {
-    if (c.tile >= total) return;
-    int g, mt, nt;
+  // A chunk is processed (and its inputs loaded) only if its rows and columns start in range.
+  auto chunk = [&](const Cursor& c, int& g, int& row0, int& col) -> bool {
+    if (c.tile >= total) return false;
+    int mt, nt;
     decode_tile(c.tile, a, g, mt, nt);
-    const int row = mt * kTileM + row_in_tile;
-    const int col = nt * kOutN + col_in_tile + c.cc;
-    if (row >= a.M) return;
-    const uint16_t* in = static_cast<const uint16_t*>(a.in0) + g * a.bsi + static_cast<int64_t>(row) * a.ldi + col;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      if (col + 8 * s < a.N) {
-        z[s] = *reinterpret_cast<const uint4*>(in + 8 * s);
-        if (kGlu) u[s] = *reinterpret_cast<const uint4*>(in + a.offi + 8 * s);
-      }
+    row0 = mt * kTileM + row_off;
+    col = nt * kOutN + c.cc;
+    return row0 < a.M && col < a.N;
+  };
+  bool pending = false;  // an input copy was issued and not yet waited for
+  auto issue = [&](const Cursor& c) {
+    int g, row0, col;
+    if (!chunk(c, g, row0, col)) return;
+    pending = true;
+    if (lane == 0) {
+      fence_proxy_async_smem();  // lanes' reads of the buffer precede the copy that overwrites it
+      mbar_arrive_expect_tx(in_bar, kInBytes);
+      tma_load_3d(ibuf, &em.m[0], in_bar, col, row0, g);
+      if constexpr (kGlu) tma_load_3d(ibuf + 2048u, &em.m[1], in_bar, col, row0, g);
     }
   };
-  uint4 cz[4], cu[4], az[4], au[4], bz[4], bu[4];
   Cursor pf{unit, 0};
-  fetch(pf, cz, cu);
+  issue(pf);
   advance(pf);
-  fetch(pf, az, au);
-  advance(pf);
+  uint32_t in_phase = 0, n_stored = 0;
   int it = 0;
   for (int tile = unit; tile < total; tile += units, ++it) {
     const int acc = it & 1;
@@ -224,56 +244,83 @@ __device__ __forceinline__ void epilogue_act_bwd_loop(const GemmArgs& a, uint32_
     const bool ok = mbar_wait(full_bar0 + 8u * acc, use, abort_flag, err, a.err_site + 4);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
     tc_fence_after();
-    int g, mt, nt;
-    decode_tile(tile, a, g, mt, nt);
-    const int row = mt * kTileM + row_in_tile;
-    const bool row_ok = row < a.M;
-    const int64_t rowoff = static_cast<int64_t>(row);
-    const uint32_t tacc = tmem_col0 + static_cast<uint32_t>(acc * kBN);
+    bool aborted = false;
 #pragma unroll 1
-    for (int cc = 0; cc < NC; cc += 32) {
-      fetch(pf, bz, bu);
-      advance(pf);
+    for (int cc = 0; cc < kOutN; cc += 32) {
+      const Cursor cur{tile, cc};
+      int g, row0, col;
+      const bool valid = chunk(cur, g, row0, col);
       uint32_t r[32];
-      tmem_ld32(tacc + cc, r);
-      tmem_ld_wait();
-      const int col = nt * kOutN + col_in_tile + cc;
-      if (row_ok && col < a.N) {
-        uint16_t* o0 = static_cast<uint16_t*>(a.out0) + g * a.bs0 + rowoff * a.ld0 + col;
-        uint16_t* o1 = static_cast<uint16_t*>(a.out1) + g * a.bs1 + rowoff * a.ld1 + col;
+      tmem_ld32(tmem_q + static_cast<uint32_t>(acc * kBN + cc), r);
+      uint32_t zi[16], ui[16];
+      if (valid) {
+        const bool got = mbar_wait(in_bar, in_phase, abort_flag, err, a.err_site + 5);
+        if (got) {
+          in_phase ^= 1u;
+          pending = false;
+        }
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          aborted = true;
+          tmem_ld_wait();
+          break;
+        }
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          if (col + 8 * s >= a.N) break;
-          const uint32_t zw[4] = {cz[s].x, cz[s].y, cz[s].z, cz[s].w};
-          float d1[8], d2[8], hv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float z = (e & 1) ? bf16hi(zw[e >> 1]) : bf16lo(zw[e >> 1]);
-            const float dh = __uint_as_float(r[8 * s + e]);
-            if constexpr (kGlu) {
-              const uint32_t uw[4] = {cu[s].x, cu[s].y, cu[s].z, cu[s].w};
-              const float u = (e & 1) ? bf16hi(uw[e >> 1]) : bf16lo(uw[e >> 1]);
-              glu_bwd(a.act, z, u, dh, d1[e], d2[e], hv[e]);
-            } else {
-              d1[e] = dh * act_grad(a.act, z);
-              hv[e] = act_fwd(a.act, z);
-            }
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = rsw + ((static_cast<uint32_t>(j) ^ rx) << 4);
+          const uint4 zv = ld_shared_v4(ibuf + off);
+          zi[4 * j] = zv.x; zi[4 * j + 1] = zv.y; zi[4 * j + 2] = zv.z; zi[4 * j + 3] = zv.w;
+          if constexpr (kGlu) {
+            const uint4 uv = ld_shared_v4(ibuf + 2048u + off);
+            ui[4 * j] = uv.x; ui[4 * j + 1] = uv.y; ui[4 * j + 2] = uv.z; ui[4 * j + 3] = uv.w;
           }
-          store8_bf16(o0 + 8 * s, d1);
-          if constexpr (kGlu) store8_bf16(o0 + a.off0 + 8 * s, d2);
-          store8_bf16(o1 + 8 * s, hv);
         }
       }
+      __syncwarp();
+      issue(pf);
+      advance(pf);
+      tmem_ld_wait();
+      if (!valid) continue;
+      uint32_t o1[16], o2[16], oh[16];
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        cz[s] = az[s];
-        az[s] = bz[s];
-        if (kGlu) {
-          cu[s] = au[s];
-          au[s] = bu[s];
+      for (int e = 0; e < 32; e += 2) {
+        const uint32_t zw = zi[e >> 1];
+        float d1a, d1b, d2a = 0.f, d2b = 0.f, ha, hb;
+        const float z0 = bf16lo(zw), z1 = bf16hi(zw);
+        const float g0 = __uint_as_float(r[e]), g1 = __uint_as_float(r[e + 1]);
+        if constexpr (kGlu) {
+          const uint32_t uw = ui[e >> 1];
+          glu_bwd(a.act, z0, bf16lo(uw), g0, d1a, d2a, ha);
+          glu_bwd(a.act, z1, bf16hi(uw), g1, d1b, d2b, hb);
+        } else {
+          d1a = g0 * act_grad(a.act, z0);
+          d1b = g1 * act_grad(a.act, z1);
+          ha = act_fwd(a.act, z0);
+          hb = act_fwd(a.act, z1);
         }
+        o1[e >> 1] = pack_bf16x2(d1a, d1b);
+        o2[e >> 1] = pack_bf16x2(d2a, d2b);
+        oh[e >> 1] = pack_bf16x2(ha, hb);
       }
+      if (lane == 0 && n_stored > 0) bulk_wait_group_read<0>();  // previous stores done reading
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t off = rsw + ((static_cast<uint32_t>(j) ^ rx) << 4);
+        st_shared_v4(obuf + off, o1[4 * j], o1[4 * j + 1], o1[4 * j + 2], o1[4 * j + 3]);
+        if constexpr (kGlu) st_shared_v4(obuf + 2048u + off, o2[4 * j], o2[4 * j + 1], o2[4 * j + 2], o2[4 * j + 3]);
+        st_shared_v4(obuf + 4096u + off, oh[4 * j], oh[4 * j + 1], oh[4 * j + 2], oh[4 * j + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&em.m[2], obuf, col, row0, g);
+        if constexpr (kGlu) tma_store_3d(&em.m[3], obuf + 2048u, col, row0, g);
+        tma_store_3d(&em.m[4], obuf + 4096u, col, row0, g);
+        bulk_commit_group();
+      }
+      ++n_stored;
     }
+    if (aborted) break;
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
@@ -283,6 +330,13 @@ __device__ __forceinline__ void epilogue_act_bwd_loop(const GemmArgs& a, uint32_
         mbar_arrive(empty_addr0 + 8u * acc);
     }
   }
+  if (lane == 0) {
+    bulk_wait_group_all();  // stores done before the staging memory goes away
+    // after an abort an input copy may still be in flight: let it land (bounded) before the CTA
+    // leaves; it completes the barrier phase with parity in_phase
+    if (pending) mbar_wait_drain(in_bar, in_phase);
+  }
+  __syncwarp();
 }
 
 // fp32 epilogue through TMA stores: each 32-column chunk of the warp's 32 rows is written to one
@@ -322,15 +376,15 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtens
 template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-  using R = Ring<PAIR>;
+                const __grid_constant__ EpiMaps em, const GemmArgs args) {
+  using R = Ring<PAIR, EPI>;
   constexpr int S = R::kStages;
   constexpr bool kGatedB = (EPI == EPI_GLU_BF16);
   constexpr int kOutN = kGatedB ? 128 : kBN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(R::kTileM, kBN, A_MN, B_MN);
   // barrier indices in the control block
   constexpr int kBarFull = 0, kBarEmpty = S, kBarTmemFull = 2 * S, kBarTmemEmpty = 2 * S + 2,
-                kBarDrain = 2 * S + 4;
+                kBarDrain = 2 * S + 4, kBarEpiIn = 2 * S + 5;  // kBarEpiIn: one per epilogue warp
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -359,13 +413,17 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       mbar_init(bar(kBarTmemEmpty + i), (PAIR ? 2 : 1) * epi_warps<EPI>());
     }
     mbar_init(bar(kBarDrain), 1);
+    for (int e = 0; e < epi_warps<EPI>(); ++e) mbar_init(bar(kBarEpiIn + e), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
-    if constexpr (EPI == EPI_F32_STORE) tma_prefetch_map(&tmC);
+    if constexpr (EPI == EPI_F32_STORE) tma_prefetch_map(&em.m[0]);
+    if constexpr (is_act_bwd(EPI))
+      for (int i = 0; i < 5; ++i)
+        if ((i != 1 && i != 3) || EPI == EPI_GLU_BWD) tma_prefetch_map(&em.m[i]);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -522,11 +580,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     const int row_in_tile = static_cast<int>(rank) * kBM + quarter * 32 + lane;
     const uint32_t staging = stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * 8192u;
     uint32_t nchunk = 0;
-    if constexpr (EPI == EPI_ACT_BWD || EPI == EPI_GLU_BWD) {
-      epilogue_act_bwd_loop<EPI, kHalfOut, R::kTileM, kOutN>(
-          args, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * kHalfOut),
-          bar(kBarTmemFull), bar(kBarTmemEmpty), PAIR, unit, units, total, row_in_tile, half * kHalfOut, lane,
-          abort_flag, err);
+    if constexpr (is_act_bwd(EPI)) {
+      epilogue_act_bwd_tma<EPI, R::kTileM, kOutN>(
+          args, em, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16), bar(kBarTmemFull), bar(kBarTmemEmpty),
+          bar(kBarEpiIn + (warp - 2)), stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * kActBwdWarpBytes,
+          PAIR, unit, units, total, static_cast<int>(rank) * kBM + quarter * 32, lane, abort_flag, err);
     } else {
       int it = 0;
       for (int tile = unit; tile < total; tile += units, ++it) {
@@ -540,7 +598,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * kBN + half * kHalfOut);
         if constexpr (EPI == EPI_F32_STORE)
-          epilogue_f32_tma<kHalfOut>(args, &tmC, tacc, g, mt * R::kTileM + row_in_tile - lane,
+          epilogue_f32_tma<kHalfOut>(args, &em.m[0], tacc, g, mt * R::kTileM + row_in_tile - lane,
                                      nt * kOutN + half * kHalfOut, staging, nchunk, lane);
         else
           epilogue_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
@@ -577,7 +635,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
 
 // Launches one GEMM: one CTA (or CTA pair) per SM (pair), persistent over the tiles.
 template <int EPI, bool A_MN, bool B_MN>
-cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
                           const GemmArgs& args, cudaStream_t st) {
   constexpr bool P = kPairMma;
   auto fn = gemm_kernel<EPI, A_MN, B_MN, P>;
@@ -628,9 +686,9 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, args);
+    return cudaLaunchKernelEx(&cfg, fn, ta, tb, em, args);
   } else {
-    fn<<<units, block_threads<EPI>(), smem, st>>>(ta, tb, tc, args);
+    fn<<<units, block_threads<EPI>(), smem, st>>>(ta, tb, em, args);
     return cudaGetLastError();
   }
 }

@@ -5,13 +5,13 @@
 
 namespace dm {
 
-cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
                             const GemmArgs& args, cudaStream_t st) {
   switch (variant) {
-    case GV_BWD_ACT: return launch_gemm_t<EPI_ACT_BWD, false, true>(ta, tb, tc, args, st);
-    case GV_BWD_GLU: return launch_gemm_t<EPI_GLU_BWD, false, true>(ta, tb, tc, args, st);
-    case GV_BWD_PARTIAL: return launch_gemm_t<EPI_F32_STORE, false, true>(ta, tb, tc, args, st);
-    case GV_WGRAD: return launch_gemm_t<EPI_F32_ACCUM, true, true>(ta, tb, tc, args, st);
+    case GV_BWD_ACT: return launch_gemm_t<EPI_ACT_BWD, false, true>(ta, tb, em, args, st);
+    case GV_BWD_GLU: return launch_gemm_t<EPI_GLU_BWD, false, true>(ta, tb, em, args, st);
+    case GV_BWD_PARTIAL: return launch_gemm_t<EPI_F32_STORE, false, true>(ta, tb, em, args, st);
+    case GV_WGRAD: return launch_gemm_t<EPI_F32_ACCUM, true, true>(ta, tb, em, args, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -64,12 +64,20 @@ struct GemmArgs {
 int gemm_out_tile_n(int variant);  // 128 for GV_FWD_GLU, else 256
 
 // Launch one GEMM; the grid (persistent: one CTA or CTA pair per SM or SM pair) is chosen here.
-// `tc` is the output map of the fp32-partial variants (GV_FWD_PARTIAL, GV_BWD_PARTIAL), whose
-// epilogue writes through TMA stores: fp32, (N, M, batches), box 32 x 32, 128-byte swizzle.  Other
-// variants ignore it.
-cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+// Tensor maps of the epilogues that move their data with TMA (box 32 x 32 elements):
+//  fp32-partial variants (GV_FWD_PARTIAL, GV_BWD_PARTIAL): m[0] = fp32 output (N, M, batches),
+//    128-byte swizzle.
+//  activation-backward variants (GV_BWD_ACT, GV_BWD_GLU), all bf16 with 64-byte swizzle and
+//    (F_i, M, shards) extents: m[0] saved Z or G (read), m[1] saved U (read, gated),
+//    m[2] dZ or dG (written), m[3] dU (written, gated), m[4] recomputed H (written).
+//  Other variants ignore the maps.
+struct EpiMaps {
+  CUtensorMap m[5];
+};
+
+cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
                             const GemmArgs& args, cudaStream_t st);
-cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
                             const GemmArgs& args, cudaStream_t st);
 // Self-test of the bounded-wait failure path (see domino_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int site, cudaStream_t st);
@@ -84,11 +92,11 @@ cudaError_t launch_shard_sum(const float* P, int t, int64_t rows, int64_t cols,
 cudaError_t launch_layernorm(const uint16_t* Z, int64_t rows, int64_t h, float eps, uint16_t* out,
                              cudaStream_t st);
 
-// Tensor maps (128-byte swizzle, zero fill out of bounds).  dims[0] is innermost;
-// strides_bytes[i] is the stride of dims[i+1].  elem_bytes: 2 = bf16, 4 = fp32.
+// Tensor maps (zero fill out of bounds).  dims[0] is innermost; strides_bytes[i] is the stride of
+// dims[i+1].  elem_bytes: 2 = bf16, 4 = fp32.  swizzle_bytes: 128 or 64.
 bool tma_encoder_ready(std::string* err);
 bool make_map(CUtensorMap* map, int elem_bytes, const void* base, int rank, const uint64_t* dims,
-              const uint64_t* strides_bytes, const uint32_t* box, std::string* err);
+              const uint64_t* strides_bytes, const uint32_t* box, std::string* err, int swizzle_bytes = 128);
 inline bool make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                           const uint64_t* strides_bytes, const uint32_t* box, std::string* err) {
   return make_map(map, 2, base, rank, dims, strides_bytes, box, err);

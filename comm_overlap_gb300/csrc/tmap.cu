@@ -29,7 +29,7 @@ bool tma_encoder_ready(std::string* err) {
 }
 
 bool make_map(CUtensorMap* map, int elem_bytes, const void* base, int rank, const uint64_t* dims,
-              const uint64_t* strides_bytes, const uint32_t* box, std::string* err) {
+              const uint64_t* strides_bytes, const uint32_t* box, std::string* err, int swizzle_bytes) {
   if (!tma_encoder_ready(err)) return false;
   cuuint64_t gdim[5];
   cuuint64_t gstride[4];
@@ -45,7 +45,8 @@ bool make_map(CUtensorMap* map, int elem_bytes, const void* base, int rank, cons
       elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUresult r = g_encode(map, dt, static_cast<cuuint32_t>(rank),
                               const_cast<void*>(base), gdim, gstride, bdim, estride,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     if (err) {
