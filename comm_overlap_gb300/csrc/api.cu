@@ -248,8 +248,7 @@ domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap
                        const dm::EpiMaps* em = nullptr) {
   const int64_t tiles = int64_t(a.batches) * a.m_tiles * a.n_tiles;
   if (tiles == 0) return DOMINO_OK;
-  const bool needs = variant == dm::GV_FWD_PARTIAL || variant == dm::GV_BWD_PARTIAL ||
-                     variant == dm::GV_BWD_ACT || variant == dm::GV_BWD_GLU;
+  const bool needs = variant != dm::GV_WGRAD;
   if (needs && em == nullptr) return fail(DOMINO_ERR_INVALID_ARG, "internal: GEMM epilogue without its maps");
   static const dm::EpiMaps kNone = {};
   const dm::EpiMaps& e = em ? *em : kNone;
@@ -362,7 +361,19 @@ domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, Sl
     a.ld1 = P.a_rows;
     a.bs1 = P.gated ? 2 * P.Fi : 0;
     a.off1 = P.Fi;
-    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD1, variant, mapX, mapA, a, S.comp));
+    // epilogue maps: H (per shard for the gated form), and the saved Z or G, U
+    dm::EpiMaps em = {};
+    if (P.gated) {
+      DM_TRY(map_epi_bf16(&em.m[0], Hbuf, P.Fi, P.m, P.t, P.F, P.Fi));
+      if (save_c) {
+        DM_TRY(map_epi_bf16(&em.m[1], save_c, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+        DM_TRY(map_epi_bf16(&em.m[2], save_c + P.Fi, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+      }
+    } else {
+      DM_TRY(map_epi_bf16(&em.m[0], Hbuf, P.F, P.m, 1, P.F, 0));
+      if (save_c) DM_TRY(map_epi_bf16(&em.m[1], save_c, P.F, P.m, 1, P.F, 0));
+    }
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD1, variant, mapX, mapA, a, S.comp, &em));
   }
   DM_TRY(map_k(&mapH, Hbuf, P.Fi, P.m, P.t, P.F, P.Fi, 128));
   for (int qc = 0; qc < P.q; ++qc) {

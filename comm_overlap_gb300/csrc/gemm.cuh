@@ -51,10 +51,14 @@ constexpr int block_threads() { return 64 + 32 * epi_warps<EPI>(); }
 //  fp32 partials: two 4 KiB buffers (32 rows x 32 fp32, 128-byte swizzle);
 //  activation backward: 4 KiB of inputs (Z or G, U) and 6 KiB of outputs (dZ or dG, dU; H), as
 //  32 rows x 32 bf16 boxes with 64-byte swizzle.
+//  forward activation: up to three 2 KiB output boxes (H; saved Z, or G and U), 64-byte swizzle.
 constexpr int kActBwdWarpBytes = 10240;
+constexpr int kFwdWarpBytes = 6144;
+constexpr bool is_act_fwd(int epi) { return epi == EPI_ACT_BF16 || epi == EPI_GLU_BF16; }
 template <int EPI>
 constexpr int staging_bytes() {
-  return EPI == EPI_F32_STORE ? 4 * 2 * 4096 : (is_act_bwd(EPI) ? 4 * kActBwdWarpBytes : 0);
+  return EPI == EPI_F32_STORE ? 4 * 2 * 4096
+                              : (is_act_bwd(EPI) ? 4 * kActBwdWarpBytes : (is_act_fwd(EPI) ? 4 * kFwdWarpBytes : 0));
 }
 template <bool PAIR, int EPI>
 constexpr int smem_bytes() {
@@ -339,6 +343,65 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
   __syncwarp();
 }
 
+// Forward first-linear epilogue through TMA stores (EPI_ACT_BF16 / EPI_GLU_BF16), one 32-column chunk
+// at a time for the warp's 32 rows: H = act(D) (or glu(gate, up)) and, when the backward's saved
+// copy is requested, the pre-activation Z (or G and U), each rounded to bf16, written to the warp's
+// staging boxes (64-byte swizzle) and stored with bulk tensor copies.  Maps: m[0] H, m[1] Z or G,
+// m[2] U.  The staging boxes are rewritten once the previous chunk's stores have read them.
+template <int EPI, int NC>
+__device__ __forceinline__ void epilogue_fwd_tma(const GemmArgs& a, const EpiMaps& em, uint32_t tacc, int g,
+                                                 int row0, int col0, uint32_t buf, uint32_t& nstore, int lane) {
+  constexpr bool kGlu = EPI == EPI_GLU_BF16;
+  if (row0 >= a.M) return;
+  const bool save = a.out1 != nullptr;
+  const uint32_t rsw = static_cast<uint32_t>(lane) * 64u;
+  const uint32_t rx = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll 1
+  for (int cc = 0; cc < NC; cc += 32) {
+    const int col = col0 + cc;
+    if (col >= a.N) break;
+    uint32_t rz[32], ru[32];
+    tmem_ld32(tacc + cc, rz);
+    if constexpr (kGlu) tmem_ld32(tacc + 128 + cc, ru);
+    tmem_ld_wait();
+    uint32_t oh[16], oz[16], ou[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const float z0 = __uint_as_float(rz[e]), z1 = __uint_as_float(rz[e + 1]);
+      if constexpr (kGlu) {
+        const float u0 = __uint_as_float(ru[e]), u1 = __uint_as_float(ru[e + 1]);
+        oh[e >> 1] = pack_bf16x2(glu_fwd(a.act, z0, u0), glu_fwd(a.act, z1, u1));
+        ou[e >> 1] = pack_bf16x2(u0, u1);
+      } else {
+        oh[e >> 1] = pack_bf16x2(act_fwd(a.act, z0), act_fwd(a.act, z1));
+      }
+      oz[e >> 1] = pack_bf16x2(z0, z1);
+    }
+    if (lane == 0 && nstore > 0) bulk_wait_group_read<0>();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t off = rsw + ((static_cast<uint32_t>(j) ^ rx) << 4);
+      st_shared_v4(buf + off, oh[4 * j], oh[4 * j + 1], oh[4 * j + 2], oh[4 * j + 3]);
+      if (save) {
+        st_shared_v4(buf + 2048u + off, oz[4 * j], oz[4 * j + 1], oz[4 * j + 2], oz[4 * j + 3]);
+        if constexpr (kGlu) st_shared_v4(buf + 4096u + off, ou[4 * j], ou[4 * j + 1], ou[4 * j + 2], ou[4 * j + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(&em.m[0], buf, col, row0, g);
+      if (save) {
+        tma_store_3d(&em.m[1], buf + 2048u, col, row0, g);
+        if constexpr (kGlu) tma_store_3d(&em.m[2], buf + 4096u, col, row0, g);
+      }
+      bulk_commit_group();
+    }
+    ++nstore;
+  }
+}
+
 // fp32 epilogue through TMA stores: each 32-column chunk of the warp's 32 rows is written to one
 // of the warp's two staging buffers (row `lane`, 16-byte chunk j at position j ^ (lane % 8), the
 // 128-byte swizzle pattern) and stored by one lane with a bulk tensor copy; TMA clips rows and
@@ -421,6 +484,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
     if constexpr (EPI == EPI_F32_STORE) tma_prefetch_map(&em.m[0]);
+    if constexpr (is_act_fwd(EPI)) {
+      tma_prefetch_map(&em.m[0]);
+      if (args.out1) tma_prefetch_map(&em.m[1]);
+      if (EPI == EPI_GLU_BF16 && args.out1) tma_prefetch_map(&em.m[2]);
+    }
     if constexpr (is_act_bwd(EPI))
       for (int i = 0; i < 5; ++i)
         if ((i != 1 && i != 3) || EPI == EPI_GLU_BWD) tma_prefetch_map(&em.m[i]);
@@ -600,6 +668,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         if constexpr (EPI == EPI_F32_STORE)
           epilogue_f32_tma<kHalfOut>(args, &em.m[0], tacc, g, mt * R::kTileM + row_in_tile - lane,
                                      nt * kOutN + half * kHalfOut, staging, nchunk, lane);
+        else if constexpr (is_act_fwd(EPI))
+          epilogue_fwd_tma<EPI, kHalfOut>(args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
+                                          nt * kOutN + half * kHalfOut,
+                                          stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * kFwdWarpBytes,
+                                          nchunk, lane);
         else
           epilogue_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
         tc_fence_before();
@@ -612,7 +685,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         }
       }
     }
-    if constexpr (EPI == EPI_F32_STORE) {
+    if constexpr (EPI == EPI_F32_STORE || is_act_fwd(EPI)) {
       if (lane == 0) bulk_wait_group_all();  // stores done before the staging memory goes away
       __syncwarp();
     }
