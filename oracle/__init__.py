@@ -45,6 +45,10 @@ def lib():
                 f.restype = _I
             L.oracle_stack_fwd_bf16.argtypes = [_I, _I64, _I64, _I64, _I, _I, _D, _P, _P, _P, _P, _I64, _P]
             L.oracle_stack_fwd_bf16.restype = _I
+            for name in ("oracle_stack_bwd_bf16", "oracle_stack_bwd_f64"):
+                f = getattr(L, name)
+                f.argtypes = [_I, _I64, _I64, _I64, _I, _I, _D, _P, _P, _P, _P, _P, _I64, _P, _P, _P]
+                f.restype = _I
             for name in ("oracle_act", "oracle_act_grad"):
                 getattr(L, name).argtypes = [_I, _D]
                 getattr(L, name).restype = _D
@@ -152,6 +156,29 @@ def stack_fwd(Z, A, B, t, act, eps=1e-5, rows=None):
     if rc != 0:
         raise ValueError(f"oracle_stack_fwd failed ({rc})")
     return out
+
+
+def stack_bwd(Z, A, B, gZ, t, act, eps=1e-5, rows=None, want_w=False):
+    """(gZ0, dA, dB) of the pre-LN residual stack for the output gradient gZ.
+
+    A: [L, a_rows, h], B: [L, t, h, F_i].  gZ0: n_rows x h.  dA, dB (want_w, all rows only):
+    the weight gradients in the A and B storage layouts, [L, a_rows, h] and [L, t, h, F_i].
+    """
+    Z, A, B, gZ = (np.ascontiguousarray(a) for a in (Z, A, B, gZ))
+    k = _kind(Z, A, B, gZ)
+    L = A.shape[0]
+    M, h, F = _shape(Z, np.empty(A.shape[1:], A.dtype), np.empty(B.shape[1:], B.dtype), t, act)
+    if want_w and rows is not None:
+        raise ValueError("weight gradients need every row")
+    r, n = _rows(rows)
+    gZ0 = np.empty((n if r is not None else M, h), np.float64)
+    dA = np.empty(A.shape, np.float64) if want_w else None
+    dB = np.empty(B.shape, np.float64) if want_w else None
+    rc = getattr(lib(), f"oracle_stack_bwd_{k}")(L, M, h, F, t, act, eps, _ptr(Z), _ptr(A), _ptr(B), _ptr(gZ),
+                                               _ptr(r), n, _ptr(gZ0), _ptr(dA), _ptr(dB))
+    if rc != 0:
+        raise ValueError(f"oracle_stack_bwd failed ({rc})")
+    return gZ0, dA, dB
 
 
 def act(a, z):

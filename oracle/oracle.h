@@ -86,6 +86,17 @@ int oracle_stack_fwd_bf16(int L, int64_t M, int64_t h, int64_t F, int t, int act
                           const uint16_t* Z0, const uint16_t* A, const uint16_t* B,
                           const int64_t* rows, int64_t n_rows, double* Zout);
 
+/* Backward of the pre-LN residual stack for the gradient gZL of Z_L: gZ0 (n_rows x h) is the
+ * gradient w.r.t. the stack input at the selected rows.  dA, dB (nullable; then rows must be
+ * NULL): the weight gradients of every layer, summed over all M rows, in the A and B storage
+ * layouts (L layer blocks each).  Returns -3 if weight gradients are asked for a row subset. */
+int oracle_stack_bwd_bf16(int L, int64_t M, int64_t h, int64_t F, int t, int act, double eps,
+                          const uint16_t* Z0, const uint16_t* A, const uint16_t* B, const uint16_t* gZL,
+                          const int64_t* rows, int64_t n_rows, double* gZ0, double* dA, double* dB);
+int oracle_stack_bwd_f64(int L, int64_t M, int64_t h, int64_t F, int t, int act, double eps,
+                         const double* Z0, const double* A, const double* B, const double* gZL,
+                         const int64_t* rows, int64_t n_rows, double* gZ0, double* dA, double* dB);
+
 /* Elementwise helpers, exposed so tests can pin them against special values. */
 double oracle_act(int act, double z);        /* non-gated activations */
 double oracle_act_grad(int act, double z);

@@ -340,3 +340,66 @@ def test_seeded_inputs_are_deterministic_bf16():
     # 1+2^-8 is a tie between bf16 neighbours 1 and 1+2^-7: ties go to even (1.0)
     assert np.array_equal(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(f))[:2], [1.0, 1.0])
     assert synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(f))[2] == np.float32(1.0078125)
+
+
+# ---------------------------------------------------------------- stack backward
+
+def _torch_stack(Z, A, B, t, act, eps):
+    """float64 autograd reference of the pre-LN residual stack (library routines)."""
+    import torch
+    gated = act in ACTS_GATED
+    z = Z
+    for l in range(A.shape[0]):
+        Bfull = torch.cat([B[l][i] for i in range(t)], dim=1)
+        if gated:
+            Fi = A.shape[1] // (2 * t)
+            gate = torch.cat([A[l][i * 2 * Fi:i * 2 * Fi + Fi] for i in range(t)], dim=0)
+            up = torch.cat([A[l][i * 2 * Fi + Fi:(i + 1) * 2 * Fi] for i in range(t)], dim=0)
+        else:
+            gate = A[l]
+        n = torch.nn.functional.layer_norm(z, (z.shape[1],), eps=eps)
+        if gated:
+            g, u = n @ gate.T, n @ up.T
+            hact = (torch.nn.functional.silu(g) * u) if act == oracle.ACT_SWIGLU else g * u
+        else:
+            zz = n @ gate.T
+            hact = {oracle.ACT_GELU: torch.nn.functional.gelu, oracle.ACT_RELU: torch.relu}.get(act, lambda v: v)(zz)
+        z = z + hact @ Bfull.T
+    return z
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_GELU, oracle.ACT_SWIGLU, oracle.ACT_NONE])
+def test_stack_bwd_matches_float64_autograd(act):
+    import torch
+    L, M, h, F, t = 3, 5, 16, 32, 2
+    s = synth.MlpShape("sb", M, h, F, act, t, 1, 1, layers=L, layernorm=True, backward=True)
+    d = synth.make_inputs(s, seed=12)
+    d["A"] = synth.normal_bf16(d["A"].shape, 0, 0.3, 12, synth.TID_A)  # larger weights: non-trivial LN paths
+    Zf, Af, Bf, gf = (synth.bf16_bits_to_f32(d[k]).astype(np.float64) for k in ("X", "A", "B", "gY"))
+    Zt = torch.from_numpy(Zf).requires_grad_(True)
+    At = torch.from_numpy(Af).requires_grad_(True)
+    Bt = torch.from_numpy(Bf).requires_grad_(True)
+    out = _torch_stack(Zt, At, Bt, t, act, 1e-5)
+    out.backward(torch.from_numpy(gf))
+    gZ0, dA, dB = oracle.stack_bwd(d["X"], d["A"], d["B"], d["gY"], t, act, 1e-5, want_w=True)
+    np.testing.assert_allclose(gZ0, Zt.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dA, At.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dB, Bt.grad.numpy(), rtol=1e-9, atol=1e-11)
+    # the double-input entry point agrees
+    gZ0_64, dA64, dB64 = oracle.stack_bwd(Zf, Af, Bf, gf, t, act, 1e-5, want_w=True)
+    np.testing.assert_allclose(gZ0_64, gZ0, rtol=1e-13, atol=1e-15)
+
+
+def test_stack_bwd_rows_and_identity():
+    L, M, h, F, t, act = 2, 9, 16, 32, 4, oracle.ACT_GELU
+    s = synth.MlpShape("sb", M, h, F, act, t, 1, 1, layers=L, layernorm=True, backward=True)
+    d = synth.make_inputs(s, seed=13)
+    full, _, _ = oracle.stack_bwd(d["X"], d["A"], d["B"], d["gY"], t, act)
+    rows = np.array([0, 4, 8])
+    part, _, _ = oracle.stack_bwd(d["X"], d["A"], d["B"], d["gY"], t, act, rows=rows)
+    assert np.array_equal(part, full[rows])
+    # zero layers: the gradient passes through unchanged
+    g0, _, _ = oracle.stack_bwd(d["X"], d["A"][:0], d["B"][:0], d["gY"], t, act)
+    assert np.array_equal(g0, synth.bf16_bits_to_f32(d["gY"]).astype(np.float64))
+    with pytest.raises(ValueError):
+        oracle.stack_bwd(d["X"], d["A"], d["B"], d["gY"], t, act, rows=rows, want_w=True)
