@@ -162,6 +162,7 @@ def kernel_work(s: synth.MlpShape):
         "gemm_wgrad_b": ("tensor", 2.0 * m * s.h * s.F),
         "gemm_dgrad_x": ("tensor", 2.0 * m * (2 * s.F if s.gated else s.F) * n),
         "gemm_wgrad_a": ("tensor", 2.0 * m * (2 * s.F if s.gated else s.F) * s.h),
+        "layernorm_bwd": ("hbm", 4.0 * m * s.h * 2.0 + m * 4.0),
     }
 
 
@@ -194,7 +195,14 @@ def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
         oracle.mlp_fwd(X, A[0], B[0], s.t, s.act, rows=rows)
         flops += len(rows) * fwd_row
         what = f"forward of {len(rows)} token rows"
-    if s.backward:
+    if s.backward and s.layernorm:
+        n_b = max(1, int(round(4 * scale)))
+        rows_b = synth.sample_indices(s.M, n_b, 2)
+        oracle.stack_bwd(X, A, B, inp["gY"], s.t, s.act, 1e-5, rows=rows_b)
+        # forward again (the row backward recomputes it) plus dH and dX per layer
+        flops += len(rows_b) * s.layers * (fwd_row + 2.0 * s.h * s.F + 2.0 * s.h * s.a_rows)
+        what += f"; input gradient of {len(rows_b)} rows through all {s.layers} layers"
+    elif s.backward:
         n_dx = max(1, int(round(8 * scale)))
         n_ft = max(1, int(round(24 * scale)))
         rows_b = synth.sample_indices(s.M, n_dx, 2)
@@ -233,21 +241,28 @@ def run_ours(args, rank, world, local_rank):
     h = dm.domino_create()
     cfg = dm.make_cfg(s.M, s.h, s.F, s.t, s.p, s.q, s.act, sched=sched, layers=s.layers, ln_eps=1e-5)
     if s.layernorm:
-        wsb = dm.domino_workspace_size(cfg, dm.PASS_STACK)
+        wsb = max(dm.domino_workspace_size(cfg, dm.PASS_STACK),
+                  dm.domino_workspace_size(cfg, dm.PASS_STACK_BWD) if s.backward else 0)
     else:
         wsb = max(dm.domino_workspace_size(cfg, dm.PASS_FWD),
                   dm.domino_workspace_size(cfg, dm.PASS_BWD) if s.backward else 0)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     Y = torch.empty((s.M, s.h), dtype=torch.bfloat16, device="cuda")
-    S = torch.empty((s.M, s.a_rows), dtype=torch.bfloat16, device="cuda") if s.backward else None
+    S = torch.empty((s.M, s.a_rows), dtype=torch.bfloat16, device="cuda") if s.backward and not s.layernorm else None
+    save = (torch.empty(dm.domino_stack_save_size(cfg), dtype=torch.uint8, device="cuda")
+            if s.backward and s.layernorm else None)
     gX = torch.empty_like(Y) if s.backward else None
-    gA = torch.zeros((s.a_rows, s.h), dtype=torch.float32, device="cuda") if s.backward else None
-    gB = torch.zeros((s.t, s.h, s.Fi), dtype=torch.float32, device="cuda") if s.backward else None
+    gA = torch.zeros((s.layers * s.a_rows, s.h), dtype=torch.float32, device="cuda") if s.backward else None
+    gB = torch.zeros((s.layers * s.t, s.h, s.Fi), dtype=torch.float32, device="cuda") if s.backward else None
     stream = torch.cuda.current_stream()
 
     def step_on(st, Xin, gYin):
         if s.layernorm:
-            dm.domino_stack_fwd(h, cfg, Xin, A, B, Y, ws, wsb, st)
+            if s.backward:
+                dm.domino_stack_fwd_train(h, cfg, Xin, A, B, Y, save, ws, None, wsb, st)
+                dm.domino_stack_bwd(h, cfg, A, B, save, gYin, gX, gA, gB, ws, None, wsb, st)
+            else:
+                dm.domino_stack_fwd(h, cfg, Xin, A, B, Y, ws, wsb, st)
             return
         dm.domino_mlp_fwd(h, cfg, Xin, A, B, Y, S, ws, wsb, st)
         if s.backward:

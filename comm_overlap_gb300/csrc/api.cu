@@ -66,7 +66,10 @@ struct Plan {
   float eps;
   bool gated;
   // workspace offsets
-  size_t off_h = 0, off_ln = 0, off_dz = 0, off_hb = 0, off_part = 0, part_slot = 0, total = 0;
+  size_t off_h = 0, off_ln = 0, off_dz = 0, off_hb = 0, off_gn = 0, off_part = 0, part_slot = 0, total = 0;
+  // layer-stack save buffer (training forward -> backward): per layer the LayerNorm output N
+  // (M x h bf16), the first-linear output (M x a_rows bf16) and 1/sqrt(var + eps) (M fp32)
+  size_t save_n = 0, save_act = 0, save_rstd = 0, save_layer = 0;
 };
 
 domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
@@ -86,11 +89,11 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
     return fail(DOMINO_ERR_ALIGNMENT, "h, ffn/t and h/q must be multiples of 8 (16-byte rows)");
   if (c->M > (int64_t(1) << 31) - 1 || c->h > (int64_t(1) << 20) || c->ffn > (int64_t(1) << 24))
     return fail(DOMINO_ERR_UNSUPPORTED, "size beyond the supported range");
-  if (pass == DOMINO_PASS_STACK) {
+  if (pass == DOMINO_PASS_STACK || pass == DOMINO_PASS_STACK_BWD) {
     if (c->layers < 1) return fail(DOMINO_ERR_INVALID_ARG, "layers must be >= 1");
     if (!(c->ln_eps > 0.0f)) return fail(DOMINO_ERR_INVALID_ARG, "ln_eps must be > 0");
   }
-  if (pass < DOMINO_PASS_FWD || pass > DOMINO_PASS_STACK) return fail(DOMINO_ERR_INVALID_ARG, "bad pass");
+  if (pass < DOMINO_PASS_FWD || pass > DOMINO_PASS_STACK_BWD) return fail(DOMINO_ERR_INVALID_ARG, "bad pass");
   Plan& p = *P;
   p.M = c->M; p.h = c->h; p.F = c->ffn; p.Fi = Fi; p.t = c->t; p.p = c->p; p.q = c->q;
   p.act = c->act; p.sched = c->sched; p.layers = c->layers; p.eps = c->ln_eps;
@@ -100,6 +103,10 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   p.a_rows = p.gated ? 2 * p.F : p.F;
   p.Ri = p.gated ? 2 * Fi : Fi;
   p.nslots = (p.p * p.q >= 2) ? 2 : 1;
+  p.save_n = 0;
+  p.save_act = align_up(size_t(p.M) * p.h * 2);
+  p.save_rstd = p.save_act + align_up(size_t(p.M) * p.a_rows * 2);
+  p.save_layer = p.save_rstd + align_up(size_t(p.M) * 4);
   size_t off = 0;
   if (p.M == 0) {
     p.total = 0;
@@ -117,6 +124,10 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
     off = align_up(off + size_t(p.m) * p.a_rows * 2);
     p.off_hb = off;
     off = align_up(off + size_t(p.m) * p.F * 2);
+    if (pass == DOMINO_PASS_STACK_BWD) {
+      p.off_gn = off;  // gradient at the LayerNorm output, all rows
+      off = align_up(off + size_t(p.M) * p.h * 2);
+    }
   }
   p.part_slot = align_up(size_t(p.t) * p.m * p.n * 4);
   p.off_part = off;
@@ -415,6 +426,164 @@ domino_status weight_maps_fwd(const Plan& P, const uint16_t* A, const uint16_t* 
   return DOMINO_OK;
 }
 
+// Buffers and maps of one backward pass that do not change across row chunks.
+struct BwdCtx {
+  uint16_t* dZ;
+  uint16_t* Hb;
+  float* parts;
+  CUtensorMap mapBmn, mapAmn, mapDZk, mapDZmn, mapHmn;
+};
+
+domino_status bwd_ctx(const Plan& P, const uint16_t* A, const uint16_t* B, uint8_t* ws, BwdCtx* C) {
+  C->dZ = reinterpret_cast<uint16_t*>(ws + P.off_dz);
+  C->Hb = reinterpret_cast<uint16_t*>(ws + P.off_hb);
+  C->parts = reinterpret_cast<float*>(ws + P.off_part);
+  // weight maps: B_i (h x F_i) read MN-major (N = F_i, K = h); A_i (R_i x h) read MN-major (N = h, K = R_i)
+  DM_TRY(map_mn(&C->mapBmn, B, P.Fi, P.h, P.t, P.Fi, P.h * P.Fi));
+  DM_TRY(map_mn(&C->mapAmn, A, P.h, P.Ri, P.t, P.h, P.Ri * P.h));
+  DM_TRY(map_k(&C->mapDZk, C->dZ, P.Ri, P.m, P.t, P.a_rows, P.Ri, 128));
+  DM_TRY(map_mn(&C->mapDZmn, C->dZ, P.Ri, P.m, P.t, P.a_rows, P.Ri));
+  DM_TRY(map_mn(&C->mapHmn, C->Hb, P.Fi, P.m, P.t, P.F, P.Fi));
+  return DOMINO_OK;
+}
+
+// Backward of one MLP for the row chunk starting at X_c / gY_c / gX_c (m rows): dH with the
+// activation backward -> dZ, H; gB += gY_c^T H; per column chunk the gX partials (compute stream)
+// and their shard-sum into gX_c (reduction stream); gA += dZ^T X_c, overlapping that reduction.
+domino_status mlp_chunk_bwd(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, const BwdCtx& C,
+                            const uint16_t* X_c, const uint16_t* save_c, const uint16_t* gY_c, uint16_t* gX_c,
+                            float* gA, float* gB) {
+  CUtensorMap mapGYk, mapGYmn, mapXmn;
+  DM_TRY(map_k(&mapGYk, gY_c, P.h, P.m, 1, P.h, 0, 128));
+  DM_TRY(map_mn(&mapGYmn, gY_c, P.h, P.m, 1, P.h, 0));
+  DM_TRY(map_mn(&mapXmn, X_c, P.h, P.m, 1, P.h, 0));
+  // dH_i = gY_c . B_i, with the activation backward in the epilogue -> dZ (dG|dU), H
+  {
+    const int variant = P.gated ? dm::GV_BWD_GLU : dm::GV_BWD_ACT;
+    GemmArgs a = gemm_args(variant, P.t, P.m, P.Fi, P.h, 3);
+    a.act = P.act;
+    a.b_bmul = 1;
+    a.in0 = save_c;
+    a.ldi = P.a_rows;
+    a.bsi = P.Ri;
+    a.offi = P.Fi;
+    a.out0 = C.dZ;
+    a.ld0 = P.a_rows;
+    a.bs0 = P.Ri;
+    a.off0 = P.Fi;
+    a.out1 = C.Hb;
+    a.ld1 = P.F;
+    a.bs1 = P.Fi;
+    // epilogue maps: saved Z (or G, U) of the chunk in, dZ (or dG, dU) and H out; each branch has
+    // its own base so a column tail is clipped at F_i
+    dm::EpiMaps em = {};
+    DM_TRY(map_epi_bf16(&em.m[0], save_c, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+    DM_TRY(map_epi_bf16(&em.m[2], C.dZ, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+    if (P.gated) {
+      DM_TRY(map_epi_bf16(&em.m[1], save_c + P.Fi, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+      DM_TRY(map_epi_bf16(&em.m[3], C.dZ + P.Fi, P.Fi, P.m, P.t, P.a_rows, P.Ri));
+    }
+    DM_TRY(map_epi_bf16(&em.m[4], C.Hb, P.Fi, P.m, P.t, P.F, P.Fi));
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_H, variant, mapGYk, C.mapBmn, a, S.comp, &em));
+  }
+  // gB_i += gY_c^T . H_i   (D = h x F_i, K = tokens of the chunk)
+  {
+    GemmArgs a = gemm_args(dm::GV_WGRAD, P.t, P.h, P.Fi, P.m, 4);
+    a.b_bmul = 1;
+    a.out0 = gB;
+    a.ld0 = P.Fi;
+    a.bs0 = P.h * P.Fi;
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_WGRAD_B, dm::GV_WGRAD, mapGYmn, C.mapHmn, a, S.comp));
+  }
+  // gX partials: P_i = dZ_i . A_i (D = m x n per column chunk), reduced on the reduction stream
+  for (int qc = 0; qc < P.q; ++qc) {
+    int slot;
+    DM_TRY(slot_acquire(H, P, S, R, &slot));
+    float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(C.parts) + P.part_slot * slot);
+    GemmArgs a = gemm_args(dm::GV_BWD_PARTIAL, P.t, P.m, P.n, P.Ri, 5);
+    a.a_bmul = 1;
+    a.b_row_off = int32_t(qc * P.n);
+    a.b_bmul = 1;
+    a.out0 = part;
+    a.ld0 = P.n;
+    a.bs0 = P.m * P.n;
+    dm::EpiMaps em = {};
+    DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, C.mapDZk, C.mapAmn, a, S.comp, &em));
+    DM_TRY(slot_handoff(H, S, slot));
+    DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, nullptr, 0, gX_c + qc * P.n, P.h, S.red));
+    DM_TRY(slot_release(H, S, R, slot));
+  }
+  // gA_i += dZ_i^T . X_c (D = R_i x h, K = tokens), overlapping the gX reduction
+  {
+    GemmArgs a = gemm_args(dm::GV_WGRAD, P.t, P.Ri, P.h, P.m, 6);
+    a.a_bmul = 1;
+    a.out0 = gA;
+    a.ld0 = P.h;
+    a.bs0 = P.Ri * P.h;
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_WGRAD_A, dm::GV_WGRAD, C.mapDZmn, mapXmn, a, S.comp));
+  }
+  return DOMINO_OK;
+}
+
+domino_status ensure_row_events(domino_handle H, int p) {
+  while (int(H->ev_row.size()) < p) {
+    cudaEvent_t e;
+    DM_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate");
+    H->ev_row.push_back(e);
+  }
+  return DOMINO_OK;
+}
+
+// Before row chunk pc of a layer (other than the first processed): INTER waits only for the same
+// row chunk of the previous layer; INTRA, at the layer's first chunk, for every row chunk of it.
+domino_status wait_previous_layer(domino_handle H, const Plan& P, const Streams& S, int pc, bool first_chunk) {
+  if (!S.overlap) return DOMINO_OK;
+  if (P.sched == DOMINO_SCHED_INTER) {
+    DM_CUDA(cudaStreamWaitEvent(S.comp, H->ev_row[pc], 0), "cudaStreamWaitEvent(row)");
+  } else if (first_chunk) {
+    for (int j = 0; j < P.p; ++j) DM_CUDA(cudaStreamWaitEvent(S.comp, H->ev_row[j], 0), "cudaStreamWaitEvent(row)");
+  }
+  return DOMINO_OK;
+}
+
+// Forward of the pre-LN residual stack; with `save` it also keeps, per layer, the LayerNorm output,
+// the first-linear output and 1/sqrt(var + eps) for domino_stack_bwd.
+domino_status stack_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_in, const uint16_t* A,
+                             const uint16_t* B, uint16_t* Z_out, uint8_t* save, void* ws, cudaStream_t caller) {
+  DM_TRY(ensure_row_events(H, P.p));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* Hbuf = reinterpret_cast<uint16_t*>(w + P.off_h);
+  uint16_t* lnbuf = reinterpret_cast<uint16_t*>(w + P.off_ln);
+  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  Streams S;
+  DM_TRY(fork(H, P, caller, &S));
+  const domino_status st = [&]() -> domino_status {
+    SlotRing R;
+    const int64_t a_layer = P.a_rows * P.h, b_layer = P.h * P.F;
+    for (int l = 0; l < P.layers; ++l) {
+      CUtensorMap mapA, mapB;
+      DM_TRY(weight_maps_fwd(P, A + l * a_layer, B + l * b_layer, &mapA, &mapB));
+      const uint16_t* src = (l == 0) ? Z_in : Z_out;
+      uint8_t* sl = save ? save + l * P.save_layer : nullptr;
+      for (int pc = 0; pc < P.p; ++pc) {
+        const int64_t r0 = pc * P.m;
+        if (l > 0) DM_TRY(wait_previous_layer(H, P, S, pc, pc == 0));
+        uint16_t* n_c = sl ? reinterpret_cast<uint16_t*>(sl + P.save_n) + r0 * P.h : lnbuf;
+        float* rstd_c = sl ? reinterpret_cast<float*>(sl + P.save_rstd) + r0 : nullptr;
+        uint16_t* act_c = sl ? reinterpret_cast<uint16_t*>(sl + P.save_act) + r0 * P.a_rows : nullptr;
+        DM_TRY(launch(H, DOMINO_K_LAYERNORM, S.comp, "LayerNorm launch", [&] {
+          return dm::launch_layernorm(src + r0 * P.h, P.m, P.h, P.eps, n_c, rstd_c, S.comp);
+        }));
+        DM_TRY(mlp_chunk_fwd(H, P, S, R, n_c, mapA, mapB, Hbuf, parts, act_c, src + r0 * P.h, Z_out + r0 * P.h, 2));
+        if (S.overlap) DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
+      }
+    }
+    return DOMINO_OK;
+  }();
+  return finish(H, S, caller, st);
+}
+
 }  // namespace
 
 namespace dm {
@@ -545,47 +714,89 @@ domino_status domino_stack_fwd(domino_handle H, const domino_cfg* cfg, const uin
   DM_TRY(check_ptr(Z_out, "Z_out"));
   DM_TRY(check_ws(P, ws, ws_bytes));
   if (P.M == 0) return DOMINO_OK;
+  return stack_fwd_impl(H, P, Z_in, A, B, Z_out, nullptr, ws, static_cast<cudaStream_t>(stream));
+}
+
+domino_status domino_stack_save_size(const domino_cfg* cfg, size_t* bytes) {
+  if (!bytes) return fail(DOMINO_ERR_INVALID_ARG, "bytes is NULL");
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_STACK, &P));
+  *bytes = P.M == 0 ? 0 : P.save_layer * size_t(P.layers);
+  return DOMINO_OK;
+}
+
+domino_status domino_stack_fwd_train(domino_handle H, const domino_cfg* cfg, const uint16_t* Z_in,
+                                     const uint16_t* A, const uint16_t* B, uint16_t* Z_out, void* save,
+                                     size_t save_bytes, void* ws, size_t ws_bytes, void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_STACK, &P));
+  DM_TRY(check_ptr(Z_in, "Z_in"));
+  DM_TRY(check_ptr(A, "A"));
+  DM_TRY(check_ptr(B, "B"));
+  DM_TRY(check_ptr(Z_out, "Z_out"));
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  if (!save || (reinterpret_cast<uintptr_t>(save) & 255u) != 0)
+    return fail(DOMINO_ERR_INVALID_ARG, "save must be a 256-byte aligned device buffer");
+  if (save_bytes < P.save_layer * size_t(P.layers))
+    return fail(DOMINO_ERR_INVALID_ARG, "save buffer too small: need " +
+                                            std::to_string(P.save_layer * size_t(P.layers)) + " bytes");
+  return stack_fwd_impl(H, P, Z_in, A, B, Z_out, static_cast<uint8_t*>(save), ws, static_cast<cudaStream_t>(stream));
+}
+
+domino_status domino_stack_bwd(domino_handle H, const domino_cfg* cfg, const uint16_t* A, const uint16_t* B,
+                               const void* save, size_t save_bytes, const uint16_t* gZ_out, uint16_t* gZ_in,
+                               float* gA, float* gB, void* ws, size_t ws_bytes, void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_STACK_BWD, &P));
+  DM_TRY(check_ptr(A, "A"));
+  DM_TRY(check_ptr(B, "B"));
+  DM_TRY(check_ptr(gZ_out, "gZ_out"));
+  DM_TRY(check_ptr(gZ_in, "gZ_in"));
+  DM_TRY(check_ptr(gA, "gA"));
+  DM_TRY(check_ptr(gB, "gB"));
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  if (!save || (reinterpret_cast<uintptr_t>(save) & 255u) != 0)
+    return fail(DOMINO_ERR_INVALID_ARG, "save must be a 256-byte aligned device buffer");
+  if (save_bytes < P.save_layer * size_t(P.layers))
+    return fail(DOMINO_ERR_INVALID_ARG, "save buffer too small");
+  DM_TRY(ensure_row_events(H, P.p));
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
-  while (int(H->ev_row.size()) < P.p) {
-    cudaEvent_t e;
-    DM_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate");
-    H->ev_row.push_back(e);
-  }
   uint8_t* w = static_cast<uint8_t*>(ws);
-  uint16_t* Hbuf = reinterpret_cast<uint16_t*>(w + P.off_h);
-  uint16_t* lnbuf = reinterpret_cast<uint16_t*>(w + P.off_ln);
-  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  uint16_t* gn = reinterpret_cast<uint16_t*>(w + P.off_gn);
+  const uint8_t* sv = static_cast<const uint8_t*>(save);
   Streams S;
   DM_TRY(fork(H, P, caller, &S));
   const domino_status st = [&]() -> domino_status {
-  SlotRing R;
-  const int64_t a_layer = P.a_rows * P.h, b_layer = P.h * P.F;
-  for (int l = 0; l < P.layers; ++l) {
-    CUtensorMap mapA, mapB;
-    DM_TRY(weight_maps_fwd(P, A + l * a_layer, B + l * b_layer, &mapA, &mapB));
-    const uint16_t* src = (l == 0) ? Z_in : Z_out;
-    for (int pc = 0; pc < P.p; ++pc) {
-      const int64_t r0 = pc * P.m;
-      if (S.overlap && l > 0) {
-        if (P.sched == DOMINO_SCHED_INTER) {
-          // row chunk pc of this layer needs only row chunk pc of the previous layer
-          DM_CUDA(cudaStreamWaitEvent(S.comp, H->ev_row[pc], 0), "cudaStreamWaitEvent(row)");
-        } else if (pc == 0) {
-          // INTRA: the previous layer ends with a synchronisation of all its row chunks
-          for (int j = 0; j < P.p; ++j)
-            DM_CUDA(cudaStreamWaitEvent(S.comp, H->ev_row[j], 0), "cudaStreamWaitEvent(row)");
-        }
+    SlotRing R;
+    const int64_t a_layer = P.a_rows * P.h, b_layer = P.h * P.F;
+    for (int l = P.layers - 1; l >= 0; --l) {
+      BwdCtx C;
+      DM_TRY(bwd_ctx(P, A + l * a_layer, B + l * b_layer, w, &C));
+      const uint8_t* sl = sv + l * P.save_layer;
+      const uint16_t* n_l = reinterpret_cast<const uint16_t*>(sl + P.save_n);
+      const uint16_t* act_l = reinterpret_cast<const uint16_t*>(sl + P.save_act);
+      const float* rstd_l = reinterpret_cast<const float*>(sl + P.save_rstd);
+      // the gradient arriving at this layer's output: the caller's for the last layer, then the
+      // running gradient kept in gZ_in
+      const uint16_t* g = (l == P.layers - 1) ? gZ_out : gZ_in;
+      for (int pc = P.p - 1; pc >= 0; --pc) {
+        const int64_t r0 = pc * P.m;
+        if (l < P.layers - 1) DM_TRY(wait_previous_layer(H, P, S, pc, pc == P.p - 1));
+        DM_TRY(mlp_chunk_bwd(H, P, S, R, C, n_l + r0 * P.h, act_l + r0 * P.a_rows, g + r0 * P.h, gn + r0 * P.h,
+                             gA + l * a_layer, gB + l * b_layer));
+        // LayerNorm backward plus the residual path for the chunk's rows, after its reductions
+        DM_TRY(launch(H, DOMINO_K_LN_BWD, S.red, "LayerNorm backward launch", [&] {
+          return dm::launch_layernorm_bwd(gn + r0 * P.h, n_l + r0 * P.h, rstd_l + r0, g + r0 * P.h,
+                                          gZ_in + r0 * P.h, P.m, P.h, S.red);
+        }));
+        if (S.overlap) DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
       }
-      DM_TRY(launch(H, DOMINO_K_LAYERNORM, S.comp, "LayerNorm launch", [&] {
-        return dm::launch_layernorm(src + r0 * P.h, P.m, P.h, P.eps, lnbuf, S.comp);
-      }));
-      DM_TRY(mlp_chunk_fwd(H, P, S, R, lnbuf, mapA, mapB, Hbuf, parts, nullptr, src + r0 * P.h,
-                           Z_out + r0 * P.h, 2));
-      if (S.overlap)
-        DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
     }
-  }
-  return DOMINO_OK;
+    return DOMINO_OK;
   }();
   return finish(H, S, caller, st);
 }
@@ -608,98 +819,19 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
   DM_TRY(check_ws(P, ws, ws_bytes));
   if (P.M == 0) return DOMINO_OK;
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  uint16_t* dZ = reinterpret_cast<uint16_t*>(w + P.off_dz);
-  uint16_t* Hb = reinterpret_cast<uint16_t*>(w + P.off_hb);
-  float* parts = reinterpret_cast<float*>(w + P.off_part);
-  // weight maps: B_i (h x F_i) read MN-major (N = F_i, K = h); A_i (R_i x h) read MN-major
-  // (N = h, K = R_i)
-  CUtensorMap mapBmn, mapAmn, mapDZk, mapDZmn, mapHmn;
-  DM_TRY(map_mn(&mapBmn, B, P.Fi, P.h, P.t, P.Fi, P.h * P.Fi));
-  DM_TRY(map_mn(&mapAmn, A, P.h, P.Ri, P.t, P.h, P.Ri * P.h));
-  DM_TRY(map_k(&mapDZk, dZ, P.Ri, P.m, P.t, P.a_rows, P.Ri, 128));
-  DM_TRY(map_mn(&mapDZmn, dZ, P.Ri, P.m, P.t, P.a_rows, P.Ri));
-  DM_TRY(map_mn(&mapHmn, Hb, P.Fi, P.m, P.t, P.F, P.Fi));
+  BwdCtx C;
+  DM_TRY(bwd_ctx(P, A, B, static_cast<uint8_t*>(ws), &C));
   Streams S;
   DM_TRY(fork(H, P, caller, &S));
   const domino_status st = [&]() -> domino_status {
-  SlotRing R;
-  // row chunks in reverse order, as the backward pass runs the forward schedule backwards
-  for (int pc = P.p - 1; pc >= 0; --pc) {
-    const int64_t r0 = pc * P.m;
-    CUtensorMap mapGYk, mapGYmn, mapXmn;
-    DM_TRY(map_k(&mapGYk, gY + r0 * P.h, P.h, P.m, 1, P.h, 0, 128));
-    DM_TRY(map_mn(&mapGYmn, gY + r0 * P.h, P.h, P.m, 1, P.h, 0));
-    DM_TRY(map_mn(&mapXmn, X + r0 * P.h, P.h, P.m, 1, P.h, 0));
-    // dH_i = gY_c . B_i, with the activation backward in the epilogue -> dZ (dG|dU), H
-    {
-      const int variant = P.gated ? dm::GV_BWD_GLU : dm::GV_BWD_ACT;
-      GemmArgs a = gemm_args(variant, P.t, P.m, P.Fi, P.h, 3);
-      a.act = P.act;
-      a.b_bmul = 1;
-      a.in0 = act_save + r0 * P.a_rows;
-      a.ldi = P.a_rows;
-      a.bsi = P.Ri;
-      a.offi = P.Fi;
-      a.out0 = dZ;
-      a.ld0 = P.a_rows;
-      a.bs0 = P.Ri;
-      a.off0 = P.Fi;
-      a.out1 = Hb;
-      a.ld1 = P.F;
-      a.bs1 = P.Fi;
-      // epilogue maps: saved Z (or G, U) of the chunk in, dZ (or dG, dU) and H out; each branch has
-      // its own base so a column tail is clipped at F_i
-      dm::EpiMaps em = {};
-      const uint16_t* save_c = act_save + r0 * P.a_rows;
-      DM_TRY(map_epi_bf16(&em.m[0], save_c, P.Fi, P.m, P.t, P.a_rows, P.Ri));
-      DM_TRY(map_epi_bf16(&em.m[2], dZ, P.Fi, P.m, P.t, P.a_rows, P.Ri));
-      if (P.gated) {
-        DM_TRY(map_epi_bf16(&em.m[1], save_c + P.Fi, P.Fi, P.m, P.t, P.a_rows, P.Ri));
-        DM_TRY(map_epi_bf16(&em.m[3], dZ + P.Fi, P.Fi, P.m, P.t, P.a_rows, P.Ri));
-      }
-      DM_TRY(map_epi_bf16(&em.m[4], Hb, P.Fi, P.m, P.t, P.F, P.Fi));
-      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_H, variant, mapGYk, mapBmn, a, S.comp, &em));
+    SlotRing R;
+    // row chunks in reverse order, as the backward pass runs the forward schedule backwards
+    for (int pc = P.p - 1; pc >= 0; --pc) {
+      const int64_t r0 = pc * P.m;
+      DM_TRY(mlp_chunk_bwd(H, P, S, R, C, X + r0 * P.h, act_save + r0 * P.a_rows, gY + r0 * P.h, gX + r0 * P.h,
+                           gA, gB));
     }
-    // gB_i += gY_c^T . H_i   (D = h x F_i, K = tokens of the chunk)
-    {
-      GemmArgs a = gemm_args(dm::GV_WGRAD, P.t, P.h, P.Fi, P.m, 4);
-      a.b_bmul = 1;
-      a.out0 = gB;
-      a.ld0 = P.Fi;
-      a.bs0 = P.h * P.Fi;
-      DM_TRY(run_gemm(H, DOMINO_K_GEMM_WGRAD_B, dm::GV_WGRAD, mapGYmn, mapHmn, a, S.comp));
-    }
-    // gX partials: P_i = dZ_i . A_i (D = m x n per column chunk), reduced on the reduction stream
-    for (int qc = 0; qc < P.q; ++qc) {
-      int slot;
-      DM_TRY(slot_acquire(H, P, S, R, &slot));
-      float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
-      GemmArgs a = gemm_args(dm::GV_BWD_PARTIAL, P.t, P.m, P.n, P.Ri, 5);
-      a.a_bmul = 1;
-      a.b_row_off = int32_t(qc * P.n);
-      a.b_bmul = 1;
-      a.out0 = part;
-      a.ld0 = P.n;
-      a.bs0 = P.m * P.n;
-      dm::EpiMaps em = {};
-      DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
-      DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, mapDZk, mapAmn, a, S.comp, &em));
-      DM_TRY(slot_handoff(H, S, slot));
-      DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, nullptr, 0, gX + r0 * P.h + qc * P.n, P.h, S.red));
-      DM_TRY(slot_release(H, S, R, slot));
-    }
-    // gA_i += dZ_i^T . X_c (D = R_i x h, K = tokens), overlapping the gX reduction
-    {
-      GemmArgs a = gemm_args(dm::GV_WGRAD, P.t, P.Ri, P.h, P.m, 6);
-      a.a_bmul = 1;
-      a.out0 = gA;
-      a.ld0 = P.h;
-      a.bs0 = P.Ri * P.h;
-      DM_TRY(run_gemm(H, DOMINO_K_GEMM_WGRAD_A, dm::GV_WGRAD, mapDZmn, mapXmn, a, S.comp));
-    }
-  }
-  return DOMINO_OK;
+    return DOMINO_OK;
   }();
   return finish(H, S, caller, st);
 }
@@ -723,6 +855,17 @@ domino_status domino_shard_sum(const float* Pp, int32_t t, int64_t rows, int64_t
   DM_CUDA(dm::launch_shard_sum(Pp, t, rows, cols, residual, ld_res, Y, ld_y, sms * 4,
                                static_cast<cudaStream_t>(stream)),
           "shard-sum launch");
+  return DOMINO_OK;
+}
+
+domino_status domino_act_eval(int32_t act, const float* a, const float* b, float* out, float* da, float* db,
+                              int64_t n, void* stream) {
+  if (act < DOMINO_ACT_NONE || act > DOMINO_ACT_BILINEAR) return fail(DOMINO_ERR_INVALID_ARG, "unknown activation");
+  if (n < 0) return fail(DOMINO_ERR_INVALID_ARG, "n must be >= 0");
+  if (n == 0) return DOMINO_OK;
+  const bool g = gated(act);
+  if (!a || !out || !da || (g && (!b || !db))) return fail(DOMINO_ERR_INVALID_ARG, "NULL vector");
+  DM_CUDA(dm::launch_act_eval(act, a, b, out, da, db, n, static_cast<cudaStream_t>(stream)), "activation launch");
   return DOMINO_OK;
 }
 

@@ -101,7 +101,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // variance of (z - mean), then (z - mean) * rsqrt(var + eps) rounded to bf16.
 __global__ void __launch_bounds__(256) layernorm_kernel(const uint16_t* __restrict__ Z, int64_t rows,
                                                         int64_t h, float eps,
-                                                        uint16_t* __restrict__ out) {
+                                                        uint16_t* __restrict__ out, float* __restrict__ rstd_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (r >= rows) return;
@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const uint16_t* __restri
     for (int e = 0; e < 8; ++e) ss += d[e] * d[e];
   }
   const float rstd = rsqrtf(warp_sum(ss) / static_cast<float>(h) + eps);
+  if (rstd_out && lane == 0) rstd_out[r] = rstd;
   for (int v = lane; v < nv; v += 32) {
     const uint4 w = z[v];
     uint4 y;
@@ -137,10 +138,94 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const uint16_t* __restri
 }
 
 cudaError_t launch_layernorm(const uint16_t* Z, int64_t rows, int64_t h, float eps, uint16_t* out,
-                             cudaStream_t st) {
+                             float* rstd, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int grid = static_cast<int>((rows + 7) / 8);
-  layernorm_kernel<<<grid, 256, 0, st>>>(Z, rows, h, eps, out);
+  layernorm_kernel<<<grid, 256, 0, st>>>(Z, rows, h, eps, out, rstd);
+  return cudaGetLastError();
+}
+
+// Backward of LayerNorm without affine parameters, fused with the residual path, one warp per row:
+//   out = bf16( res + r (gN - mean(gN) - N mean(gN N)) )
+// gN: gradient at the LayerNorm output; N: the (bf16) LayerNorm output; r = 1/sqrt(var + eps) of
+// the forward; res: the gradient arriving through the residual connection.  out may equal res.
+__global__ void __launch_bounds__(256) layernorm_bwd_kernel(const uint16_t* __restrict__ gN,
+                                                            const uint16_t* __restrict__ N,
+                                                            const float* __restrict__ rstd,
+                                                            const uint16_t* res, uint16_t* out, int64_t rows,
+                                                            int64_t h) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (r >= rows) return;
+  const uint4* g = reinterpret_cast<const uint4*>(gN + r * h);
+  const uint4* n = reinterpret_cast<const uint4*>(N + r * h);
+  const int nv = static_cast<int>(h / 8);
+  float sg = 0.0f, sgn = 0.0f;
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 gw = g[v], nw = n[v];
+    const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w}, na[4] = {nw.x, nw.y, nw.z, nw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float g0 = bf16lo(ga[e]), g1 = bf16hi(ga[e]);
+      sg += g0 + g1;
+      sgn += g0 * bf16lo(na[e]) + g1 * bf16hi(na[e]);
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float mg = warp_sum(sg) * inv_h, mgn = warp_sum(sgn) * inv_h;
+  const float rs = rstd[r];
+  const uint4* rr = reinterpret_cast<const uint4*>(res + r * h);
+  uint4* o = reinterpret_cast<uint4*>(out + r * h);
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 gw = g[v], nw = n[v], rw = rr[v];
+    const uint32_t ga[4] = {gw.x, gw.y, gw.z, gw.w}, na[4] = {nw.x, nw.y, nw.z, nw.w},
+                   ra[4] = {rw.x, rw.y, rw.z, rw.w};
+    uint32_t oa[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float d0 = rs * (bf16lo(ga[e]) - mg - bf16lo(na[e]) * mgn);
+      const float d1 = rs * (bf16hi(ga[e]) - mg - bf16hi(na[e]) * mgn);
+      oa[e] = pack_bf16x2(bf16lo(ra[e]) + d0, bf16hi(ra[e]) + d1);
+    }
+    o[v] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+  }
+}
+
+cudaError_t launch_layernorm_bwd(const uint16_t* gN, const uint16_t* N, const float* rstd, const uint16_t* res,
+                                 uint16_t* out, int64_t rows, int64_t h, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const int grid = static_cast<int>((rows + 7) / 8);
+  layernorm_bwd_kernel<<<grid, 256, 0, st>>>(gN, N, rstd, res, out, rows, h);
+  return cudaGetLastError();
+}
+
+// The epilogues' activation functions on a vector: non-gated out = act(a), da = act'(a); gated
+// out = glu(a, b), da = d out / d a, db = d out / d b.
+__global__ void act_eval_kernel(int act, const float* __restrict__ a, const float* __restrict__ b,
+                                float* __restrict__ out, float* __restrict__ da, float* __restrict__ db, int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    if (act == ACT_SWIGLU || act == ACT_BILINEAR) {
+      float dg, du, hv;
+      glu_bwd(act, a[i], b[i], 1.0f, dg, du, hv);
+      out[i] = glu_fwd(act, a[i], b[i]);
+      da[i] = dg;
+      db[i] = du;
+    } else {
+      float hv, d;
+      act_fwd_grad(act, a[i], hv, d);
+      out[i] = act_fwd(act, a[i]);
+      da[i] = d;
+      if (db) db[i] = act_grad(act, a[i]) - d;  // 0 when the two code paths agree
+    }
+  }
+}
+
+cudaError_t launch_act_eval(int act, const float* a, const float* b, float* out, float* da, float* db, int64_t n,
+                            cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int grid = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  act_eval_kernel<<<grid, 256, 0, st>>>(act, a, b, out, da, db, n);
   return cudaGetLastError();
 }
 

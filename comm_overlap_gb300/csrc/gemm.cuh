@@ -296,10 +296,11 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
           glu_bwd(a.act, z0, bf16lo(uw), g0, d1a, d2a, ha);
           glu_bwd(a.act, z1, bf16hi(uw), g1, d1b, d2b, hb);
         } else {
-          d1a = g0 * act_grad(a.act, z0);
-          d1b = g1 * act_grad(a.act, z1);
-          ha = act_fwd(a.act, z0);
-          hb = act_fwd(a.act, z1);
+          float da, db;
+          act_fwd_grad(a.act, z0, ha, da);
+          act_fwd_grad(a.act, z1, hb, db);
+          d1a = g0 * da;
+          d1b = g1 * db;
         }
         o1[e >> 1] = pack_bf16x2(d1a, d1b);
         o2[e >> 1] = pack_bf16x2(d2a, d2b);

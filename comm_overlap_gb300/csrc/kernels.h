@@ -90,7 +90,11 @@ cudaError_t launch_shard_sum(const float* P, int t, int64_t rows, int64_t cols,
                              const uint16_t* res, int64_t ld_res, uint16_t* Y, int64_t ld_y,
                              int grid_cap, cudaStream_t st);
 cudaError_t launch_layernorm(const uint16_t* Z, int64_t rows, int64_t h, float eps, uint16_t* out,
-                             cudaStream_t st);
+                             float* rstd, cudaStream_t st);
+cudaError_t launch_act_eval(int act, const float* a, const float* b, float* out, float* da, float* db, int64_t n,
+                            cudaStream_t st);
+cudaError_t launch_layernorm_bwd(const uint16_t* gN, const uint16_t* N, const float* rstd, const uint16_t* res,
+                                 uint16_t* out, int64_t rows, int64_t h, cudaStream_t st);
 
 // Tensor maps (zero fill out of bounds).  dims[0] is innermost; strides_bytes[i] is the stride of
 // dims[i+1].  elem_bytes: 2 = bf16, 4 = fp32.  swizzle_bytes: 128 or 64.

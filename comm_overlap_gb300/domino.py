@@ -19,11 +19,11 @@ STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTE
           4: "DOMINO_ERR_WORKSPACE", 5: "DOMINO_ERR_CUDA", 6: "DOMINO_ERR_TIMEOUT", 7: "DOMINO_ERR_DEVICE"}
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_SWIGLU, ACT_BILINEAR = 0, 1, 2, 3, 4
 SCHED_SERIAL, SCHED_INTRA, SCHED_INTER = 0, 1, 2
-PASS_FWD, PASS_BWD, PASS_STACK = 0, 1, 2
+PASS_FWD, PASS_BWD, PASS_STACK, PASS_STACK_BWD = 0, 1, 2, 3
 (K_GEMM_FWD1, K_GEMM_FWD2, K_SHARD_SUM, K_LAYERNORM, K_GEMM_DGRAD_H, K_GEMM_WGRAD_B, K_GEMM_DGRAD_X,
- K_GEMM_WGRAD_A) = range(8)
+ K_GEMM_WGRAD_A, K_LN_BWD) = range(9)
 KERNEL_NAMES = ["gemm_fwd1", "gemm_fwd2", "shard_sum", "layernorm", "gemm_dgrad_h", "gemm_wgrad_b",
-                "gemm_dgrad_x", "gemm_wgrad_a"]
+                "gemm_dgrad_x", "gemm_wgrad_a", "layernorm_bwd"]
 
 
 class DominoError(RuntimeError):
@@ -55,8 +55,14 @@ _SIGS = {
     "domino_mlp_bwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "domino_mlp_fwd_noalloc": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P],
     "domino_stack_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "domino_stack_save_size": [ctypes.POINTER(domino_cfg), ctypes.POINTER(ctypes.c_size_t)],
+    "domino_stack_fwd_train": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                               ctypes.c_size_t, _P],
+    "domino_stack_bwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P, _P,
+                         ctypes.c_size_t, _P],
     "domino_shard_sum": [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int64, _P,
                          ctypes.c_int64, _P],
+    "domino_act_eval": [ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int64, _P],
     "domino_device_status": [_P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
     "domino_timing_enable": [_P, ctypes.c_int32],
     "domino_timing_reset": [_P],
@@ -161,8 +167,38 @@ def domino_stack_fwd(handle, cfg, Z_in, A, B, Z_out, workspace, workspace_bytes=
                                   _ptr(workspace), wb, _stream(stream)))
 
 
+def _nbytes(buf, given):
+    if given is not None:
+        return given
+    return 0 if buf is None else buf.numel() * buf.element_size()
+
+
+def domino_stack_save_size(cfg) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().domino_stack_save_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def domino_stack_fwd_train(handle, cfg, Z_in, A, B, Z_out, save, workspace, save_bytes=None, workspace_bytes=None,
+                           stream=None) -> None:
+    _check(lib().domino_stack_fwd_train(handle, ctypes.byref(cfg), _ptr(Z_in), _ptr(A), _ptr(B), _ptr(Z_out),
+                                        _ptr(save), _nbytes(save, save_bytes), _ptr(workspace),
+                                        _nbytes(workspace, workspace_bytes), _stream(stream)))
+
+
+def domino_stack_bwd(handle, cfg, A, B, save, gZ_out, gZ_in, gA, gB, workspace, save_bytes=None,
+                     workspace_bytes=None, stream=None) -> None:
+    _check(lib().domino_stack_bwd(handle, ctypes.byref(cfg), _ptr(A), _ptr(B), _ptr(save), _nbytes(save, save_bytes),
+                                  _ptr(gZ_out), _ptr(gZ_in), _ptr(gA), _ptr(gB), _ptr(workspace),
+                                  _nbytes(workspace, workspace_bytes), _stream(stream)))
+
+
 def domino_shard_sum(P, t, rows, cols, residual, ld_res, Y, ld_y, stream=None) -> None:
     _check(lib().domino_shard_sum(_ptr(P), t, rows, cols, _ptr(residual), ld_res, _ptr(Y), ld_y, _stream(stream)))
+
+
+def domino_act_eval(act, a, b, out, da, db, n, stream=None) -> None:
+    _check(lib().domino_act_eval(act, _ptr(a), _ptr(b), _ptr(out), _ptr(da), _ptr(db), n, _stream(stream)))
 
 
 def domino_device_status(handle) -> tuple[int, int]:

@@ -80,7 +80,12 @@ typedef enum {
  *          reductions of row chunk j of layer l finish (no wait for the whole layer). */
 typedef enum { DOMINO_SCHED_SERIAL = 0, DOMINO_SCHED_INTRA = 1, DOMINO_SCHED_INTER = 2 } domino_sched;
 
-typedef enum { DOMINO_PASS_FWD = 0, DOMINO_PASS_BWD = 1, DOMINO_PASS_STACK = 2 } domino_pass;
+typedef enum {
+  DOMINO_PASS_FWD = 0,       /* domino_mlp_fwd */
+  DOMINO_PASS_BWD = 1,       /* domino_mlp_bwd */
+  DOMINO_PASS_STACK = 2,     /* domino_stack_fwd, domino_stack_fwd_train */
+  DOMINO_PASS_STACK_BWD = 3  /* domino_stack_bwd */
+} domino_pass;
 
 typedef struct {
   int64_t M;      /* tokens (batch x sequence); M % p == 0 */
@@ -156,6 +161,30 @@ DOMINO_API domino_status domino_stack_fwd(domino_handle handle, const domino_cfg
                                const uint16_t* A, const uint16_t* B, uint16_t* Z_out,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Training forward of the layer stack: as domino_stack_fwd, and additionally keeps in `save` what
+ * domino_stack_bwd needs, per layer: the bf16 LayerNorm output (M x h), the bf16 first-linear
+ * output (M x F, or M x 2F gated, laid out as act_save of domino_mlp_fwd) and the fp32
+ * 1/sqrt(var + eps) of every row.  `save` is a 256-byte aligned device buffer of at least
+ * domino_stack_save_size() bytes. */
+DOMINO_API domino_status domino_stack_save_size(const domino_cfg* cfg, size_t* bytes);
+DOMINO_API domino_status domino_stack_fwd_train(domino_handle handle, const domino_cfg* cfg,
+                                                const uint16_t* Z_in, const uint16_t* A, const uint16_t* B,
+                                                uint16_t* Z_out, void* save, size_t save_bytes,
+                                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of the layer stack ("实现与优化" figure 10: the forward schedule in reverse).  From the
+ * gradient gZ_out of the stack output, per layer l = L-1 .. 0 and row chunk (in reverse):
+ *   gN = MLP_l input gradient (domino_mlp_bwd with X = the saved LayerNorm output),
+ *   g  = bf16( g + r (gN - mean(gN) - N mean(gN N)) )   (LayerNorm backward + residual),
+ * with gA, gB (L consecutive layer blocks, fp32) accumulated with +=.  gZ_in (M x h) receives the
+ * gradient of the stack input; it also holds the running gradient between layers.  Workspace:
+ * domino_workspace_size(cfg, DOMINO_PASS_STACK_BWD).  With DOMINO_SCHED_INTER, row chunk j of layer
+ * l-1 starts once row chunk j of layer l has finished its LayerNorm backward. */
+DOMINO_API domino_status domino_stack_bwd(domino_handle handle, const domino_cfg* cfg, const uint16_t* A,
+                                          const uint16_t* B, const void* save, size_t save_bytes,
+                                          const uint16_t* gZ_out, uint16_t* gZ_in, float* gA, float* gB,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* The reduction step alone (the AllReduce stand-in):
  *   Y[r, c] = bf16( (residual[r, c]) + (((P_0[r,c] + P_1[r,c]) + ...) + P_{t-1}[r,c]) )
  * P: t slices of rows x cols fp32, slice i at P + i*rows*cols, row stride cols.
@@ -164,6 +193,13 @@ DOMINO_API domino_status domino_stack_fwd(domino_handle handle, const domino_cfg
 DOMINO_API domino_status domino_shard_sum(const float* P, int32_t t, int64_t rows, int64_t cols,
                                const uint16_t* residual, int64_t ld_res, uint16_t* Y,
                                int64_t ld_y, void* stream);
+
+/* The activation functions exactly as the GEMM epilogues evaluate them, on n fp32 device values:
+ * non-gated: out = act(a), da = act'(a), db (nullable) = 0 when the separate and the combined
+ * derivative code paths agree; gated: out = glu(a, b), da = d out/d a, db = d out/d b (b, db
+ * required).  GeLU uses Phi from erf by Abramowitz & Stegun 7.1.26 (|erf error| <= 1.5e-7). */
+DOMINO_API domino_status domino_act_eval(int32_t act, const float* a, const float* b, float* out, float* da,
+                                         float* db, int64_t n, void* stream);
 
 /* Reads and clears the device error word of every kernel of this library.  *out is
  * DOMINO_OK or DOMINO_ERR_TIMEOUT; *site (nullable) receives the code of the wait that
@@ -182,7 +218,8 @@ typedef enum {
   DOMINO_K_GEMM_WGRAD_B = 5,/* gB += gY^T . H */
   DOMINO_K_GEMM_DGRAD_X = 6,/* dZ_i . A_i -> fp32 shard partials of gX */
   DOMINO_K_GEMM_WGRAD_A = 7,/* gA += dZ^T . X */
-  DOMINO_K_COUNT = 8
+  DOMINO_K_LN_BWD = 8,      /* LayerNorm backward + residual (layer stack) */
+  DOMINO_K_COUNT = 9
 } domino_kernel_kind;
 DOMINO_API domino_status domino_timing_enable(domino_handle handle, int32_t enable);
 DOMINO_API domino_status domino_timing_reset(domino_handle handle);
