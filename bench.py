@@ -230,7 +230,8 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     s = args.shape
-    sched = {"serial": dm.SCHED_SERIAL, "intra": dm.SCHED_INTRA, "inter": dm.SCHED_INTER}[args.sched]
+    sched = {"serial": dm.SCHED_SERIAL, "intra": dm.SCHED_INTRA, "inter": dm.SCHED_INTER,
+             "fused": dm.SCHED_FUSED}[args.sched]
     inp = synth.make_inputs(s, seed=0)
 
     def dev(a):
@@ -477,7 +478,7 @@ def main():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.SHAPES))
-    ap.add_argument("--sched", default="intra", choices=["serial", "intra", "inter"])
+    ap.add_argument("--sched", default="intra", choices=["serial", "intra", "inter", "fused"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pass", dest="pass_", default=None, choices=["fwd", "fwd+bwd"],
                     help="override the workload's pass (profiling aid)")

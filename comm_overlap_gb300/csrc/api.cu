@@ -79,7 +79,7 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
     return fail(DOMINO_ERR_INVALID_ARG, "need M >= 0, h > 0, ffn > 0, t >= 1, p >= 1, q >= 1");
   if (c->act < DOMINO_ACT_NONE || c->act > DOMINO_ACT_BILINEAR)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown activation");
-  if (c->sched < DOMINO_SCHED_SERIAL || c->sched > DOMINO_SCHED_INTER)
+  if (c->sched < DOMINO_SCHED_SERIAL || c->sched > DOMINO_SCHED_FUSED)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
   if (c->M % c->p != 0) return fail(DOMINO_ERR_INVALID_ARG, "M must be divisible by p");
   if (c->h % c->q != 0) return fail(DOMINO_ERR_INVALID_ARG, "h must be divisible by q");
@@ -129,7 +129,13 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
       off = align_up(off + size_t(p.M) * p.h * 2);
     }
   }
-  p.part_slot = align_up(size_t(p.t) * p.m * p.n * 4);
+  // partial slots of t x m x n fp32; the fused schedule needs only one m x n fp32 sum
+  if (p.sched == DOMINO_SCHED_FUSED) {
+    p.nslots = 1;
+    p.part_slot = align_up(size_t(p.m) * p.n * 4);
+  } else {
+    p.part_slot = align_up(size_t(p.t) * p.m * p.n * 4);
+  }
   p.off_part = off;
   off += p.part_slot * p.nslots;
   p.total = off;
@@ -263,10 +269,27 @@ domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap
   if (needs && em == nullptr) return fail(DOMINO_ERR_INVALID_ARG, "internal: GEMM epilogue without its maps");
   static const dm::EpiMaps kNone = {};
   const dm::EpiMaps& e = em ? *em : kNone;
+  const bool fwd_tu = variant <= dm::GV_FWD_PARTIAL || variant == dm::GV_FWD_REDUCE;
   return launch(H, kind, st, "GEMM launch", [&] {
-    return variant <= dm::GV_FWD_PARTIAL ? dm::launch_gemm_fwd(variant, ta, tb, e, a, st)
-                                         : dm::launch_gemm_bwd(variant, ta, tb, e, a, st);
+    return fwd_tu ? dm::launch_gemm_fwd(variant, ta, tb, e, a, st) : dm::launch_gemm_bwd(variant, ta, tb, e, a, st);
   });
+}
+
+// The fused second linear (or input-gradient GEMM) + shard-sum of one column chunk: `Sbuf` is the
+// m x n fp32 sum, `res` (nullable) and `Y` are row-major with leading dimension ld.
+domino_status run_fused_reduce(domino_handle H, int kind, int variant, const Plan& P, const CUtensorMap& ta,
+                               const CUtensorMap& tb, GemmArgs a, float* Sbuf, const uint16_t* res, uint16_t* Y,
+                               int64_t ld, cudaStream_t st) {
+  a.out0 = Sbuf;
+  a.ld0 = P.n;
+  a.bs0 = 0;
+  a.out1 = Y;
+  a.ld1 = ld;
+  a.in0 = res;
+  a.ldi = ld;
+  dm::EpiMaps em = {};
+  DM_TRY(map_f32_out(&em.m[0], Sbuf, P.n, P.m, 1));
+  return run_gemm(H, kind, variant, ta, tb, a, st, &em);
 }
 
 domino_status run_shard_sum(domino_handle H, const float* P, int t, int64_t rows, int64_t cols,
@@ -285,7 +308,8 @@ struct Streams {
 };
 
 domino_status fork(domino_handle H, const Plan& P, cudaStream_t caller, Streams* S) {
-  S->overlap = P.sched != DOMINO_SCHED_SERIAL;
+  // the fused schedule overlaps inside its kernels and runs on the caller's stream
+  S->overlap = P.sched != DOMINO_SCHED_SERIAL && P.sched != DOMINO_SCHED_FUSED;
   if (!S->overlap) {
     S->comp = S->red = caller;
     return DOMINO_OK;
@@ -388,6 +412,15 @@ domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, Sl
   }
   DM_TRY(map_k(&mapH, Hbuf, P.Fi, P.m, P.t, P.F, P.Fi, 128));
   for (int qc = 0; qc < P.q; ++qc) {
+    if (P.sched == DOMINO_SCHED_FUSED) {
+      GemmArgs a = gemm_args(dm::GV_FWD_REDUCE, P.t, P.m, P.n, P.Fi, site + 1);
+      a.a_bmul = 1;
+      a.b_row_off = int32_t(qc * P.n);
+      a.b_bmul = 1;
+      DM_TRY(run_fused_reduce(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_REDUCE, P, mapH, mapB, a, parts,
+                              res_c ? res_c + qc * P.n : nullptr, Yc + qc * P.n, P.h, S.comp));
+      continue;
+    }
     int slot;
     DM_TRY(slot_acquire(H, P, S, R, &slot));
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
@@ -497,6 +530,15 @@ domino_status mlp_chunk_bwd(domino_handle H, const Plan& P, const Streams& S, Sl
   }
   // gX partials: P_i = dZ_i . A_i (D = m x n per column chunk), reduced on the reduction stream
   for (int qc = 0; qc < P.q; ++qc) {
+    if (P.sched == DOMINO_SCHED_FUSED) {
+      GemmArgs a = gemm_args(dm::GV_BWD_REDUCE, P.t, P.m, P.n, P.Ri, 5);
+      a.a_bmul = 1;
+      a.b_row_off = int32_t(qc * P.n);
+      a.b_bmul = 1;
+      DM_TRY(run_fused_reduce(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_REDUCE, P, C.mapDZk, C.mapAmn, a, C.parts,
+                              nullptr, gX_c + qc * P.n, P.h, S.comp));
+      continue;
+    }
     int slot;
     DM_TRY(slot_acquire(H, P, S, R, &slot));
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(C.parts) + P.part_slot * slot);

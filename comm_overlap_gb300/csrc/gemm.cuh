@@ -45,8 +45,11 @@ constexpr int kCtrlBytes = 1024;
 // Block = TMA warp + MMA warp + epilogue warps.
 template <int EPI>
 constexpr int epi_warps() { return 4; }
+// The fused shard-sum adds four finaliser warps (one per lane quarter) after the epilogue warps.
 template <int EPI>
-constexpr int block_threads() { return 64 + 32 * epi_warps<EPI>(); }
+constexpr int fin_warps() { return EPI == EPI_F32_REDUCE ? 4 : 0; }
+template <int EPI>
+constexpr int block_threads() { return 64 + 32 * (epi_warps<EPI>() + fin_warps<EPI>()); }
 // Epilogues that move data with TMA stage it in shared memory, per epilogue warp:
 //  fp32 partials: two 4 KiB buffers (32 rows x 32 fp32, 128-byte swizzle);
 //  activation backward: 4 KiB of inputs (Z or G, U) and 6 KiB of outputs (dZ or dG, dU; H), as
@@ -57,7 +60,7 @@ constexpr int kFwdWarpBytes = 6144;
 constexpr bool is_act_fwd(int epi) { return epi == EPI_ACT_BF16 || epi == EPI_GLU_BF16; }
 template <int EPI>
 constexpr int staging_bytes() {
-  return EPI == EPI_F32_STORE ? 4 * 2 * 4096
+  return (EPI == EPI_F32_STORE || EPI == EPI_F32_REDUCE) ? 4 * 2 * 4096
                               : (is_act_bwd(EPI) ? 4 * kActBwdWarpBytes : (is_act_fwd(EPI) ? 4 * kFwdWarpBytes : 0));
 }
 template <bool PAIR, int EPI>
@@ -81,6 +84,26 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, int& g,
   const int in = r - grp * span;
   mt = first_m + in % gsize;
   nt = in / gsize;
+}
+
+// Sub-tile s (0, 1, ...) of a unit's sequence.  Every variant but the fused shard-sum visits tiles
+// unit, unit + units, ... of the (batch, M, N) tile space; the fused shard-sum visits output tiles
+// unit, unit + units, ... of the (M, N) space and, for each, its `batches` shards in order, so that
+// one unit produces every partial of the tiles it owns.  False past the end of the sequence.
+template <int EPI>
+__device__ __forceinline__ bool tile_at(int s, const GemmArgs& a, int unit, int units, int& g, int& mt, int& nt) {
+  if constexpr (EPI == EPI_F32_REDUCE) {
+    const int ot = unit + (s / a.batches) * units;
+    if (ot >= a.m_tiles * a.n_tiles) return false;
+    decode_tile(ot, a, g, mt, nt);
+    g = s - (s / a.batches) * a.batches;
+    return true;
+  } else {
+    const int tile = unit + s * units;
+    if (tile >= a.batches * a.m_tiles * a.n_tiles) return false;
+    decode_tile(tile, a, g, mt, nt);
+    return true;
+  }
 }
 
 // Bounded wait that ignores the abort flag (used while draining after an abort).
@@ -437,6 +460,122 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtens
   }
 }
 
+// Fused shard-sum epilogue (EPI_F32_REDUCE) of one sub-tile, shard g of an output tile, for the
+// warp's 32 rows, in 32-column chunks staged as in epilogue_f32_tma.  A unit visits the shards of
+// an output tile consecutively, so the warp that handles these rows for shard g handled them for
+// every earlier shard too.  Shard 0 stores its fp32 partial into the sum S (out0, map m[0]); shard
+// g > 0 has the TMA unit add its partial into S at L2, issued only after the warp's writes for
+// shard g-1 completed, so every element of S receives ((P_0 + P_1) + ...) + P_g in shard order,
+// each add rounded to nearest.  After the last shard's adds complete, the rows are handed to the
+// finaliser warp of the same lane quarter (two-slot mbarrier ring `fin_ready` / `fin_done`,
+// counted by `nfin`).  Returns false if a bounded wait gave up.
+template <int NC>
+__device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const EpiMaps& em, uint32_t tacc, int g,
+                                                    int row0, int col0, uint32_t staging, uint32_t& nchunk,
+                                                    uint32_t fin_ready, uint32_t fin_done, uint32_t& nfin,
+                                                    int lane, volatile int* abort_flag, int* err) {
+  if (row0 >= a.M) return true;
+  if (g > 0) {
+    if (lane == 0) bulk_wait_group_all();  // the writes of shard g-1 to these rows have completed
+    __syncwarp();
+  }
+#pragma unroll 1
+  for (int cc = 0; cc < NC; cc += 32) {
+    if (col0 + cc >= a.N) break;
+    const uint32_t buf = staging + (nchunk & 1u) * 4096u;
+    if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
+    __syncwarp();
+    uint32_t r[32];
+    tmem_ld32(tacc + cc, r);
+    tmem_ld_wait();
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u)) << 4), r[4 * j],
+                   r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (g == 0)
+        tma_store_3d(&em.m[0], buf, col0 + cc, row0, 0);
+      else
+        tma_reduce_add_3d(&em.m[0], buf, col0 + cc, row0, 0);
+      bulk_commit_group();
+    }
+    ++nchunk;
+  }
+  if (g < a.batches - 1) return true;
+  const uint32_t slot = nfin & 1u, use = (nfin >> 1) & 1u;
+  ++nfin;
+  bool ok = true;
+  if (lane == 0) {
+    bulk_wait_group_all();       // S holds the full sum for these rows
+    fence_proxy_async_global();  // ... and the finaliser's generic loads come after those writes
+    ok = mbar_wait(fin_done + 8u * slot, use ^ 1u, abort_flag, err, a.err_site + 6);
+    if (ok) mbar_arrive(fin_ready + 8u * slot);
+  }
+  return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+// Finaliser warp of the fused shard-sum: for each output tile of the unit whose rows of this lane
+// quarter are in range, waits until the epilogue warp of the quarter handed the completed sum over,
+// then writes Y = bf16(res + S) (out1 / ld1; residual in0 / ldi, nullable) with coalesced loads and
+// stores (lane l covers columns 8l .. 8l+7 of one row at a time, four rows in flight), and hands
+// the slot back.  It works while the epilogue and MMA warps go on with the next tile's shards.
+__device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, int units, int tile_m, int row_base,
+                                                  uint32_t fin_ready, uint32_t fin_done, int lane,
+                                                  volatile int* abort_flag, int* err) {
+  const int out_tiles = a.m_tiles * a.n_tiles;
+  uint32_t nfin = 0;
+  for (int ot = unit; ot < out_tiles; ot += units) {
+    int g, mt, nt;
+    decode_tile(ot, a, g, mt, nt);
+    const int row0 = mt * tile_m + row_base;
+    if (row0 >= a.M) continue;
+    const uint32_t slot = nfin & 1u, use = (nfin >> 1) & 1u;
+    ++nfin;
+    const bool ok = mbar_wait(fin_ready + 8u * slot, use, abort_flag, err, a.err_site + 7);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return;
+    fence_proxy_async_global();
+    const int c = nt * kBN + lane * 8;
+    const bool col_ok = c < a.N;  // N is a multiple of 8: a lane's 8 columns are all in or all out
+    const float* S = static_cast<const float*>(a.out0);
+    const uint16_t* res = static_cast<const uint16_t*>(a.in0);
+    uint16_t* Y = static_cast<uint16_t*>(a.out1);
+#pragma unroll 1
+    for (int r = 0; r < 32; r += 4) {
+      float4 lo[4], hi[4];
+      uint4 rv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = row0 + r + u;
+        const bool in = col_ok && row < a.M;
+        const float* sp = S + static_cast<int64_t>(row) * a.ld0 + c;
+        lo[u] = in ? __ldcg(reinterpret_cast<const float4*>(sp)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        hi[u] = in ? __ldcg(reinterpret_cast<const float4*>(sp + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        rv[u] = (in && res) ? __ldcg(reinterpret_cast<const uint4*>(res + static_cast<int64_t>(row) * a.ldi + c))
+                            : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = row0 + r + u;
+        if (!(col_ok && row < a.M)) continue;
+        float v[8] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w, hi[u].x, hi[u].y, hi[u].z, hi[u].w};
+        if (res) {
+          // residual first, then the sum, as in the stand-alone shard-sum: res + S, one rounding
+          v[0] = bf16lo(rv[u].x) + v[0]; v[1] = bf16hi(rv[u].x) + v[1];
+          v[2] = bf16lo(rv[u].y) + v[2]; v[3] = bf16hi(rv[u].y) + v[3];
+          v[4] = bf16lo(rv[u].z) + v[4]; v[5] = bf16hi(rv[u].z) + v[5];
+          v[6] = bf16lo(rv[u].w) + v[6]; v[7] = bf16hi(rv[u].w) + v[7];
+        }
+        store8_bf16(Y + static_cast<int64_t>(row) * a.ld1 + c, v);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(fin_done + 8u * slot);
+  }
+}
+
 template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -449,6 +588,9 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
   // barrier indices in the control block
   constexpr int kBarFull = 0, kBarEmpty = S, kBarTmemFull = 2 * S, kBarTmemEmpty = 2 * S + 2,
                 kBarDrain = 2 * S + 4, kBarEpiIn = 2 * S + 5;  // kBarEpiIn: one per epilogue warp
+  // fused shard-sum hand-off, two slots per lane quarter: ready (epilogue -> finaliser), done (back)
+  constexpr int kBarFinReady = kBarEpiIn + epi_warps<EPI>(), kBarFinDone = kBarFinReady + 8;
+  static_assert(8 * (kBarFinDone + 8) <= 512, "barriers overlap the TMEM slot");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -478,6 +620,8 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     }
     mbar_init(bar(kBarDrain), 1);
     for (int e = 0; e < epi_warps<EPI>(); ++e) mbar_init(bar(kBarEpiIn + e), 1);
+    if constexpr (EPI == EPI_F32_REDUCE)
+      for (int i = 0; i < 16; ++i) mbar_init(bar(kBarFinReady + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -485,6 +629,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
     if constexpr (EPI == EPI_F32_STORE) tma_prefetch_map(&em.m[0]);
+    if constexpr (EPI == EPI_F32_REDUCE) tma_prefetch_map(&em.m[0]);
     if constexpr (is_act_fwd(EPI)) {
       tma_prefetch_map(&em.m[0]);
       if (args.out1) tma_prefetch_map(&em.m[1]);
@@ -517,9 +662,8 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       // ---------------- TMA producer (both CTAs of a pair load their own halves)
       uint32_t s = 0, ph = 0, armed = 0, armed_ph = 0;
       bool ok = true;
-      for (int tile = unit; tile < total && ok; tile += units) {
-        int g, mt, nt;
-        decode_tile(tile, args, g, mt, nt);
+      int g, mt, nt;
+      for (int sq = 0; ok && tile_at<EPI>(sq, args, unit, units, g, mt, nt); ++sq) {
         const int m0 = mt * R::kTileM + static_cast<int>(rank) * kBM + args.a_row_off;
         const int n0 = nt * kOutN + args.b_row_off + ((PAIR && !kGatedB) ? static_cast<int>(rank) * 128 : 0);
         const int ga = g * args.a_bmul, gb = g * args.b_bmul;
@@ -592,8 +736,8 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       // ---------------- MMA issuer (the leader CTA of a pair issues for both)
       uint32_t s = 0, ph = 0;
       bool ok = true;
-      int it = 0;
-      for (int tile = unit; tile < total && ok; tile += units, ++it) {
+      int g, mt, nt;
+      for (int it = 0; ok && tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait(bar(kBarTmemEmpty + acc), use ^ 1u, abort_flag, err, args.err_site + 2)) break;
@@ -639,6 +783,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         umma_commit(bar(kBarDrain));
       mbar_wait_drain(bar(kBarDrain), 0);
     }
+  } else if (fin_warps<EPI>() > 0 && warp >= 2 + epi_warps<EPI>()) {
+    // ---------------- finaliser warps of the fused shard-sum (rows of lane quarter warp % 4)
+    const int quarter = warp & 3;
+    finalize_sum_rows(args, unit, units, R::kTileM, static_cast<int>(rank) * kBM + quarter * 32,
+                      bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), lane, abort_flag, err);
   } else {
     // ---------------- epilogue warps 2..: TMEM lane quarter = warp % 4; with 8 epilogue warps,
     // warps 2-5 take the first half of the accumulator's columns and warps 6-9 the second
@@ -648,27 +797,32 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     constexpr int kHalfOut = kOutN / kParts;
     const int row_in_tile = static_cast<int>(rank) * kBM + quarter * 32 + lane;
     const uint32_t staging = stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * 8192u;
-    uint32_t nchunk = 0;
+    uint32_t nchunk = 0, nfin = 0;
     if constexpr (is_act_bwd(EPI)) {
       epilogue_act_bwd_tma<EPI, R::kTileM, kOutN>(
           args, em, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16), bar(kBarTmemFull), bar(kBarTmemEmpty),
           bar(kBarEpiIn + (warp - 2)), stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * kActBwdWarpBytes,
           PAIR, unit, units, total, static_cast<int>(rank) * kBM + quarter * 32, lane, abort_flag, err);
     } else {
-      int it = 0;
-      for (int tile = unit; tile < total; tile += units, ++it) {
+      int g, mt, nt;
+      for (int it = 0; tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         const bool ok = mbar_wait(bar(kBarTmemFull + acc), use, abort_flag, err, args.err_site + 4);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
-        int g, mt, nt;
-        decode_tile(tile, args, g, mt, nt);
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * kBN + half * kHalfOut);
         if constexpr (EPI == EPI_F32_STORE)
           epilogue_f32_tma<kHalfOut>(args, &em.m[0], tacc, g, mt * R::kTileM + row_in_tile - lane,
                                      nt * kOutN + half * kHalfOut, staging, nchunk, lane);
+        else if constexpr (EPI == EPI_F32_REDUCE) {
+          if (!epilogue_f32_reduce<kHalfOut>(args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
+                                             nt * kOutN + half * kHalfOut, staging, nchunk,
+                                             bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), nfin,
+                                             lane, abort_flag, err))
+            break;
+        }
         else if constexpr (is_act_fwd(EPI))
           epilogue_fwd_tma<EPI, kHalfOut>(args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
                                           nt * kOutN + half * kHalfOut,
@@ -686,7 +840,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         }
       }
     }
-    if constexpr (EPI == EPI_F32_STORE || is_act_fwd(EPI)) {
+    if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_REDUCE || is_act_fwd(EPI)) {
       if (lane == 0) bulk_wait_group_all();  // stores done before the staging memory goes away
       __syncwarp();
     }
@@ -744,8 +898,9 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ep
       max_units = sms;
     }
   }
-  const int64_t tiles = int64_t(args.batches) * args.m_tiles * args.n_tiles;
-  if (tiles == 0) return cudaSuccess;
+  // units own whole output tiles (with all their shards) in the fused shard-sum
+  const int64_t tiles = int64_t(EPI == EPI_F32_REDUCE ? 1 : args.batches) * args.m_tiles * args.n_tiles;
+  if (tiles == 0 || args.batches == 0) return cudaSuccess;
   const int units = static_cast<int>(tiles < max_units ? tiles : max_units);
   if constexpr (P) {
     cudaLaunchConfig_t cfg = {};

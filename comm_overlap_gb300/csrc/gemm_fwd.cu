@@ -1,5 +1,5 @@
 // gemm_fwd.cu -- forward GEMM instantiations: first linear (+activation) and second linear
-// (-> fp32 shard partials).
+// (-> fp32 shard partials, or fused with their shard-sum).
 #include "gemm.cuh"
 
 namespace dm {
@@ -12,6 +12,7 @@ cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMa
     case GV_FWD_ACT: return launch_gemm_t<EPI_ACT_BF16, false, false>(ta, tb, em, args, st);
     case GV_FWD_GLU: return launch_gemm_t<EPI_GLU_BF16, false, false>(ta, tb, em, args, st);
     case GV_FWD_PARTIAL: return launch_gemm_t<EPI_F32_STORE, false, false>(ta, tb, em, args, st);
+    case GV_FWD_REDUCE: return launch_gemm_t<EPI_F32_REDUCE, false, false>(ta, tb, em, args, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -28,6 +28,8 @@ enum GemmEpi : int {
   EPI_F32_ACCUM = 3, // out0 += D (fp32)
   EPI_ACT_BWD = 4,   // in0 = Z: out0 = bf16(D * act'(Z)); out1 = bf16(act(Z))
   EPI_GLU_BWD = 5,   // in0: G at +0, U at +offi: out0: dG at +0, dU at +off0; out1 = bf16(glu(G, U))
+  EPI_F32_REDUCE = 6 // batch g = shard, the shards of a tile in order: S (fp32, out0) = P_0, S += P_g;
+                     //   then out1 = bf16(in0 + S) (residual in0 nullable)
 };
 
 // The kernel instantiations the library uses.  A/B operand majorness: K = K-major
@@ -40,7 +42,9 @@ enum GemmVariant : int {
   GV_BWD_GLU = 4,     // dH with gated backward:      EPI_GLU_BWD,   A K, B MN
   GV_BWD_PARTIAL = 5, // dX partials:                 EPI_F32_STORE, A K, B MN
   GV_WGRAD = 6,       // weight gradients (+=):       EPI_F32_ACCUM, A MN, B MN
-  GV_COUNT = 7
+  GV_FWD_REDUCE = 7,  // second linear + shard-sum:   EPI_F32_REDUCE, A K, B K
+  GV_BWD_REDUCE = 8,  // dX partials + shard-sum:     EPI_F32_REDUCE, A K, B MN
+  GV_COUNT = 9
 };
 
 // Per-launch GEMM description.  D[g] (M x N per batch g) = A_op[g] . B_op[g]^T.
@@ -70,6 +74,8 @@ int gemm_out_tile_n(int variant);  // 128 for GV_FWD_GLU, else 256
 //  activation-backward variants (GV_BWD_ACT, GV_BWD_GLU), all bf16 with 64-byte swizzle and
 //    (F_i, M, shards) extents: m[0] saved Z or G (read), m[1] saved U (read, gated),
 //    m[2] dZ or dG (written), m[3] dU (written, gated), m[4] recomputed H (written).
+//  fused shard-sum variants (GV_FWD_REDUCE, GV_BWD_REDUCE): m[0] = fp32 sum S (N, M, 1), 128-byte
+//    swizzle (TMA stores and reduce-adds).
 //  Other variants ignore the maps.
 struct EpiMaps {
   CUtensorMap m[5];

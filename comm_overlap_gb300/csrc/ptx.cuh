@@ -109,6 +109,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
+// Element-wise add of a shared-memory box into global memory, performed by the TMA unit at L2
+// (the tensor map's element type, here fp32).  Same box, swizzle and clipping as tma_store_3d.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
+                                                  int32_t c2) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed bulk groups are still reading their shared-memory source.
@@ -124,6 +134,10 @@ __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.b
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// Orders this thread's later generic-proxy global accesses after async-proxy (TMA) writes to global
+// memory that have completed.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;

@@ -18,7 +18,7 @@ DOMINO_OK = 0
 STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTED", 3: "DOMINO_ERR_ALIGNMENT",
           4: "DOMINO_ERR_WORKSPACE", 5: "DOMINO_ERR_CUDA", 6: "DOMINO_ERR_TIMEOUT", 7: "DOMINO_ERR_DEVICE"}
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_SWIGLU, ACT_BILINEAR = 0, 1, 2, 3, 4
-SCHED_SERIAL, SCHED_INTRA, SCHED_INTER = 0, 1, 2
+SCHED_SERIAL, SCHED_INTRA, SCHED_INTER, SCHED_FUSED = 0, 1, 2, 3
 PASS_FWD, PASS_BWD, PASS_STACK, PASS_STACK_BWD = 0, 1, 2, 3
 (K_GEMM_FWD1, K_GEMM_FWD2, K_SHARD_SUM, K_LAYERNORM, K_GEMM_DGRAD_H, K_GEMM_WGRAD_B, K_GEMM_DGRAD_X,
  K_GEMM_WGRAD_A, K_LN_BWD) = range(9)

@@ -77,8 +77,22 @@ typedef enum {
  *  SERIAL: every kernel on the caller's stream, no overlap (the naive TP order).
  *  INTRA : reduction of chunk k on a side stream, overlapping the GEMMs of chunk k+1.
  *  INTER : as INTRA; in the layer stack, row chunk j of layer l+1 starts as soon as the
- *          reductions of row chunk j of layer l finish (no wait for the whole layer). */
-typedef enum { DOMINO_SCHED_SERIAL = 0, DOMINO_SCHED_INTRA = 1, DOMINO_SCHED_INTER = 2 } domino_sched;
+ *          reductions of row chunk j of layer l finish (no wait for the whole layer).
+ *  FUSED : the reduction is overlapped at tile granularity inside the second linear (and the
+ *          input-gradient GEMM of the backward), the one-GPU analogue of GEMM + reduce-scatter
+ *          tile pipelining ("04 · TP/SP 的通信-计算 overlap 与工程优化" §3, userbuffers): one
+ *          persistent kernel computes, per output tile, the t shard partials in shard order;
+ *          each leaves the SM as an fp32 tile that the TMA unit adds into an fp32 sum at L2
+ *          (shard 0 stores, shard i > 0 adds after shard i-1's adds completed), and the last
+ *          shard's epilogue rounds the sum (plus the residual) once to bf16.  Same arithmetic
+ *          and order as the other schedules; everything runs on the caller's stream; the
+ *          workspace holds one m x n fp32 sum instead of the partial slots. */
+typedef enum {
+  DOMINO_SCHED_SERIAL = 0,
+  DOMINO_SCHED_INTRA = 1,
+  DOMINO_SCHED_INTER = 2,
+  DOMINO_SCHED_FUSED = 3
+} domino_sched;
 
 typedef enum {
   DOMINO_PASS_FWD = 0,       /* domino_mlp_fwd */
