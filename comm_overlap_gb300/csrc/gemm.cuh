@@ -496,10 +496,12 @@ __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const Epi
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
+      // the sum stays in L2 until its tile is finalised
+      const uint64_t keep = l2_policy_evict_last();
       if (g == 0)
-        tma_store_3d(&em.m[0], buf, col0 + cc, row0, 0);
+        tma_store_3d_hint(&em.m[0], buf, col0 + cc, row0, 0, keep);
       else
-        tma_reduce_add_3d(&em.m[0], buf, col0 + cc, row0, 0);
+        tma_reduce_add_3d_hint(&em.m[0], buf, col0 + cc, row0, 0, keep);
       bulk_commit_group();
     }
     ++nchunk;
@@ -522,6 +524,8 @@ __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const Epi
 // then writes Y = bf16(res + S) (out1 / ld1; residual in0 / ldi, nullable) with coalesced loads and
 // stores (lane l covers columns 8l .. 8l+7 of one row at a time, four rows in flight), and hands
 // the slot back.  It works while the epilogue and MMA warps go on with the next tile's shards.
+// When S rows are whole 128-byte lines (ld0 % 32 == 0), every line of the tile belongs to this
+// tile alone, and once read it is dropped from L2 without a write-back: S is scratch.
 __device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, int units, int tile_m, int row_base,
                                                   uint32_t fin_ready, uint32_t fin_done, int lane,
                                                   volatile int* abort_flag, int* err) {
@@ -542,6 +546,7 @@ __device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, i
     const float* S = static_cast<const float*>(a.out0);
     const uint16_t* res = static_cast<const uint16_t*>(a.in0);
     uint16_t* Y = static_cast<uint16_t*>(a.out1);
+    const bool drop = (a.ld0 & 31) == 0 && (lane & 3) == 0;  // lanes 0, 4, ... start a 128-byte line
 #pragma unroll 1
     for (int r = 0; r < 32; r += 4) {
       float4 lo[4], hi[4];
@@ -569,6 +574,14 @@ __device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, i
           v[6] = bf16lo(rv[u].w) + v[6]; v[7] = bf16hi(rv[u].w) + v[7];
         }
         store8_bf16(Y + static_cast<int64_t>(row) * a.ld1 + c, v);
+      }
+      __syncwarp();  // every lane has its values before a line is dropped
+      if (drop) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int row = row0 + r + u;
+          if (col_ok && row < a.M) discard_l2_line(S + static_cast<int64_t>(row) * a.ld0 + c);
+        }
       }
     }
     __syncwarp();
