@@ -225,12 +225,12 @@ DOMINO_API domino_status domino_device_status(domino_handle handle, domino_statu
  * kernel kind, the number of launches and their summed duration since the last reset. */
 typedef enum {
   DOMINO_K_GEMM_FWD1 = 0,   /* first linear + activation epilogue */
-  DOMINO_K_GEMM_FWD2 = 1,   /* second linear -> fp32 shard partials */
+  DOMINO_K_GEMM_FWD2 = 1,   /* second linear -> fp32 shard partials (FUSED: + shard-sum) */
   DOMINO_K_SHARD_SUM = 2,   /* shard-sum (AllReduce stand-in) */
   DOMINO_K_LAYERNORM = 3,
   DOMINO_K_GEMM_DGRAD_H = 4,/* gY . Bfull with activation-backward epilogue */
   DOMINO_K_GEMM_WGRAD_B = 5,/* gB += gY^T . H */
-  DOMINO_K_GEMM_DGRAD_X = 6,/* dZ_i . A_i -> fp32 shard partials of gX */
+  DOMINO_K_GEMM_DGRAD_X = 6,/* dZ_i . A_i -> fp32 shard partials of gX (FUSED: + shard-sum) */
   DOMINO_K_GEMM_WGRAD_A = 7,/* gA += dZ^T . X */
   DOMINO_K_LN_BWD = 8,      /* LayerNorm backward + residual (layer stack) */
   DOMINO_K_COUNT = 9
