@@ -33,6 +33,7 @@ GATED = (ACT_SWIGLU, ACT_BILINEAR)
 
 # tensor ids used to derive independent sub-streams
 TID_X, TID_A, TID_B, TID_GY, TID_GA0, TID_GB0, TID_MISC = 1, 2, 3, 4, 5, 6, 7
+TID_WQKV, TID_WO = 8, 9  # attention sublayer weights
 
 
 def _rng(seed: int, tid: int, layer: int = 0) -> np.random.Generator:

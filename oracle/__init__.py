@@ -55,6 +55,11 @@ def lib():
             for name in ("oracle_glu", "oracle_glu_dg", "oracle_glu_du"):
                 getattr(L, name).argtypes = [_I, _D, _D]
                 getattr(L, name).restype = _D
+            L.oracle_attn_fwd_bf16.argtypes = [_I64, _I64, _I, _I64, _I, _P, _P, _P, _P, _I64, _I, _P]
+            L.oracle_attn_fwd_bf16.restype = _I
+            L.oracle_block_fwd_bf16.argtypes = [_I, _I64, _I64, _I64, _I, _I64, _I, _I, _D, _P, _P, _P, _P, _P, _P,
+                                                _I64, _I64, _P]
+            L.oracle_block_fwd_bf16.restype = _I
             L.oracle_num_threads.restype = _I
             _lib = L
     return _lib
@@ -179,6 +184,46 @@ def stack_bwd(Z, A, B, gZ, t, act, eps=1e-5, rows=None, want_w=False):
     if rc != 0:
         raise ValueError(f"oracle_stack_bwd failed ({rc})")
     return gZ0, dA, dB
+
+
+def attn_fwd(X, Wqkv, Wo, t, heads, seq, rows=None, sharded=False):
+    """Attention sublayer Y = sum over heads of causal attention(X) . Wo^T (no residual).
+
+    X: M x h bf16 bits (sequences of `seq` consecutive tokens); Wqkv: (3h) x h as t shards of
+    (3 h/t) x h (query heads, key heads, value heads); Wo: t x h x (h/t).  Returns n_rows x h.
+    """
+    X, Wqkv, Wo = (np.ascontiguousarray(a) for a in (X, Wqkv, Wo))
+    assert X.dtype == np.uint16 and Wqkv.dtype == np.uint16 and Wo.dtype == np.uint16
+    M, h = X.shape
+    r, n = _rows(rows)
+    Y = np.empty((n if r is not None else M, h), np.float64)
+    rc = lib().oracle_attn_fwd_bf16(M, h, heads, seq, t, _ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(r), n, int(sharded),
+                                    _ptr(Y))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd failed ({rc})")
+    return Y
+
+
+def block_fwd(Z, Wqkv, Wo, A, B, t, heads, seq, act, eps=1e-5, seqs=None, upto=None):
+    """Pre-LN transformer block stack, L = Wqkv.shape[0] layers of Z += Attn(LN(Z)); Z += MLP(LN(Z)).
+
+    Returns the selected sequences' positions 0 .. upto-1: n_seqs x upto x h (all sequences and
+    positions by default).  Per-layer weights stacked on axis 0: Wqkv L x 3h x h, Wo L x t x h x h/t,
+    A L x a_rows x h, B L x t x h x F/t.
+    """
+    Z, Wqkv, Wo, A, B = (np.ascontiguousarray(a) for a in (Z, Wqkv, Wo, A, B))
+    M, h = Z.shape
+    L = Wqkv.shape[0]
+    F = B.shape[1] * B.shape[3]
+    upto = seq if upto is None else int(upto)
+    sq, ns = _rows(seqs)
+    n_out = ns if sq is not None else M // seq
+    out = np.empty((n_out, upto, h), np.float64)
+    rc = lib().oracle_block_fwd_bf16(L, M, h, F, heads, seq, t, act, eps, _ptr(Z), _ptr(Wqkv), _ptr(Wo), _ptr(A),
+                                     _ptr(B), _ptr(sq), ns, upto, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_block_fwd failed ({rc})")
+    return out
 
 
 def act(a, z):

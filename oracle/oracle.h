@@ -1,5 +1,5 @@
 /*
- * oracle.h -- CPU oracle for the chunked tensor-parallel MLP (test infrastructure).
+ * oracle.h -- CPU oracle for the chunked tensor-parallel MLP and attention (test infrastructure).
  *
  * This library is test infrastructure.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg load it.  It shares no code, header, table or constant
@@ -96,6 +96,24 @@ int oracle_stack_bwd_bf16(int L, int64_t M, int64_t h, int64_t F, int t, int act
 int oracle_stack_bwd_f64(int L, int64_t M, int64_t h, int64_t F, int t, int act, double eps,
                          const double* Z0, const double* A, const double* B, const double* gZL,
                          const int64_t* rows, int64_t n_rows, double* gZ0, double* dA, double* dB);
+
+/* Attention sublayer (oracle_attn.c): causal multi-head self-attention within sequences of `seq`
+ * tokens (M % seq == 0, token r at position r % seq), heads split over t shards, then the output
+ * projection; Y (n_rows x h) = sum over heads of attention(X) . Wo^T, no residual.  sharded = 1
+ * forms each shard's partial and sums them in shard order.  Layouts in oracle_attn.c. */
+int oracle_attn_fwd_bf16(int64_t M, int64_t h, int heads, int64_t seq, int t, const uint16_t* X,
+                         const uint16_t* Wqkv, const uint16_t* Wo, const int64_t* rows, int64_t n_rows,
+                         int sharded, double* Y);
+
+/* Pre-LN transformer block stack (oracle_attn.c), L layers of
+ *   Z += Attn(LN(Z));  Z += MLP(LN(Z))
+ * evaluated for the sequences seqs[n_seqs] (NULL: all M / seq), positions 0 .. upto-1 of each
+ * (causality makes the prefix independent of later positions).  Zout: n_seqs x upto x h.
+ * Per-layer weights: Wqkv (3h x h as t shards), Wo (h x h as t shards), A and B as the MLP. */
+int oracle_block_fwd_bf16(int L, int64_t M, int64_t h, int64_t F, int heads, int64_t seq, int t, int act,
+                          double eps, const uint16_t* Z0, const uint16_t* Wqkv, const uint16_t* Wo,
+                          const uint16_t* A, const uint16_t* B, const int64_t* seqs, int64_t n_seqs,
+                          int64_t upto, double* Zout);
 
 /* Elementwise helpers, exposed so tests can pin them against special values. */
 double oracle_act(int act, double z);        /* non-gated activations */
