@@ -163,12 +163,17 @@ def kernel_work(s: synth.MlpShape):
         "gemm_dgrad_x": ("tensor", 2.0 * m * (2 * s.F if s.gated else s.F) * n),
         "gemm_wgrad_a": ("tensor", 2.0 * m * (2 * s.F if s.gated else s.F) * s.h),
         "layernorm_bwd": ("hbm", 4.0 * m * s.h * 2.0 + m * 4.0),
+        "gemm_qkv": ("tensor", 2.0 * m * s.h * 3 * s.h),
+        # q.k and p.v over the visible (causal) key positions: 4 d per pair, seq (seq + 1) / 2 pairs
+        # per sequence and head
+        "attention": ("tensor", 4.0 * s.h * m * (s.seq + 1) / 2.0),
+        "gemm_oproj": ("tensor", 2.0 * m * s.h * n),
     }
 
 
 def config_json(s: synth.MlpShape, sched: str, n_gpus: int):
     return {"workload": s.name, "M": s.M, "batch": s.batch, "seq": s.seq, "h": s.h, "ffn": s.F,
-            "act": ACT_NAMES[s.act], "t": s.t, "p": s.p, "q": s.q, "layers": s.layers,
+            "act": ACT_NAMES[s.act], "t": s.t, "p": s.p, "q": s.q, "layers": s.layers, "heads": s.heads,
             "layernorm": s.layernorm, "pass": "fwd+bwd" if s.backward else "fwd", "sched": sched,
             "seed": 0, "l2": "inputs larger than L2 (129 MB); no flush needed",
             "parallelism": "replicas" if n_gpus > 1 else "single GPU, t shards emulated in HBM"}
@@ -187,7 +192,14 @@ def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
     rows = synth.sample_indices(s.M, n_fwd, 1)
     flops = 0.0
     t0 = time.perf_counter()
-    if s.layernorm:
+    if s.attention:
+        # causality: the first positions of one sequence do not depend on the rest of it
+        upto = max(2, int(round(12 * scale)))
+        oracle.block_fwd(X, inp["Wqkv"], inp["Wo"], A, B, s.t, s.heads, s.seq, s.act, 1e-5, seqs=[0], upto=upto)
+        attn_row = 2.0 * s.h * 4 * s.h + 4.0 * s.h * (upto + 1) / 2.0
+        flops += upto * (fwd_row + attn_row) * s.layers
+        what = f"the first {upto} positions of one sequence through all {s.layers} blocks"
+    elif s.layernorm:
         oracle.stack_fwd(X, A, B, s.t, s.act, 1e-5, rows=rows)
         flops += len(rows) * fwd_row * s.layers
         what = f"{len(rows)} token rows through all {s.layers} layers"
@@ -240,8 +252,13 @@ def run_ours(args, rank, world, local_rank):
     X, A, B = dev(inp["X"]), dev(inp["A"]), dev(inp["B"])
     gY = dev(inp["gY"]) if s.backward else None
     h = dm.domino_create()
-    cfg = dm.make_cfg(s.M, s.h, s.F, s.t, s.p, s.q, s.act, sched=sched, layers=s.layers, ln_eps=1e-5)
-    if s.layernorm:
+    cfg = dm.make_cfg(s.M, s.h, s.F, s.t, s.p, s.q, s.act, sched=sched, layers=s.layers, ln_eps=1e-5,
+                      heads=s.heads, seq=s.seq if s.attention else 0)
+    Wqkv = dev(inp["Wqkv"]) if s.attention else None
+    Wo = dev(inp["Wo"]) if s.attention else None
+    if s.attention:
+        wsb = dm.domino_workspace_size(cfg, dm.PASS_BLOCK)
+    elif s.layernorm:
         wsb = max(dm.domino_workspace_size(cfg, dm.PASS_STACK),
                   dm.domino_workspace_size(cfg, dm.PASS_STACK_BWD) if s.backward else 0)
     else:
@@ -260,6 +277,9 @@ def run_ours(args, rank, world, local_rank):
     def step_on(st, Xin, gYin, Yout=None, gXout=None):
         Yout = Y if Yout is None else Yout
         gXout = gX if gXout is None else gXout
+        if s.attention:
+            dm.domino_block_fwd(h, cfg, Xin, Wqkv, Wo, A, B, Yout, ws, wsb, st)
+            return
         if s.layernorm:
             if s.backward:
                 dm.domino_stack_fwd_train(h, cfg, Xin, A, B, Yout, save, ws, None, wsb, st)

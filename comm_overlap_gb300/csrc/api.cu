@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -63,10 +64,12 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 struct Plan {
   int64_t M, h, F, Fi, m, n, a_rows, Ri;
   int t, p, q, act, sched, layers, nslots;
+  int heads = 0, seq = 0;  // attention passes
   float eps;
   bool gated;
   // workspace offsets
   size_t off_h = 0, off_ln = 0, off_dz = 0, off_hb = 0, off_gn = 0, off_part = 0, part_slot = 0, total = 0;
+  size_t off_qkv = 0, off_o = 0;  // attention: fused projection output (m x 3h), attention output (m x h)
   // layer-stack save buffer (training forward -> backward): per layer the LayerNorm output N
   // (M x h bf16), the first-linear output (M x a_rows bf16) and 1/sqrt(var + eps) (M fp32)
   size_t save_n = 0, save_act = 0, save_rstd = 0, save_layer = 0;
@@ -75,7 +78,7 @@ struct Plan {
 domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   if (!c) return fail(DOMINO_ERR_INVALID_ARG, "cfg is NULL");
   if (c->flags != 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->flags must be 0");
-  if (c->M < 0 || c->h <= 0 || c->ffn <= 0 || c->t < 1 || c->p < 1 || c->q < 1)
+  if (c->M < 0 || c->h <= 0 || (pass != DOMINO_PASS_ATTN && c->ffn <= 0) || c->t < 1 || c->p < 1 || c->q < 1)
     return fail(DOMINO_ERR_INVALID_ARG, "need M >= 0, h > 0, ffn > 0, t >= 1, p >= 1, q >= 1");
   if (c->act < DOMINO_ACT_NONE || c->act > DOMINO_ACT_BILINEAR)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown activation");
@@ -83,20 +86,40 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
     return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
   if (c->M % c->p != 0) return fail(DOMINO_ERR_INVALID_ARG, "M must be divisible by p");
   if (c->h % c->q != 0) return fail(DOMINO_ERR_INVALID_ARG, "h must be divisible by q");
-  if (c->ffn % c->t != 0) return fail(DOMINO_ERR_INVALID_ARG, "ffn must be divisible by t");
-  const int64_t Fi = c->ffn / c->t;
+  const bool attn = pass == DOMINO_PASS_ATTN || pass == DOMINO_PASS_BLOCK;
+  const bool mlp = pass != DOMINO_PASS_ATTN;
+  if (mlp && c->ffn % c->t != 0) return fail(DOMINO_ERR_INVALID_ARG, "ffn must be divisible by t");
+  const int64_t Fi = mlp ? c->ffn / c->t : 8;
   if (c->h % 8 != 0 || Fi % 8 != 0 || (c->h / c->q) % 8 != 0)
     return fail(DOMINO_ERR_ALIGNMENT, "h, ffn/t and h/q must be multiples of 8 (16-byte rows)");
+  if (attn) {
+    if (c->heads < 1 || c->seq < 1) return fail(DOMINO_ERR_INVALID_ARG, "attention needs heads >= 1 and seq >= 1");
+    if (c->h % c->heads != 0 || c->heads % c->t != 0)
+      return fail(DOMINO_ERR_INVALID_ARG, "need h % heads == 0 and heads % t == 0");
+    if (c->h / c->heads != 128) return fail(DOMINO_ERR_UNSUPPORTED, "head dimension h / heads must be 128");
+    if ((c->M / c->p) % c->seq != 0)
+      return fail(DOMINO_ERR_INVALID_ARG, "row chunks must hold whole sequences: M % (p * seq) == 0");
+    if (c->heads > 65535 || (c->M / c->p) / c->seq > 65535)
+      return fail(DOMINO_ERR_UNSUPPORTED, "more heads or sequences per chunk than one launch covers");
+  }
   if (c->M > (int64_t(1) << 31) - 1 || c->h > (int64_t(1) << 20) || c->ffn > (int64_t(1) << 24))
     return fail(DOMINO_ERR_UNSUPPORTED, "size beyond the supported range");
   if (pass == DOMINO_PASS_STACK || pass == DOMINO_PASS_STACK_BWD) {
     if (c->layers < 1) return fail(DOMINO_ERR_INVALID_ARG, "layers must be >= 1");
     if (!(c->ln_eps > 0.0f)) return fail(DOMINO_ERR_INVALID_ARG, "ln_eps must be > 0");
   }
-  if (pass < DOMINO_PASS_FWD || pass > DOMINO_PASS_STACK_BWD) return fail(DOMINO_ERR_INVALID_ARG, "bad pass");
+  if (pass < DOMINO_PASS_FWD || pass > DOMINO_PASS_BLOCK) return fail(DOMINO_ERR_INVALID_ARG, "bad pass");
+  if (pass == DOMINO_PASS_BLOCK) {
+    if (c->layers < 1) return fail(DOMINO_ERR_INVALID_ARG, "layers must be >= 1");
+    if (!(c->ln_eps > 0.0f)) return fail(DOMINO_ERR_INVALID_ARG, "ln_eps must be > 0");
+  }
   Plan& p = *P;
   p.M = c->M; p.h = c->h; p.F = c->ffn; p.Fi = Fi; p.t = c->t; p.p = c->p; p.q = c->q;
   p.act = c->act; p.sched = c->sched; p.layers = c->layers; p.eps = c->ln_eps;
+  if (attn) {
+    p.heads = c->heads;
+    p.seq = c->seq;
+  }
   p.gated = gated(c->act);
   p.m = c->M / c->p;
   p.n = c->h / c->q;
@@ -112,7 +135,18 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
     p.total = 0;
     return DOMINO_OK;
   }
-  if (pass == DOMINO_PASS_FWD || pass == DOMINO_PASS_STACK) {
+  if (attn) {
+    p.off_qkv = off;
+    off = align_up(off + size_t(p.m) * 3 * p.h * 2);
+    p.off_o = off;
+    off = align_up(off + size_t(p.m) * p.h * 2);
+    if (pass == DOMINO_PASS_BLOCK) {
+      p.off_ln = off;
+      off = align_up(off + size_t(p.m) * p.h * 2);
+      p.off_h = off;
+      off = align_up(off + size_t(p.m) * p.F * 2);
+    }
+  } else if (pass == DOMINO_PASS_FWD || pass == DOMINO_PASS_STACK) {
     p.off_h = off;
     off = align_up(off + size_t(p.m) * p.F * 2);
     if (pass == DOMINO_PASS_STACK) {
@@ -376,6 +410,45 @@ domino_status ready(domino_handle H) {
   return DOMINO_OK;
 }
 
+// ---- the row-parallel second linear of a sublayer for one row chunk: per column chunk the t shard
+// partials P_i = H_i . B_i^T (reduction length Kc per shard) into a partial slot on the compute
+// stream and their shard-sum (+ residual res_c) into Yc on the reduction stream, or both in one
+// kernel with the fused schedule.  mapH: (Kc, m, t) view of the chunk's shard inputs; mapB: the
+// shards' weights (Kc, h, t).
+domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, int kind,
+                            const CUtensorMap& mapH, const CUtensorMap& mapB, int64_t Kc, float* parts,
+                            const uint16_t* res_c, uint16_t* Yc, int site) {
+  for (int qc = 0; qc < P.q; ++qc) {
+    if (P.sched == DOMINO_SCHED_FUSED) {
+      GemmArgs a = gemm_args(dm::GV_FWD_REDUCE, P.t, P.m, P.n, Kc, site);
+      a.a_bmul = 1;
+      a.b_row_off = int32_t(qc * P.n);
+      a.b_bmul = 1;
+      DM_TRY(run_fused_reduce(H, kind, dm::GV_FWD_REDUCE, P, mapH, mapB, a, parts,
+                              res_c ? res_c + qc * P.n : nullptr, Yc + qc * P.n, P.h, S.comp));
+      continue;
+    }
+    int slot;
+    DM_TRY(slot_acquire(H, P, S, R, &slot));
+    float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
+    GemmArgs a = gemm_args(dm::GV_FWD_PARTIAL, P.t, P.m, P.n, Kc, site);
+    a.a_bmul = 1;
+    a.b_row_off = int32_t(qc * P.n);
+    a.b_bmul = 1;
+    a.out0 = part;
+    a.ld0 = P.n;
+    a.bs0 = P.m * P.n;
+    dm::EpiMaps em = {};
+    DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
+    DM_TRY(run_gemm(H, kind, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp, &em));
+    DM_TRY(slot_handoff(H, S, slot));
+    DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, res_c ? res_c + qc * P.n : nullptr, P.h,
+                         Yc + qc * P.n, P.h, S.red));
+    DM_TRY(slot_release(H, S, R, slot));
+  }
+  return DOMINO_OK;
+}
+
 // ---- forward of one MLP for row chunk pc: first linear into H, then the q column chunks of the
 // second linear into partial slots, each followed by its shard-sum on the reduction stream.
 domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, SlotRing& R,
@@ -411,35 +484,7 @@ domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, Sl
     DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD1, variant, mapX, mapA, a, S.comp, &em));
   }
   DM_TRY(map_k(&mapH, Hbuf, P.Fi, P.m, P.t, P.F, P.Fi, 128));
-  for (int qc = 0; qc < P.q; ++qc) {
-    if (P.sched == DOMINO_SCHED_FUSED) {
-      GemmArgs a = gemm_args(dm::GV_FWD_REDUCE, P.t, P.m, P.n, P.Fi, site + 1);
-      a.a_bmul = 1;
-      a.b_row_off = int32_t(qc * P.n);
-      a.b_bmul = 1;
-      DM_TRY(run_fused_reduce(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_REDUCE, P, mapH, mapB, a, parts,
-                              res_c ? res_c + qc * P.n : nullptr, Yc + qc * P.n, P.h, S.comp));
-      continue;
-    }
-    int slot;
-    DM_TRY(slot_acquire(H, P, S, R, &slot));
-    float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
-    GemmArgs a = gemm_args(dm::GV_FWD_PARTIAL, P.t, P.m, P.n, P.Fi, site + 1);
-    a.a_bmul = 1;
-    a.b_row_off = int32_t(qc * P.n);
-    a.b_bmul = 1;
-    a.out0 = part;
-    a.ld0 = P.n;
-    a.bs0 = P.m * P.n;
-    dm::EpiMaps em = {};
-    DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
-    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD2, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp, &em));
-    DM_TRY(slot_handoff(H, S, slot));
-    DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, res_c ? res_c + qc * P.n : nullptr, P.h,
-                         Yc + qc * P.n, P.h, S.red));
-    DM_TRY(slot_release(H, S, R, slot));
-  }
-  return DOMINO_OK;
+  return second_linear(H, P, S, R, DOMINO_K_GEMM_FWD2, mapH, mapB, P.Fi, parts, res_c, Yc, site + 1);
 }
 
 domino_status weight_maps_fwd(const Plan& P, const uint16_t* A, const uint16_t* B, CUtensorMap* mapA,
@@ -619,6 +664,119 @@ domino_status stack_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_i
         }));
         DM_TRY(mlp_chunk_fwd(H, P, S, R, n_c, mapA, mapB, Hbuf, parts, act_c, src + r0 * P.h, Z_out + r0 * P.h, 2));
         if (S.overlap) DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
+      }
+    }
+    return DOMINO_OK;
+  }();
+  return finish(H, S, caller, st);
+}
+
+// ---- attention sublayer ----------------------------------------------------------------------
+
+// Tensor maps of the attention kernel for one row chunk: QKV (head dim, 3 * heads slots, position,
+// sequence) and O (head dim, heads, position, sequence), 128-byte swizzle.
+domino_status attn_maps(const Plan& P, const uint16_t* QKV, const uint16_t* O, CUtensorMap* tq, CUtensorMap* to) {
+  const uint64_t nseq = uint64_t(P.m / P.seq);
+  std::string err;
+  {
+    const uint64_t dims[4] = {128, uint64_t(3 * P.heads), uint64_t(P.seq), nseq};
+    const uint64_t strides[3] = {256, uint64_t(3 * P.h) * 2, uint64_t(P.seq) * uint64_t(3 * P.h) * 2};
+    const uint32_t box[4] = {64, 1, 128, 1};
+    if (!dm::make_map(tq, 2, QKV, 4, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
+  }
+  {
+    const uint64_t dims[4] = {128, uint64_t(P.heads), uint64_t(P.seq), nseq};
+    const uint64_t strides[3] = {256, uint64_t(P.h) * 2, uint64_t(P.seq) * uint64_t(P.h) * 2};
+    const uint32_t box[4] = {64, 1, 32, 1};
+    if (!dm::make_map(to, 2, O, 4, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
+  }
+  return DOMINO_OK;
+}
+
+// Weight maps of one attention sublayer: Wqkv (h, 3h) K-major; Wo shards (h/t, h, t) like B.
+domino_status weight_maps_attn(const Plan& P, const uint16_t* Wqkv, const uint16_t* Wo, CUtensorMap* mapW,
+                               CUtensorMap* mapO) {
+  const int64_t Kc = P.h / P.t;
+  DM_TRY(map_k(mapW, Wqkv, P.h, 3 * P.h, 1, P.h, 0, dm::kBBoxRows));
+  DM_TRY(map_k(mapO, Wo, Kc, P.h, P.t, Kc, P.h * Kc, dm::kBBoxRows));
+  return DOMINO_OK;
+}
+
+// Attention sublayer for one row chunk Xc (m rows = whole sequences): the fused projection
+// QKV = Xc . Wqkv^T (every shard's query, key and value heads), causal attention per (query block,
+// head, sequence) into O, then the row-parallel output projection with its shard-sum (+ residual)
+// exactly as the MLP's second linear, with O_i (the shard's heads) in place of H_i.
+domino_status attn_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, const uint16_t* Xc,
+                             const CUtensorMap& mapW, const CUtensorMap& mapWo, uint16_t* QKV, uint16_t* O,
+                             float* parts, const uint16_t* res_c, uint16_t* Yc) {
+  CUtensorMap mapX;
+  DM_TRY(map_k(&mapX, Xc, P.h, P.m, 1, P.h, 0, 128));
+  {
+    GemmArgs a = gemm_args(dm::GV_FWD_ACT, 1, P.m, 3 * P.h, P.h, 7);
+    a.act = DOMINO_ACT_NONE;
+    a.out0 = QKV;
+    a.ld0 = 3 * P.h;
+    dm::EpiMaps em = {};
+    DM_TRY(map_epi_bf16(&em.m[0], QKV, 3 * P.h, P.m, 1, 3 * P.h, 0));
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_QKV, dm::GV_FWD_ACT, mapX, mapW, a, S.comp, &em));
+  }
+  {
+    CUtensorMap tq, to;
+    DM_TRY(attn_maps(P, QKV, O, &tq, &to));
+    dm::AttnArgs aa;
+    aa.seq = P.seq;
+    aa.heads = P.heads;
+    aa.nhi = P.heads / P.t;
+    aa.n_qblk = int32_t(cdiv(P.seq, 128));
+    aa.scale_log2 = float(1.4426950408889634 / std::sqrt(128.0));
+    aa.err_site = 8 << 4;
+    DM_TRY(launch(H, DOMINO_K_ATTN, S.comp, "attention launch",
+                  [&] { return dm::launch_attention(tq, to, aa, int(P.m / P.seq), S.comp); }));
+  }
+  const int64_t Kc = P.h / P.t;
+  CUtensorMap mapO;
+  DM_TRY(map_k(&mapO, O, Kc, P.m, P.t, P.h, Kc, 128));
+  return second_linear(H, P, S, R, DOMINO_K_GEMM_OPROJ, mapO, mapWo, Kc, parts, res_c, Yc, 9);
+}
+
+// Stack of pre-LN Transformer blocks: sublayers attention, MLP, attention, ... each over all row
+// chunks, each chunk waiting (INTER) for the same chunk of the previous sublayer or (INTRA) for
+// the whole previous sublayer before its LayerNorm.
+domino_status block_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_in, const uint16_t* Wqkv,
+                             const uint16_t* Wo, const uint16_t* A, const uint16_t* B, uint16_t* Z_out, void* ws,
+                             cudaStream_t caller) {
+  DM_TRY(ensure_row_events(H, P.p));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* QKV = reinterpret_cast<uint16_t*>(w + P.off_qkv);
+  uint16_t* O = reinterpret_cast<uint16_t*>(w + P.off_o);
+  uint16_t* lnbuf = reinterpret_cast<uint16_t*>(w + P.off_ln);
+  uint16_t* Hbuf = reinterpret_cast<uint16_t*>(w + P.off_h);
+  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  Streams S;
+  DM_TRY(fork(H, P, caller, &S));
+  const domino_status st = [&]() -> domino_status {
+    SlotRing R;
+    const int64_t qkv_layer = 3 * P.h * P.h, o_layer = P.h * P.h;
+    const int64_t a_layer = P.a_rows * P.h, b_layer = P.h * P.F;
+    for (int l = 0; l < P.layers; ++l) {
+      CUtensorMap mapW, mapWo, mapA, mapB;
+      DM_TRY(weight_maps_attn(P, Wqkv + l * qkv_layer, Wo + l * o_layer, &mapW, &mapWo));
+      DM_TRY(weight_maps_fwd(P, A + l * a_layer, B + l * b_layer, &mapA, &mapB));
+      for (int sub = 0; sub < 2; ++sub) {
+        const uint16_t* src = (l == 0 && sub == 0) ? Z_in : Z_out;
+        for (int pc = 0; pc < P.p; ++pc) {
+          const int64_t r0 = pc * P.m;
+          if (l > 0 || sub > 0) DM_TRY(wait_previous_layer(H, P, S, pc, pc == 0));
+          DM_TRY(launch(H, DOMINO_K_LAYERNORM, S.comp, "LayerNorm launch", [&] {
+            return dm::launch_layernorm(src + r0 * P.h, P.m, P.h, P.eps, lnbuf, nullptr, S.comp);
+          }));
+          if (sub == 0)
+            DM_TRY(attn_chunk_fwd(H, P, S, R, lnbuf, mapW, mapWo, QKV, O, parts, src + r0 * P.h, Z_out + r0 * P.h));
+          else
+            DM_TRY(mlp_chunk_fwd(H, P, S, R, lnbuf, mapA, mapB, Hbuf, parts, nullptr, src + r0 * P.h,
+                                 Z_out + r0 * P.h, 2));
+          if (S.overlap) DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
+        }
       }
     }
     return DOMINO_OK;
@@ -878,6 +1036,55 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
   return finish(H, S, caller, st);
 }
 
+domino_status domino_attn_fwd(domino_handle H, const domino_cfg* cfg, const uint16_t* X, const uint16_t* Wqkv,
+                              const uint16_t* Wo, uint16_t* Y, void* ws, size_t ws_bytes, void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_ATTN, &P));
+  DM_TRY(check_ptr(X, "X"));
+  DM_TRY(check_ptr(Wqkv, "Wqkv"));
+  DM_TRY(check_ptr(Wo, "Wo"));
+  DM_TRY(check_ptr(Y, "Y"));
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  CUtensorMap mapW, mapWo;
+  DM_TRY(weight_maps_attn(P, Wqkv, Wo, &mapW, &mapWo));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* QKV = reinterpret_cast<uint16_t*>(w + P.off_qkv);
+  uint16_t* O = reinterpret_cast<uint16_t*>(w + P.off_o);
+  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  Streams S;
+  DM_TRY(fork(H, P, caller, &S));
+  const domino_status st = [&]() -> domino_status {
+    SlotRing R;
+    for (int pc = 0; pc < P.p; ++pc) {
+      const int64_t r0 = pc * P.m;
+      DM_TRY(attn_chunk_fwd(H, P, S, R, X + r0 * P.h, mapW, mapWo, QKV, O, parts, nullptr, Y + r0 * P.h));
+    }
+    return DOMINO_OK;
+  }();
+  return finish(H, S, caller, st);
+}
+
+domino_status domino_block_fwd(domino_handle H, const domino_cfg* cfg, const uint16_t* Z_in, const uint16_t* Wqkv,
+                               const uint16_t* Wo, const uint16_t* A, const uint16_t* B, uint16_t* Z_out, void* ws,
+                               size_t ws_bytes, void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_BLOCK, &P));
+  DM_TRY(check_ptr(Z_in, "Z_in"));
+  DM_TRY(check_ptr(Wqkv, "Wqkv"));
+  DM_TRY(check_ptr(Wo, "Wo"));
+  DM_TRY(check_ptr(A, "A"));
+  DM_TRY(check_ptr(B, "B"));
+  DM_TRY(check_ptr(Z_out, "Z_out"));
+  if (Z_out == Z_in) return fail(DOMINO_ERR_INVALID_ARG, "Z_out may not alias Z_in");
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  return block_fwd_impl(H, P, Z_in, Wqkv, Wo, A, B, Z_out, ws, static_cast<cudaStream_t>(stream));
+}
+
 domino_status domino_shard_sum(const float* Pp, int32_t t, int64_t rows, int64_t cols,
                                const uint16_t* residual, int64_t ld_res, uint16_t* Y, int64_t ld_y,
                                void* stream) {
@@ -915,10 +1122,11 @@ domino_status domino_device_status(domino_handle H, domino_status* out, int32_t*
   DM_TRY(ready(H));
   if (!out) return fail(DOMINO_ERR_INVALID_ARG, "out is NULL");
   DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-  int c1 = 0, c2 = 0;
+  int c1 = 0, c2 = 0, c3 = 0;
   DM_CUDA(dm::take_gemm_fwd_error(&c1), "reading the device error word");
   DM_CUDA(dm::take_gemm_bwd_error(&c2), "reading the device error word");
-  const int code = c1 ? c1 : c2;
+  DM_CUDA(dm::take_attn_error(&c3), "reading the device error word");
+  const int code = c1 ? c1 : (c2 ? c2 : c3);
   *out = code ? DOMINO_ERR_TIMEOUT : DOMINO_OK;
   if (site) *site = code;
   return DOMINO_OK;

@@ -91,6 +91,23 @@ cudaError_t launch_wait_selftest(uint64_t timeout_ns, int site, cudaStream_t st)
 cudaError_t take_gemm_fwd_error(int* code);
 cudaError_t take_gemm_bwd_error(int* code);
 
+// Causal multi-head self-attention of one row chunk (attention.cu), head dimension 128.  QKV: the
+// fused projection output, per token the t shards' [query heads | key heads | value heads], head
+// slot (shard * 3 + which) * nhi + local head; O: per token the heads in global order.  Maps:
+// tm_qkv 4-D (128, 3 * heads, seq, sequences), box (64, 1, 128, 1); tm_o 4-D (128, heads, seq,
+// sequences), box (64, 1, 32, 1); both bf16 with 128-byte swizzle.
+struct AttnArgs {
+  int32_t seq;       // tokens per sequence
+  int32_t heads;     // heads in total
+  int32_t nhi;       // heads per shard
+  int32_t n_qblk;    // query blocks of 128 per sequence
+  float scale_log2;  // log2(e) / sqrt(head dimension)
+  int32_t err_site;
+};
+cudaError_t launch_attention(const CUtensorMap& tm_qkv, const CUtensorMap& tm_o, const AttnArgs& a, int nseq,
+                             cudaStream_t st);
+cudaError_t take_attn_error(int* code);
+
 // Shard-sum (AllReduce stand-in) and LayerNorm.
 cudaError_t launch_shard_sum(const float* P, int t, int64_t rows, int64_t cols,
                              const uint16_t* res, int64_t ld_res, uint16_t* Y, int64_t ld_y,

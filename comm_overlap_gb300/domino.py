@@ -19,11 +19,11 @@ STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTE
           4: "DOMINO_ERR_WORKSPACE", 5: "DOMINO_ERR_CUDA", 6: "DOMINO_ERR_TIMEOUT", 7: "DOMINO_ERR_DEVICE"}
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_SWIGLU, ACT_BILINEAR = 0, 1, 2, 3, 4
 SCHED_SERIAL, SCHED_INTRA, SCHED_INTER, SCHED_FUSED = 0, 1, 2, 3
-PASS_FWD, PASS_BWD, PASS_STACK, PASS_STACK_BWD = 0, 1, 2, 3
+PASS_FWD, PASS_BWD, PASS_STACK, PASS_STACK_BWD, PASS_ATTN, PASS_BLOCK = 0, 1, 2, 3, 4, 5
 (K_GEMM_FWD1, K_GEMM_FWD2, K_SHARD_SUM, K_LAYERNORM, K_GEMM_DGRAD_H, K_GEMM_WGRAD_B, K_GEMM_DGRAD_X,
- K_GEMM_WGRAD_A, K_LN_BWD) = range(9)
+ K_GEMM_WGRAD_A, K_LN_BWD, K_GEMM_QKV, K_ATTN, K_GEMM_OPROJ) = range(12)
 KERNEL_NAMES = ["gemm_fwd1", "gemm_fwd2", "shard_sum", "layernorm", "gemm_dgrad_h", "gemm_wgrad_b",
-                "gemm_dgrad_x", "gemm_wgrad_a", "layernorm_bwd"]
+                "gemm_dgrad_x", "gemm_wgrad_a", "layernorm_bwd", "gemm_qkv", "attention", "gemm_oproj"]
 
 
 class DominoError(RuntimeError):
@@ -35,11 +35,13 @@ class DominoError(RuntimeError):
 class domino_cfg(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("h", ctypes.c_int64), ("ffn", ctypes.c_int64), ("t", ctypes.c_int32),
                 ("p", ctypes.c_int32), ("q", ctypes.c_int32), ("act", ctypes.c_int32), ("sched", ctypes.c_int32),
-                ("layers", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("flags", ctypes.c_int32)]
+                ("layers", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("flags", ctypes.c_int32),
+                ("heads", ctypes.c_int32), ("seq", ctypes.c_int32)]
 
 
-def make_cfg(M, h, ffn, t, p=1, q=1, act=ACT_GELU, sched=SCHED_INTRA, layers=1, ln_eps=1e-5, flags=0) -> domino_cfg:
-    return domino_cfg(M, h, ffn, t, p, q, act, sched, layers, ln_eps, flags)
+def make_cfg(M, h, ffn, t, p=1, q=1, act=ACT_GELU, sched=SCHED_INTRA, layers=1, ln_eps=1e-5, flags=0, heads=0,
+             seq=0) -> domino_cfg:
+    return domino_cfg(M, h, ffn, t, p, q, act, sched, layers, ln_eps, flags, heads, seq)
 
 
 _lib = None
@@ -60,6 +62,8 @@ _SIGS = {
                                ctypes.c_size_t, _P],
     "domino_stack_bwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P, _P,
                          ctypes.c_size_t, _P],
+    "domino_attn_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "domino_block_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "domino_shard_sum": [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int64, _P,
                          ctypes.c_int64, _P],
     "domino_act_eval": [ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int64, _P],
@@ -171,6 +175,17 @@ def _nbytes(buf, given):
     if given is not None:
         return given
     return 0 if buf is None else buf.numel() * buf.element_size()
+
+
+def domino_attn_fwd(handle, cfg, X, Wqkv, Wo, Y, workspace, workspace_bytes=None, stream=None) -> None:
+    _check(lib().domino_attn_fwd(handle, ctypes.byref(cfg), _ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(Y), _ptr(workspace),
+                                 _nbytes(workspace, workspace_bytes), _stream(stream)))
+
+
+def domino_block_fwd(handle, cfg, Z_in, Wqkv, Wo, A, B, Z_out, workspace, workspace_bytes=None, stream=None) -> None:
+    _check(lib().domino_block_fwd(handle, ctypes.byref(cfg), _ptr(Z_in), _ptr(Wqkv), _ptr(Wo), _ptr(A), _ptr(B),
+                                  _ptr(Z_out), _ptr(workspace), _nbytes(workspace, workspace_bytes),
+                                  _stream(stream)))
 
 
 def domino_stack_save_size(cfg) -> int:

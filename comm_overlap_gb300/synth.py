@@ -126,6 +126,7 @@ class MlpShape:
     seq: int = 0
     x_std: float = 1.0
     w_std: float = 0.02
+    heads: int = 0            # > 0: Transformer blocks (attention sublayer before each MLP)
 
     @property
     def Fi(self) -> int:
@@ -140,9 +141,22 @@ class MlpShape:
         """Rows of all A shards together (2F for gated activations)."""
         return 2 * self.F if self.gated else self.F
 
+    @property
+    def attention(self) -> bool:
+        return self.heads > 0
+
+    def attn_flops(self) -> float:
+        """Flops of one attention sublayer: the QKV and output projections (2 M h 3h + 2 M h h) and
+        the causal attention, 4 M d per visible key-query pair summed over heads (q.k and p.v),
+        i.e. 4 h M (seq + 1) / 2 for a full sequence."""
+        if not self.attention:
+            return 0.0
+        core = 4.0 * self.h * self.M * (self.seq + 1) / 2.0
+        return 2.0 * self.M * self.h * 3 * self.h + 2.0 * self.M * self.h * self.h + core
+
     def gemm_flops(self) -> float:
-        """Dense GEMM flops of one pass: forward, plus backward (2x) if enabled."""
-        fwd = 2.0 * self.M * self.h * self.a_rows + 2.0 * self.M * self.F * self.h
+        """Dense GEMM (and attention) flops of one pass: forward, plus backward (2x) if enabled."""
+        fwd = 2.0 * self.M * self.h * self.a_rows + 2.0 * self.M * self.F * self.h + self.attn_flops()
         return self.layers * fwd * (3.0 if self.backward else 1.0)
 
 
@@ -156,13 +170,17 @@ SHAPES = {
                                  layernorm=True, batch=16, seq=2048),
     "llama3_8b_swiglu_fwdbwd": MlpShape("llama3_8b_swiglu_fwdbwd", 32768, 4096, 14336, ACT_SWIGLU, 8, 2, 1,
                                         backward=True, batch=8, seq=4096),
+    # the GPT-3 6.7B stack with its attention sublayers (32 heads of 128): full Transformer blocks
+    "gpt3_6.7b_block4": MlpShape("gpt3_6.7b_block4", 32768, 4096, 16384, ACT_GELU, 4, 2, 2, layers=4,
+                                 layernorm=True, batch=16, seq=2048, heads=32),
 }
 
 
 def make_inputs(s: MlpShape, seed: int = 0, integer: bool = False, layers: int | None = None) -> dict:
     """Seeded inputs for shape ``s`` as bf16 bit arrays (uint16).
 
-    Keys: X [M,h]; A [L, t*(2)F_i, h]; B [L, t, h, F_i]; gY [M,h] if backward.
+    Keys: X [M,h]; A [L, t*(2)F_i, h]; B [L, t, h, F_i]; gY [M,h] if backward; for attention
+    shapes Wqkv [L, 3h, h] (t shards of query, key and value heads) and Wo [L, t, h, h/t].
     ``integer=True`` draws every tensor from {-1, 0, +1}.
     """
     L = s.layers if layers is None else layers
@@ -179,6 +197,10 @@ def make_inputs(s: MlpShape, seed: int = 0, integer: bool = False, layers: int |
         out["B"] = np.stack([normal_bf16((s.t, s.h, s.Fi), 0.0, s.w_std, seed, TID_B, l) for l in range(L)])
         if s.backward:
             out["gY"] = normal_bf16((s.M, s.h), 0.0, 1.0, seed, TID_GY)
+        if s.attention:
+            out["Wqkv"] = np.stack([normal_bf16((3 * s.h, s.h), 0.0, s.w_std, seed, TID_WQKV, l) for l in range(L)])
+            out["Wo"] = np.stack([normal_bf16((s.t, s.h, s.h // s.t), 0.0, s.w_std, seed, TID_WO, l)
+                                  for l in range(L)])
     return out
 
 

@@ -98,7 +98,9 @@ typedef enum {
   DOMINO_PASS_FWD = 0,       /* domino_mlp_fwd */
   DOMINO_PASS_BWD = 1,       /* domino_mlp_bwd */
   DOMINO_PASS_STACK = 2,     /* domino_stack_fwd, domino_stack_fwd_train */
-  DOMINO_PASS_STACK_BWD = 3  /* domino_stack_bwd */
+  DOMINO_PASS_STACK_BWD = 3, /* domino_stack_bwd */
+  DOMINO_PASS_ATTN = 4,      /* domino_attn_fwd */
+  DOMINO_PASS_BLOCK = 5      /* domino_block_fwd */
 } domino_pass;
 
 typedef struct {
@@ -113,6 +115,8 @@ typedef struct {
   int32_t layers; /* domino_stack_fwd only: number of layers (>= 1) */
   float ln_eps;   /* domino_stack_fwd only: LayerNorm epsilon (> 0) */
   int32_t flags;  /* reserved, must be 0 */
+  int32_t heads;  /* attention passes only: attention heads, h / heads == 128, heads % t == 0 */
+  int32_t seq;    /* attention passes only: tokens per sequence; M % (p * seq) == 0 */
 } domino_cfg;
 
 typedef struct domino_handle_s* domino_handle;
@@ -199,6 +203,41 @@ DOMINO_API domino_status domino_stack_bwd(domino_handle handle, const domino_cfg
                                           const uint16_t* gZ_out, uint16_t* gZ_in, float* gA, float* gB,
                                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Attention sublayer of one Transformer block ("TP 的数据依赖：通信为何难以隐藏": for the attention
+ * layer of XAB=Y, X is the input, A the multi-head attention and B a linear layer; the AllReduce
+ * follows):
+ *   Y = sum_i Attn_i(X) . Wo_i^T,   Attn_i = causal self-attention of shard i's heads,
+ * heads split over the t shards (Megatron style), with the same chunking (p row chunks holding
+ * whole sequences, q column chunks of the output projection), schedules and fp32 shard-sum as
+ * domino_mlp_fwd; bf16 output rounded once.  Per head (d = h / heads = 128): q, k, v = X . W^T,
+ * o = softmax(q k^T / sqrt(d) over positions <= the query's, within its sequence) v.
+ *   X:    M x h bf16; token r is position r % seq of sequence r / seq.
+ *   Wqkv: t shards of (3 h/t) x h, each [query heads; key heads; value heads] of the shard, d rows
+ *         per head, nn.Linear [out, in] layout.
+ *   Wo:   t shards of h x (h/t); column j*d + e of shard i multiplies element e of its head j.
+ * cfg->heads and cfg->seq are required; cfg->ffn and cfg->act are ignored.  Unsupported head
+ * dimensions return DOMINO_ERR_UNSUPPORTED.  Workspace: domino_workspace_size(cfg,
+ * DOMINO_PASS_ATTN). */
+DOMINO_API domino_status domino_attn_fwd(domino_handle handle, const domino_cfg* cfg, const uint16_t* X,
+                                         const uint16_t* Wqkv, const uint16_t* Wo, uint16_t* Y, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/* Stack of cfg->layers pre-LN Transformer blocks ("实现与优化", figure 9: one self-attention layer
+ * and one MLP layer per block, LayerNorm and residual between them):
+ *   Z += Attn(LN(Z));  Z += MLP(LN(Z))
+ * LayerNorm as in domino_stack_fwd; the attention sublayer as in domino_attn_fwd, the MLP as in
+ * domino_mlp_fwd; each sublayer's residual is added in fp32 to its shard-sum before the one bf16
+ * rounding.  Per-layer weights are consecutive blocks: Wqkv (3h x h), Wo (h x h as t shards), A
+ * and B as in domino_stack_fwd.  The sublayers run in the order attention (all row chunks), MLP
+ * (all row chunks), next layer; with INTER a row chunk of one sublayer starts as soon as the
+ * reductions of the same row chunk of the previous sublayer are done (the fig-9 interleaving:
+ * a chunk's reduction overlaps the next chunk's compute).  Z_in is not modified; Z_out may not
+ * alias it.  Workspace: domino_workspace_size(cfg, DOMINO_PASS_BLOCK). */
+DOMINO_API domino_status domino_block_fwd(domino_handle handle, const domino_cfg* cfg, const uint16_t* Z_in,
+                                          const uint16_t* Wqkv, const uint16_t* Wo, const uint16_t* A,
+                                          const uint16_t* B, uint16_t* Z_out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
 /* The reduction step alone (the AllReduce stand-in):
  *   Y[r, c] = bf16( (residual[r, c]) + (((P_0[r,c] + P_1[r,c]) + ...) + P_{t-1}[r,c]) )
  * P: t slices of rows x cols fp32, slice i at P + i*rows*cols, row stride cols.
@@ -233,7 +272,10 @@ typedef enum {
   DOMINO_K_GEMM_DGRAD_X = 6,/* dZ_i . A_i -> fp32 shard partials of gX (FUSED: + shard-sum) */
   DOMINO_K_GEMM_WGRAD_A = 7,/* gA += dZ^T . X */
   DOMINO_K_LN_BWD = 8,      /* LayerNorm backward + residual (layer stack) */
-  DOMINO_K_COUNT = 9
+  DOMINO_K_GEMM_QKV = 9,    /* fused query/key/value projection of the attention sublayer */
+  DOMINO_K_ATTN = 10,       /* causal multi-head attention */
+  DOMINO_K_GEMM_OPROJ = 11, /* attention output projection -> fp32 shard partials (FUSED: + shard-sum) */
+  DOMINO_K_COUNT = 12
 } domino_kernel_kind;
 DOMINO_API domino_status domino_timing_enable(domino_handle handle, int32_t enable);
 DOMINO_API domino_status domino_timing_reset(domino_handle handle);
