@@ -108,6 +108,16 @@ def normal_f32(shape, mean: float, std: float, seed: int, tid: int, layer: int =
     return x.reshape(shape)
 
 
+def e4m3_codes(shape, std: float, scale: float, seed: int, tid: int, layer: int = 0) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) of N(0, std) draws stored with per-tensor scale ``scale``: the draw
+    divided by the scale, clipped to the largest finite magnitude 448, cast by PyTorch's
+    float8_e4m3fn conversion (nearest, ties to even)."""
+    import torch
+    v = normal_f32(shape, 0.0, std, seed, tid, layer) / np.float32(scale)
+    v = np.clip(v, -448.0, 448.0).astype(np.float32)
+    return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
 @dataclasses.dataclass(frozen=True)
 class MlpShape:
     """One workload of the chunked tensor-parallel MLP."""

@@ -60,6 +60,12 @@ def lib():
             L.oracle_block_fwd_bf16.argtypes = [_I, _I64, _I64, _I64, _I, _I64, _I, _I, _D, _P, _P, _P, _P, _P, _P,
                                                 _I64, _I64, _P]
             L.oracle_block_fwd_bf16.restype = _I
+            L.oracle_mlp_fwd_fp8.argtypes = [_I64, _I64, _I64, _I, _I, _P, _P, _P, _D, _D, _D, _D, _P, _I64, _P, _P]
+            L.oracle_mlp_fwd_fp8.restype = _I
+            L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_decode.restype = _D
+            L.oracle_e4m3_encode.argtypes = [_D]
+            L.oracle_e4m3_encode.restype = ctypes.c_uint8
             L.oracle_num_threads.restype = _I
             _lib = L
     return _lib
@@ -224,6 +230,36 @@ def block_fwd(Z, Wqkv, Wo, A, B, t, heads, seq, act, eps=1e-5, seqs=None, upto=N
     if rc != 0:
         raise ValueError(f"oracle_block_fwd failed ({rc})")
     return out
+
+
+def mlp_fwd_fp8(X8, A8, B8, t, act, scales, rows=None, return_h8=False):
+    """FP8 forward: E4M3 codes (uint8) in the MLP layouts, scales = (sx, sa, sb, sh).  Returns Y
+    (n_rows x h, double) and, with return_h8, the E4M3 codes of the quantised first-linear output."""
+    X8, A8, B8 = (np.ascontiguousarray(a, dtype=np.uint8) for a in (X8, A8, B8))
+    M, h = X8.shape
+    F = B8.shape[-1] * t
+    r, n = _rows(rows)
+    n_out = n if r is not None else M
+    Y = np.empty((n_out, h), np.float64)
+    H8 = np.empty((n_out, F), np.uint8) if return_h8 else None
+    sx, sa, sb, sh = (float(v) for v in scales)
+    rc = lib().oracle_mlp_fwd_fp8(M, h, F, t, act, _ptr(X8), _ptr(A8), _ptr(B8), sx, sa, sb, sh, _ptr(r), n,
+                                  _ptr(Y), _ptr(H8))
+    if rc != 0:
+        raise ValueError(f"oracle_mlp_fwd_fp8 failed ({rc})")
+    return (Y, H8) if return_h8 else Y
+
+
+def e4m3_decode(codes):
+    f = lib().oracle_e4m3_decode
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([f(int(v)) for v in c.ravel()]).reshape(c.shape)
+
+
+def e4m3_encode(x):
+    f = lib().oracle_e4m3_encode
+    a = np.asarray(x, dtype=np.float64)
+    return np.array([f(float(v)) for v in a.ravel()], dtype=np.uint8).reshape(a.shape)
 
 
 def act(a, z):

@@ -1,4 +1,4 @@
-"""Builds the CPU oracle (oracle.c, oracle_attn.c) into liboracle.so next to this file.
+"""Builds the CPU oracle (oracle.c, oracle_attn.c, oracle_fp8.c) into liboracle.so next to this file.
 
 Test infrastructure: plain gcc, no CUDA.  ``-ffp-contract=off`` keeps the double
 arithmetic free of fused multiply-adds so x86 and Arm hosts round identically.
@@ -10,7 +10,7 @@ import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SOURCES = ["oracle.c", "oracle_core.inc", "oracle_attn.c", "oracle.h"]
+SOURCES = ["oracle.c", "oracle_core.inc", "oracle_attn.c", "oracle_fp8.c", "oracle.h"]
 LIB = os.path.join(HERE, "liboracle.so")
 
 
@@ -25,7 +25,8 @@ def build(force: bool = False) -> str:
     if force or needs_build():
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=gnu11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-               "-Wall", "-o", tmp, os.path.join(HERE, "oracle.c"), os.path.join(HERE, "oracle_attn.c"), "-lm"]
+               "-Wall", "-o", tmp, os.path.join(HERE, "oracle.c"), os.path.join(HERE, "oracle_attn.c"),
+               os.path.join(HERE, "oracle_fp8.c"), "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, LIB)
     return LIB

@@ -115,6 +115,17 @@ int oracle_block_fwd_bf16(int L, int64_t M, int64_t h, int64_t F, int heads, int
                           const uint16_t* A, const uint16_t* B, const int64_t* seqs, int64_t n_seqs,
                           int64_t upto, double* Zout);
 
+/* FP8 variant of the MLP forward (oracle_fp8.c): E4M3 operands X8 (M x h), A8, B8 (the MLP
+ * layouts) with per-tensor scales sx, sa, sb; H re-quantised to E4M3 with scale sh; Y (n_rows x h)
+ * = sh sb (H8 . B8^T) in double.  H8_out (nullable): the n_rows x F codes of H8. */
+int oracle_mlp_fwd_fp8(int64_t M, int64_t h, int64_t F, int t, int act, const uint8_t* X8, const uint8_t* A8,
+                       const uint8_t* B8, double sx, double sa, double sb, double sh, const int64_t* rows,
+                       int64_t n_rows, double* Y, uint8_t* H8_out);
+/* E4M3 code <-> value: decode exactly; encode an fp32 value to the nearest, ties to even, saturating
+ * at +-448; NaN -> 0x7F. */
+double oracle_e4m3_decode(uint8_t code);
+uint8_t oracle_e4m3_encode(double x);
+
 /* Elementwise helpers, exposed so tests can pin them against special values. */
 double oracle_act(int act, double z);        /* non-gated activations */
 double oracle_act_grad(int act, double z);
