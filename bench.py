@@ -228,6 +228,28 @@ def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
     return flops, dt, what
 
 
+def fp8_inputs(s: synth.MlpShape) -> dict:
+    """E4M3 codes of the workload's draws with power-of-two per-tensor scales: X ~ N(0, 1) at 2^-6,
+    the weights ~ N(0, 0.02) at 2^-11, and the first-linear output at 2^-6 (GeLU) or 2^-5 (SwiGLU),
+    which keep |value / scale| inside the E4M3 range 448."""
+    sx, sw = 2.0 ** -6, 2.0 ** -11
+    sh = 2.0 ** -5 if s.gated else 2.0 ** -6
+    return {"X": synth.e4m3_codes((s.M, s.h), s.x_std, sx, 0, synth.TID_X),
+            "A": synth.e4m3_codes((s.a_rows, s.h), s.w_std, sw, 0, synth.TID_A),
+            "B": synth.e4m3_codes((s.t, s.h, s.Fi), s.w_std, sw, 0, synth.TID_B),
+            "scales": (sx, sw, sw, sh)}
+
+
+def oracle_sample_fp8(s: synth.MlpShape, inp: dict, scale: float = 1.0):
+    import oracle
+    rows = synth.sample_indices(s.M, max(2, int(round(24 * scale))), 1)
+    t0 = time.perf_counter()
+    oracle.mlp_fwd_fp8(inp["X"], inp["A"], inp["B"], s.t, s.act, inp["scales"], rows=rows)
+    dt = time.perf_counter() - t0
+    flops = len(rows) * (2.0 * s.h * s.a_rows + 2.0 * s.F * s.h)
+    return flops, dt, f"FP8 forward of {len(rows)} token rows"
+
+
 # ------------------------------------------------------------------------------ our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -244,9 +266,14 @@ def run_ours(args, rank, world, local_rank):
     s = args.shape
     sched = {"serial": dm.SCHED_SERIAL, "intra": dm.SCHED_INTRA, "inter": dm.SCHED_INTER,
              "fused": dm.SCHED_FUSED}[args.sched]
-    inp = synth.make_inputs(s, seed=0)
+    fp8 = args.fp8
+    if fp8 and (s.backward or s.layernorm or s.attention):
+        raise SystemExit("--fp8 runs the single-MLP forward workloads (add --pass fwd for the fwd+bwd one)")
+    inp = synth.make_inputs(s, seed=0) if not fp8 else fp8_inputs(s)
 
     def dev(a):
+        if a.dtype == np.uint8:
+            return torch.from_numpy(np.ascontiguousarray(a)).cuda()
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
 
     X, A, B = dev(inp["X"]), dev(inp["A"]), dev(inp["B"])
@@ -256,7 +283,9 @@ def run_ours(args, rank, world, local_rank):
                       heads=s.heads, seq=s.seq if s.attention else 0)
     Wqkv = dev(inp["Wqkv"]) if s.attention else None
     Wo = dev(inp["Wo"]) if s.attention else None
-    if s.attention:
+    if fp8:
+        wsb = dm.domino_workspace_size(cfg, dm.PASS_FWD_FP8)
+    elif s.attention:
         wsb = dm.domino_workspace_size(cfg, dm.PASS_BLOCK)
     elif s.layernorm:
         wsb = max(dm.domino_workspace_size(cfg, dm.PASS_STACK),
@@ -277,6 +306,9 @@ def run_ours(args, rank, world, local_rank):
     def step_on(st, Xin, gYin, Yout=None, gXout=None):
         Yout = Y if Yout is None else Yout
         gXout = gX if gXout is None else gXout
+        if fp8:
+            dm.domino_mlp_fwd_fp8(h, cfg, Xin, A, B, inp["scales"], Yout, ws, wsb, st)
+            return
         if s.attention:
             dm.domino_block_fwd(h, cfg, Xin, Wqkv, Wo, A, B, Yout, ws, wsb, st)
             return
@@ -353,7 +385,8 @@ def run_ours(args, rank, world, local_rank):
     # memory and reads its outputs (Y, gX) back.  As a training loop would, the next step's inputs
     # are prefetched on one copy stream while the current step computes, and each step's outputs
     # are read back on another while the next step computes (double-buffered device buffers).
-    hX = torch.from_numpy(inp["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hX = (torch.from_numpy(inp["X"]) if fp8 else torch.from_numpy(inp["X"].view(np.int16)).view(torch.bfloat16))
+    hX = hX.pin_memory()
     hgY = torch.from_numpy(inp["gY"].view(np.int16)).view(torch.bfloat16).pin_memory() if s.backward else None
     hY = torch.empty((s.M, s.h), dtype=torch.bfloat16).pin_memory()
     hgX = torch.empty((s.M, s.h), dtype=torch.bfloat16).pin_memory() if s.backward else None
@@ -361,7 +394,7 @@ def run_ours(args, rank, world, local_rank):
     gYs = [torch.empty_like(gY) for _ in range(2)] if s.backward else [None, None]
     Ys = [Y, torch.empty_like(Y)]
     gXs = [gX, torch.empty_like(gX)] if s.backward else [None, None]
-    h2d = hX.numel() * 2 + (hgY.numel() * 2 if s.backward else 0)
+    h2d = hX.numel() * hX.element_size() + (hgY.numel() * 2 if s.backward else 0)
     d2h = hY.numel() * 2 + (hgX.numel() * 2 if s.backward else 0)
     cs_in, cs_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
@@ -423,12 +456,19 @@ def run_ours(args, rank, world, local_rank):
     sha = kernel_source_sha()
     traffic = NCU_TRAFFIC.get((s.name, dom))
     traffic_val = traffic["bytes_per_launch"] if traffic and traffic.get("src_sha") == sha else None
+    # FP8 contractions: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25 = 2.  The
+    # sustained (power-capped) peak applies when the run hit the power cap; a run that held its
+    # clocks (short steps) is held to the burst figure.
+    capped = "sw_power_cap" in (clk.get("reasons") or [])
+    peak_key = "bf16_tflops_sustained" if capped else "bf16_tflops"
+    peak_scale = 2.0 if fp8 else 1.0
+    peak_kind = ("e4m3 = 2 x " if fp8 else "") + ("bf16 sustained" if capped else "bf16 burst")
     if bound == "tensor":
         achieved = per_launch / (avg_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak = peaks[peak_key] * peak_scale
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic_val,
-                "peak_kind": f"bf16 sustained ({peaks['source']})", "algorithmic_flops_per_launch": per_launch,
+                "peak_kind": f"{peak_kind} ({peaks['source']})", "algorithmic_flops_per_launch": per_launch,
                 "avg_launch_ms": avg_ms}
     else:
         achieved = per_launch / (avg_ms * 1e-3) / 1e9
@@ -447,18 +487,21 @@ def run_ours(args, rank, world, local_rank):
             v["gbs"] = w / (v["avg_ms"] * 1e-3) / 1e9
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
            "config": config_json(s, args.sched, world),
-           "pct_of_peak": {"of_sustained": value / world / peaks["bf16_tflops_sustained"],
-                           "of_burst": value / world / peaks["bf16_tflops"], "peaks": peaks["source"]},
+           "pct_of_peak": {"of_sustained": value / world / (peaks["bf16_tflops_sustained"] * peak_scale),
+                           "of_burst": value / world / (peaks["bf16_tflops"] * peak_scale),
+                           "peaks": peaks["source"] + (" x 2 for e4m3" if fp8 else "")},
            "roofline": roof,
            "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
            "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
+    if fp8:
+        out["config"]["operands"] = "e4m3 with per-tensor scales (sx, sa, sb, sh) = " + str(inp["scales"])
     if args.graph:
         out["config"]["graph"] = True
         out["eager_value"] = world * args.steps * flops / (ms_eager * 1e-3) / 1e12
     if world == 1 and not args.no_cpu_baseline:
-        flops_s, dt, what = oracle_sample(s, inp, scale=5.0)
+        flops_s, dt, what = (oracle_sample_fp8 if fp8 else oracle_sample)(s, inp, scale=5.0)
         import oracle
         out["cpu_baseline"] = {"value": flops_s / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                                "kind": "oracle", "sample": what, "seconds": dt}
@@ -507,6 +550,7 @@ def main():
     ap.add_argument("--M", type=int, default=None, help="override the token count (profiling aid)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="time replays of one step captured as a CUDA graph")
+    ap.add_argument("--fp8", action="store_true", help="E4M3 operands (domino_mlp_fwd_fp8), forward MLP workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

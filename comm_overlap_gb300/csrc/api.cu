@@ -92,6 +92,8 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   const int64_t Fi = mlp ? c->ffn / c->t : 8;
   if (c->h % 8 != 0 || Fi % 8 != 0 || (c->h / c->q) % 8 != 0)
     return fail(DOMINO_ERR_ALIGNMENT, "h, ffn/t and h/q must be multiples of 8 (16-byte rows)");
+  if (pass == DOMINO_PASS_FWD_FP8 && (c->h % 16 != 0 || Fi % 16 != 0))
+    return fail(DOMINO_ERR_ALIGNMENT, "FP8: h and ffn/t must be multiples of 16 (16-byte rows)");
   if (attn) {
     if (c->heads < 1 || c->seq < 1) return fail(DOMINO_ERR_INVALID_ARG, "attention needs heads >= 1 and seq >= 1");
     if (c->h % c->heads != 0 || c->heads % c->t != 0)
@@ -108,7 +110,7 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
     if (c->layers < 1) return fail(DOMINO_ERR_INVALID_ARG, "layers must be >= 1");
     if (!(c->ln_eps > 0.0f)) return fail(DOMINO_ERR_INVALID_ARG, "ln_eps must be > 0");
   }
-  if (pass < DOMINO_PASS_FWD || pass > DOMINO_PASS_BLOCK) return fail(DOMINO_ERR_INVALID_ARG, "bad pass");
+  if (pass < DOMINO_PASS_FWD || pass > DOMINO_PASS_FWD_FP8) return fail(DOMINO_ERR_INVALID_ARG, "bad pass");
   if (pass == DOMINO_PASS_BLOCK) {
     if (c->layers < 1) return fail(DOMINO_ERR_INVALID_ARG, "layers must be >= 1");
     if (!(c->ln_eps > 0.0f)) return fail(DOMINO_ERR_INVALID_ARG, "ln_eps must be > 0");
@@ -146,6 +148,9 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
       p.off_h = off;
       off = align_up(off + size_t(p.m) * p.F * 2);
     }
+  } else if (pass == DOMINO_PASS_FWD_FP8) {
+    p.off_h = off;  // E4M3 first-linear output of one row chunk
+    off = align_up(off + size_t(p.m) * p.F);
   } else if (pass == DOMINO_PASS_FWD || pass == DOMINO_PASS_STACK) {
     p.off_h = off;
     off = align_up(off + size_t(p.m) * p.F * 2);
@@ -237,6 +242,17 @@ domino_status map_epi_bf16(CUtensorMap* m, const void* base, int64_t cols, int64
   return DOMINO_OK;
 }
 
+// 8-bit (E4M3) K-major operand: (K, rows, batch) with a 128-element (128-byte) K box.
+domino_status map_k8(CUtensorMap* m, const void* base, int64_t K, int64_t rows, int64_t batch, int64_t row_stride,
+                     int64_t batch_stride, uint32_t box_rows) {
+  const uint64_t dims[3] = {uint64_t(K), uint64_t(rows), uint64_t(batch)};
+  const uint64_t strides[2] = {uint64_t(row_stride), uint64_t(batch > 1 ? batch_stride : row_stride * rows)};
+  const uint32_t box[3] = {128, box_rows, 1};
+  std::string err;
+  if (!dm::make_map(m, 1, base, 3, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
+  return DOMINO_OK;
+}
+
 // fp32 output map of a partial slot: t contiguous rows x cols blocks, TMA-store box 32 x 32.
 domino_status map_f32_out(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, int64_t batch) {
   const uint64_t dims[3] = {uint64_t(cols), uint64_t(rows), uint64_t(batch)};
@@ -290,6 +306,9 @@ GemmArgs gemm_args(int variant, int batches, int64_t M, int64_t N, int64_t K, in
   a.n_tiles = int32_t(cdiv(N, dm::gemm_out_tile_n(variant)));
   a.k_blocks = int32_t(cdiv(K, dm::kBK));
   a.err_site = site << 4;
+  a.alpha = 1.0f;
+  a.out_scale = 1.0f;
+  if (variant >= dm::GV_F8_FWD_ACT) a.k_blocks = int32_t(cdiv(K, 128));  // 128 E4M3 codes per K step
   return a;
 }
 
@@ -299,13 +318,16 @@ domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap
                        const dm::EpiMaps* em = nullptr) {
   const int64_t tiles = int64_t(a.batches) * a.m_tiles * a.n_tiles;
   if (tiles == 0) return DOMINO_OK;
-  const bool needs = variant != dm::GV_WGRAD;
+  const bool needs = variant != dm::GV_WGRAD && variant != dm::GV_F8_FWD_ACT && variant != dm::GV_F8_FWD_GLU;
   if (needs && em == nullptr) return fail(DOMINO_ERR_INVALID_ARG, "internal: GEMM epilogue without its maps");
   static const dm::EpiMaps kNone = {};
   const dm::EpiMaps& e = em ? *em : kNone;
   const bool fwd_tu = variant <= dm::GV_FWD_PARTIAL || variant == dm::GV_FWD_REDUCE;
+  const bool fp8_tu = variant >= dm::GV_F8_FWD_ACT;
   return launch(H, kind, st, "GEMM launch", [&] {
-    return fwd_tu ? dm::launch_gemm_fwd(variant, ta, tb, e, a, st) : dm::launch_gemm_bwd(variant, ta, tb, e, a, st);
+    return fp8_tu   ? dm::launch_gemm_fp8(variant, ta, tb, e, a, st)
+           : fwd_tu ? dm::launch_gemm_fwd(variant, ta, tb, e, a, st)
+                    : dm::launch_gemm_bwd(variant, ta, tb, e, a, st);
   });
 }
 
@@ -417,21 +439,25 @@ domino_status ready(domino_handle H) {
 // shards' weights (Kc, h, t).
 domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, int kind,
                             const CUtensorMap& mapH, const CUtensorMap& mapB, int64_t Kc, float* parts,
-                            const uint16_t* res_c, uint16_t* Yc, int site) {
+                            const uint16_t* res_c, uint16_t* Yc, int site, bool fp8 = false, float alpha = 1.0f) {
+  const int v_reduce = fp8 ? dm::GV_F8_FWD_REDUCE : dm::GV_FWD_REDUCE;
+  const int v_partial = fp8 ? dm::GV_F8_FWD_PARTIAL : dm::GV_FWD_PARTIAL;
   for (int qc = 0; qc < P.q; ++qc) {
     if (P.sched == DOMINO_SCHED_FUSED) {
-      GemmArgs a = gemm_args(dm::GV_FWD_REDUCE, P.t, P.m, P.n, Kc, site);
+      GemmArgs a = gemm_args(v_reduce, P.t, P.m, P.n, Kc, site);
       a.a_bmul = 1;
       a.b_row_off = int32_t(qc * P.n);
       a.b_bmul = 1;
-      DM_TRY(run_fused_reduce(H, kind, dm::GV_FWD_REDUCE, P, mapH, mapB, a, parts,
-                              res_c ? res_c + qc * P.n : nullptr, Yc + qc * P.n, P.h, S.comp));
+      a.alpha = alpha;
+      DM_TRY(run_fused_reduce(H, kind, v_reduce, P, mapH, mapB, a, parts, res_c ? res_c + qc * P.n : nullptr,
+                              Yc + qc * P.n, P.h, S.comp));
       continue;
     }
     int slot;
     DM_TRY(slot_acquire(H, P, S, R, &slot));
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
-    GemmArgs a = gemm_args(dm::GV_FWD_PARTIAL, P.t, P.m, P.n, Kc, site);
+    GemmArgs a = gemm_args(v_partial, P.t, P.m, P.n, Kc, site);
+    a.alpha = alpha;
     a.a_bmul = 1;
     a.b_row_off = int32_t(qc * P.n);
     a.b_bmul = 1;
@@ -440,7 +466,7 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
     a.bs0 = P.m * P.n;
     dm::EpiMaps em = {};
     DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
-    DM_TRY(run_gemm(H, kind, dm::GV_FWD_PARTIAL, mapH, mapB, a, S.comp, &em));
+    DM_TRY(run_gemm(H, kind, v_partial, mapH, mapB, a, S.comp, &em));
     DM_TRY(slot_handoff(H, S, slot));
     DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, res_c ? res_c + qc * P.n : nullptr, P.h,
                          Yc + qc * P.n, P.h, S.red));
@@ -485,6 +511,45 @@ domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, Sl
   }
   DM_TRY(map_k(&mapH, Hbuf, P.Fi, P.m, P.t, P.F, P.Fi, 128));
   return second_linear(H, P, S, R, DOMINO_K_GEMM_FWD2, mapH, mapB, P.Fi, parts, res_c, Yc, site + 1);
+}
+
+// ---- FP8 forward of one row chunk: the first linear on E4M3 operands with the activation and the
+// E4M3 re-quantisation of H (scale 1 / sh) in its epilogue, then the second linear on E4M3 H and B
+// into fp32 partials (scaled by sh sb) and their fp32 shard-sum.
+domino_status mlp_chunk_fwd_fp8(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, const uint8_t* X8c,
+                                const CUtensorMap& mapA, const CUtensorMap& mapB, uint8_t* H8, float* parts,
+                                uint16_t* Yc, const float* sc) {
+  CUtensorMap mapX, mapH;
+  DM_TRY(map_k8(&mapX, X8c, P.h, P.m, 1, P.h, 0, 128));
+  {
+    const int variant = P.gated ? dm::GV_F8_FWD_GLU : dm::GV_F8_FWD_ACT;
+    GemmArgs a = gemm_args(variant, P.gated ? P.t : 1, P.m, P.gated ? P.Fi : P.F, P.h, 10);
+    a.act = P.act;
+    a.out0 = H8;
+    a.ld0 = P.F;
+    a.bs0 = P.gated ? P.Fi : 0;
+    a.alpha = sc[0] * sc[1];
+    a.out_scale = 1.0f / sc[3];
+    DM_TRY(run_gemm(H, DOMINO_K_GEMM_FWD1, variant, mapX, mapA, a, S.comp, nullptr));
+  }
+  DM_TRY(map_k8(&mapH, H8, P.Fi, P.m, P.t, P.F, P.Fi, 128));
+  return second_linear(H, P, S, R, DOMINO_K_GEMM_FWD2, mapH, mapB, P.Fi, parts, nullptr, Yc, 11, true,
+                       sc[3] * sc[2]);
+}
+
+domino_status weight_maps_fp8(const Plan& P, const uint8_t* A8, const uint8_t* B8, CUtensorMap* mapA,
+                              CUtensorMap* mapB) {
+  if (P.gated) {
+    const uint64_t dims[4] = {uint64_t(P.h), uint64_t(P.Fi), 2, uint64_t(P.t)};
+    const uint64_t strides[3] = {uint64_t(P.h), uint64_t(P.Fi * P.h), uint64_t(2 * P.Fi * P.h)};
+    const uint32_t box[4] = {128, 128, 1, 1};
+    std::string err;
+    if (!dm::make_map(mapA, 1, A8, 4, dims, strides, box, &err)) return fail(DOMINO_ERR_CUDA, err);
+  } else {
+    DM_TRY(map_k8(mapA, A8, P.h, P.F, 1, P.h, 0, dm::kBBoxRows));
+  }
+  DM_TRY(map_k8(mapB, B8, P.Fi, P.h, P.t, P.Fi, P.h * P.Fi, dm::kBBoxRows));
+  return DOMINO_OK;
 }
 
 domino_status weight_maps_fwd(const Plan& P, const uint16_t* A, const uint16_t* B, CUtensorMap* mapA,
@@ -1036,6 +1101,42 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
   return finish(H, S, caller, st);
 }
 
+domino_status domino_mlp_fwd_fp8(domino_handle H, const domino_cfg* cfg, const uint8_t* X8, const uint8_t* A8,
+                                 const uint8_t* B8, const float* scales, uint16_t* Y, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  DM_TRY(ready(H));
+  Plan P;
+  DM_TRY(make_plan(cfg, DOMINO_PASS_FWD_FP8, &P));
+  DM_TRY(check_ptr(X8, "X8"));
+  DM_TRY(check_ptr(A8, "A8"));
+  DM_TRY(check_ptr(B8, "B8"));
+  DM_TRY(check_ptr(Y, "Y"));
+  if (!scales) return fail(DOMINO_ERR_INVALID_ARG, "scales is NULL");
+  for (int i = 0; i < 4; ++i)
+    if (!(scales[i] > 0.0f) || !std::isfinite(scales[i]))
+      return fail(DOMINO_ERR_INVALID_ARG, "scales must be finite and > 0");
+  DM_TRY(check_ws(P, ws, ws_bytes));
+  if (P.M == 0) return DOMINO_OK;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  CUtensorMap mapA, mapB;
+  DM_TRY(weight_maps_fp8(P, A8, B8, &mapA, &mapB));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint8_t* H8 = w + P.off_h;
+  float* parts = reinterpret_cast<float*>(w + P.off_part);
+  const float sc[4] = {scales[0], scales[1], scales[2], scales[3]};
+  Streams S;
+  DM_TRY(fork(H, P, caller, &S));
+  const domino_status st = [&]() -> domino_status {
+    SlotRing R;
+    for (int pc = 0; pc < P.p; ++pc) {
+      const int64_t r0 = pc * P.m;
+      DM_TRY(mlp_chunk_fwd_fp8(H, P, S, R, X8 + r0 * P.h, mapA, mapB, H8, parts, Y + r0 * P.h, sc));
+    }
+    return DOMINO_OK;
+  }();
+  return finish(H, S, caller, st);
+}
+
 domino_status domino_attn_fwd(domino_handle H, const domino_cfg* cfg, const uint16_t* X, const uint16_t* Wqkv,
                               const uint16_t* Wo, uint16_t* Y, void* ws, size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
@@ -1122,11 +1223,12 @@ domino_status domino_device_status(domino_handle H, domino_status* out, int32_t*
   DM_TRY(ready(H));
   if (!out) return fail(DOMINO_ERR_INVALID_ARG, "out is NULL");
   DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-  int c1 = 0, c2 = 0, c3 = 0;
+  int c1 = 0, c2 = 0, c3 = 0, c4 = 0;
   DM_CUDA(dm::take_gemm_fwd_error(&c1), "reading the device error word");
   DM_CUDA(dm::take_gemm_bwd_error(&c2), "reading the device error word");
   DM_CUDA(dm::take_attn_error(&c3), "reading the device error word");
-  const int code = c1 ? c1 : (c2 ? c2 : c3);
+  DM_CUDA(dm::take_gemm_fp8_error(&c4), "reading the device error word");
+  const int code = c1 ? c1 : (c2 ? c2 : (c3 ? c3 : c4));
   *out = code ? DOMINO_ERR_TIMEOUT : DOMINO_OK;
   if (site) *site = code;
   return DOMINO_OK;

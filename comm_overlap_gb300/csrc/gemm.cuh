@@ -14,6 +14,7 @@
 // and returns, leaving a code in the translation unit's error word.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "actfn.cuh"
 #include "kernels.h"
@@ -58,6 +59,8 @@ constexpr int block_threads() { return 64 + 32 * (epi_warps<EPI>() + fin_warps<E
 constexpr int kActBwdWarpBytes = 10240;
 constexpr int kFwdWarpBytes = 6144;
 constexpr bool is_act_fwd(int epi) { return epi == EPI_ACT_BF16 || epi == EPI_GLU_BF16; }
+constexpr bool is_act_f8(int epi) { return epi == EPI_ACT_F8 || epi == EPI_GLU_F8; }
+constexpr bool is_gated_b(int epi) { return epi == EPI_GLU_BF16 || epi == EPI_GLU_F8; }
 template <int EPI>
 constexpr int staging_bytes() {
   return (EPI == EPI_F32_STORE || EPI == EPI_F32_REDUCE) ? 4 * 2 * 4096
@@ -426,12 +429,57 @@ __device__ __forceinline__ void epilogue_fwd_tma(const GemmArgs& a, const EpiMap
   }
 }
 
+// Four fp32 values -> four E4M3 codes (nearest, ties to even, saturating at +-448), the first in the
+// lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// FP8 first-linear epilogue (EPI_ACT_F8 / EPI_GLU_F8) of NC accumulator columns for the calling
+// thread's row: H = act(alpha D) (gated: glu(alpha gate, alpha up), the up columns 128 further),
+// times out_scale, rounded to E4M3 and stored with two 16-byte stores per 32 columns (N is a
+// multiple of 16).
+template <int EPI, int NC>
+__device__ __forceinline__ void epilogue_f8_cols(const GemmArgs& a, uint32_t tacc, int g, int row, int col0) {
+  const bool row_ok = row < a.M;
+#pragma unroll 1
+  for (int cc = 0; cc < NC; cc += 32) {
+    uint32_t rz[32], ru[32];
+    tmem_ld32(tacc + cc, rz);
+    if constexpr (EPI == EPI_GLU_F8) tmem_ld32(tacc + 128 + cc, ru);
+    tmem_ld_wait();
+    const int col = col0 + cc;
+    if (!row_ok || col >= a.N) continue;
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float z = __uint_as_float(rz[e + k]) * a.alpha;
+        float hv;
+        if constexpr (EPI == EPI_GLU_F8)
+          hv = glu_fwd(a.act, z, __uint_as_float(ru[e + k]) * a.alpha);
+        else
+          hv = act_fwd(a.act, z);
+        v[k] = hv * a.out_scale;
+      }
+      w[e >> 2] = pack_e4m3x4(v[0], v[1], v[2], v[3]);
+    }
+    uint8_t* o = static_cast<uint8_t*>(a.out0) + g * a.bs0 + static_cast<int64_t>(row) * a.ld0 + col;
+    *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (col + 16 < a.N) *reinterpret_cast<uint4*>(o + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // fp32 epilogue through TMA stores: each 32-column chunk of the warp's 32 rows is written to one
 // of the warp's two staging buffers (row `lane`, 16-byte chunk j at position j ^ (lane % 8), the
 // 128-byte swizzle pattern) and stored by one lane with a bulk tensor copy; TMA clips rows and
 // columns outside the output.  A buffer is rewritten only after the store issued from it two
 // chunks earlier has finished reading it.
-template <int NC>
+template <int NC, bool SCALE>
 __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtensorMap* tmC, uint32_t tacc, int g,
                                                  int row0, int col0, uint32_t staging, uint32_t& nchunk,
                                                  int lane) {
@@ -445,6 +493,10 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtens
     uint32_t r[32];
     tmem_ld32(tacc + cc, r);
     tmem_ld_wait();
+    if constexpr (SCALE) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a.alpha);
+    }
     const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -469,7 +521,7 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtens
 // each add rounded to nearest.  After the last shard's adds complete, the rows are handed to the
 // finaliser warp of the same lane quarter (two-slot mbarrier ring `fin_ready` / `fin_done`,
 // counted by `nfin`).  Returns false if a bounded wait gave up.
-template <int NC>
+template <int NC, bool SCALE>
 __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const EpiMaps& em, uint32_t tacc, int g,
                                                     int row0, int col0, uint32_t staging, uint32_t& nchunk,
                                                     uint32_t fin_ready, uint32_t fin_done, uint32_t& nfin,
@@ -488,6 +540,10 @@ __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const Epi
     uint32_t r[32];
     tmem_ld32(tacc + cc, r);
     tmem_ld_wait();
+    if constexpr (SCALE) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a.alpha);
+    }
     const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -589,15 +645,21 @@ __device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, i
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool PAIR>
+// F8: operands are E4M3 codes (kind::f8f6f4), 128 elements per 128-byte K step.
+template <int EPI, bool A_MN, bool B_MN, bool PAIR, bool F8 = false>
 __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ EpiMaps em, const GemmArgs args) {
   using R = Ring<PAIR, EPI>;
   constexpr int S = R::kStages;
-  constexpr bool kGatedB = (EPI == EPI_GLU_BF16);
+  static_assert(!F8 || (!A_MN && !B_MN && PAIR), "FP8 operands: K-major, CTA pair");
+  static_assert(is_act_f8(EPI) ? F8 : (!F8 || EPI == EPI_F32_STORE || EPI == EPI_F32_REDUCE),
+                "the E4M3 epilogues go with FP8 operands, which take only those and the fp32 ones");
+  constexpr bool kGatedB = is_gated_b(EPI);
   constexpr int kOutN = kGatedB ? 128 : kBN;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(R::kTileM, kBN, A_MN, B_MN);
+  constexpr int kKe = F8 ? 128 : kBK;  // K elements per stage (always 128 bytes per row)
+  constexpr uint32_t kIdesc =
+      F8 ? idesc_e4m3_f32(R::kTileM, kBN, A_MN, B_MN) : idesc_bf16_f32(R::kTileM, kBN, A_MN, B_MN);
   // barrier indices in the control block
   constexpr int kBarFull = 0, kBarEmpty = S, kBarTmemFull = 2 * S, kBarTmemEmpty = 2 * S + 2,
                 kBarDrain = 2 * S + 4, kBarEpiIn = 2 * S + 5;  // kBarEpiIn: one per epilogue warp
@@ -687,7 +749,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
           }
           const uint32_t sa = stage0 + s * R::kStageBytes, sb = sa + R::kABytes;
           const uint32_t fb_local = bar(kBarFull + s);
-          const int k0 = kb * kBK;
+          const int k0 = kb * kKe;
           if constexpr (PAIR) {
             // the leader's full barrier counts the bytes of both CTAs
             const uint32_t fb = mapa_shared(fb_local, 0);
@@ -769,7 +831,9 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
                                      : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-            if constexpr (PAIR)
+            if constexpr (F8)
+              umma_f8_pair(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
+            else if constexpr (PAIR)
               umma_bf16_pair(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
             else
               umma_bf16(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
@@ -827,10 +891,12 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * kBN + half * kHalfOut);
         if constexpr (EPI == EPI_F32_STORE)
-          epilogue_f32_tma<kHalfOut>(args, &em.m[0], tacc, g, mt * R::kTileM + row_in_tile - lane,
-                                     nt * kOutN + half * kHalfOut, staging, nchunk, lane);
+          epilogue_f32_tma<kHalfOut, F8>(args, &em.m[0], tacc, g, mt * R::kTileM + row_in_tile - lane,
+                                         nt * kOutN + half * kHalfOut, staging, nchunk, lane);
+        else if constexpr (is_act_f8(EPI))
+          epilogue_f8_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
         else if constexpr (EPI == EPI_F32_REDUCE) {
-          if (!epilogue_f32_reduce<kHalfOut>(args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
+          if (!epilogue_f32_reduce<kHalfOut, F8>(args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
                                              nt * kOutN + half * kHalfOut, staging, nchunk,
                                              bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), nfin,
                                              lane, abort_flag, err))
@@ -875,11 +941,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
 }
 
 // Launches one GEMM: one CTA (or CTA pair) per SM (pair), persistent over the tiles.
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, bool F8 = false>
 cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
                           const GemmArgs& args, cudaStream_t st) {
   constexpr bool P = kPairMma;
-  auto fn = gemm_kernel<EPI, A_MN, B_MN, P>;
+  auto fn = gemm_kernel<EPI, A_MN, B_MN, P, F8>;
   constexpr int smem = smem_bytes<P, EPI>();
   static_assert(smem <= 232448, "shared memory beyond the per-CTA limit");
   static int max_units = 0;  // co-resident CTAs (single) or clusters (pair)

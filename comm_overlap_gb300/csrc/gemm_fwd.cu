@@ -4,7 +4,7 @@
 
 namespace dm {
 
-int gemm_out_tile_n(int variant) { return variant == GV_FWD_GLU ? 128 : kBN; }
+int gemm_out_tile_n(int variant) { return (variant == GV_FWD_GLU || variant == GV_F8_FWD_GLU) ? 128 : kBN; }
 
 cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
                             const GemmArgs& args, cudaStream_t st) {

@@ -28,8 +28,10 @@ enum GemmEpi : int {
   EPI_F32_ACCUM = 3, // out0 += D (fp32)
   EPI_ACT_BWD = 4,   // in0 = Z: out0 = bf16(D * act'(Z)); out1 = bf16(act(Z))
   EPI_GLU_BWD = 5,   // in0: G at +0, U at +offi: out0: dG at +0, dU at +off0; out1 = bf16(glu(G, U))
-  EPI_F32_REDUCE = 6 // batch g = shard, the shards of a tile in order: S (fp32, out0) = P_0, S += P_g;
-                     //   then out1 = bf16(in0 + S) (residual in0 nullable)
+  EPI_F32_REDUCE = 6, // batch g = shard, the shards of a tile in order: S (fp32, out0) = P_0, S += P_g;
+                      //   then out1 = bf16(in0 + S) (residual in0 nullable)
+  EPI_ACT_F8 = 7,     // FP8 operands: out0 = e4m3(act(alpha D) * out_scale)
+  EPI_GLU_F8 = 8,     // FP8 operands, D = [gate | up]: out0 = e4m3(glu(alpha gate, alpha up) * out_scale)
 };
 
 // The kernel instantiations the library uses.  A/B operand majorness: K = K-major
@@ -44,7 +46,12 @@ enum GemmVariant : int {
   GV_WGRAD = 6,       // weight gradients (+=):       EPI_F32_ACCUM, A MN, B MN
   GV_FWD_REDUCE = 7,  // second linear + shard-sum:   EPI_F32_REDUCE, A K, B K
   GV_BWD_REDUCE = 8,  // dX partials + shard-sum:     EPI_F32_REDUCE, A K, B MN
-  GV_COUNT = 9
+  // FP8 (E4M3) operands, fp32 accumulation (gemm_fp8.cu); the fp32 epilogues scale D by alpha
+  GV_F8_FWD_ACT = 9,      // first linear, non-gated -> E4M3 H:  EPI_ACT_F8
+  GV_F8_FWD_GLU = 10,     // first linear, gated -> E4M3 H:      EPI_GLU_F8
+  GV_F8_FWD_PARTIAL = 11, // second linear -> fp32 partials:     EPI_F32_STORE
+  GV_F8_FWD_REDUCE = 12,  // second linear + shard-sum:          EPI_F32_REDUCE
+  GV_COUNT = 13
 };
 
 // Per-launch GEMM description.  D[g] (M x N per batch g) = A_op[g] . B_op[g]^T.
@@ -57,6 +64,8 @@ struct GemmArgs {
   int32_t b_row_off, b_bmul;
   int32_t act;
   int32_t err_site;
+  float alpha;      // FP8 variants: scale of the accumulator (product of the operand scales)
+  float out_scale;  // EPI_ACT_F8 / EPI_GLU_F8: factor applied before the E4M3 rounding (1 / sh)
   void* out0;
   int64_t ld0, bs0, off0;
   void* out1;
@@ -85,11 +94,16 @@ cudaError_t launch_gemm_fwd(int variant, const CUtensorMap& ta, const CUtensorMa
                             const GemmArgs& args, cudaStream_t st);
 cudaError_t launch_gemm_bwd(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
                             const GemmArgs& args, cudaStream_t st);
+// FP8 variants (GV_F8_*); operand maps are uint8 with 128-element (128-byte) K boxes, and
+// args.k_blocks counts 128-element K steps.
+cudaError_t launch_gemm_fp8(int variant, const CUtensorMap& ta, const CUtensorMap& tb, const EpiMaps& em,
+                            const GemmArgs& args, cudaStream_t st);
 // Self-test of the bounded-wait failure path (see domino_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int site, cudaStream_t st);
 // Reads and clears the device error word of the GEMM kernels in each translation unit.
 cudaError_t take_gemm_fwd_error(int* code);
 cudaError_t take_gemm_bwd_error(int* code);
+cudaError_t take_gemm_fp8_error(int* code);
 
 // Causal multi-head self-attention of one row chunk (attention.cu), head dimension 128.  QKV: the
 // fused projection output, per token the t shards' [query heads | key heads | value heads], head
@@ -120,7 +134,7 @@ cudaError_t launch_layernorm_bwd(const uint16_t* gN, const uint16_t* N, const fl
                                  uint16_t* out, int64_t rows, int64_t h, cudaStream_t st);
 
 // Tensor maps (zero fill out of bounds).  dims[0] is innermost; strides_bytes[i] is the stride of
-// dims[i+1].  elem_bytes: 2 = bf16, 4 = fp32.  swizzle_bytes: 128 or 64.
+// dims[i+1].  elem_bytes: 1 = 8-bit codes, 2 = bf16, 4 = fp32.  swizzle_bytes: 128 or 64.
 bool tma_encoder_ready(std::string* err);
 bool make_map(CUtensorMap* map, int elem_bytes, const void* base, int rank, const uint64_t* dims,
               const uint64_t* strides_bytes, const uint32_t* box, std::string* err, int swizzle_bytes = 128);

@@ -41,8 +41,9 @@ bool make_map(CUtensorMap* map, int elem_bytes, const void* base, int rank, cons
     estride[i] = 1;
     if (i + 1 < rank) gstride[i] = strides_bytes[i];
   }
-  const CUtensorMapDataType dt =
-      elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUresult r = g_encode(map, dt, static_cast<cuuint32_t>(rank),
                               const_cast<void*>(base), gdim, gstride, bdim, estride,
                               CU_TENSOR_MAP_INTERLEAVE_NONE,

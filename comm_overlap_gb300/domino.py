@@ -19,7 +19,7 @@ STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTE
           4: "DOMINO_ERR_WORKSPACE", 5: "DOMINO_ERR_CUDA", 6: "DOMINO_ERR_TIMEOUT", 7: "DOMINO_ERR_DEVICE"}
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_SWIGLU, ACT_BILINEAR = 0, 1, 2, 3, 4
 SCHED_SERIAL, SCHED_INTRA, SCHED_INTER, SCHED_FUSED = 0, 1, 2, 3
-PASS_FWD, PASS_BWD, PASS_STACK, PASS_STACK_BWD, PASS_ATTN, PASS_BLOCK = 0, 1, 2, 3, 4, 5
+PASS_FWD, PASS_BWD, PASS_STACK, PASS_STACK_BWD, PASS_ATTN, PASS_BLOCK, PASS_FWD_FP8 = 0, 1, 2, 3, 4, 5, 6
 (K_GEMM_FWD1, K_GEMM_FWD2, K_SHARD_SUM, K_LAYERNORM, K_GEMM_DGRAD_H, K_GEMM_WGRAD_B, K_GEMM_DGRAD_X,
  K_GEMM_WGRAD_A, K_LN_BWD, K_GEMM_QKV, K_ATTN, K_GEMM_OPROJ) = range(12)
 KERNEL_NAMES = ["gemm_fwd1", "gemm_fwd2", "shard_sum", "layernorm", "gemm_dgrad_h", "gemm_wgrad_b",
@@ -62,6 +62,8 @@ _SIGS = {
                                ctypes.c_size_t, _P],
     "domino_stack_bwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P, _P,
                          ctypes.c_size_t, _P],
+    "domino_mlp_fwd_fp8": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, ctypes.POINTER(ctypes.c_float), _P, _P,
+                           ctypes.c_size_t, _P],
     "domino_attn_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "domino_block_fwd": [_P, ctypes.POINTER(domino_cfg), _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "domino_shard_sum": [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int64, _P,
@@ -175,6 +177,13 @@ def _nbytes(buf, given):
     if given is not None:
         return given
     return 0 if buf is None else buf.numel() * buf.element_size()
+
+
+def domino_mlp_fwd_fp8(handle, cfg, X8, A8, B8, scales, Y, workspace, workspace_bytes=None, stream=None) -> None:
+    """scales = (sx, sa, sb, sh); X8, A8, B8 are uint8 tensors of E4M3 codes."""
+    sc = (ctypes.c_float * 4)(*[float(v) for v in scales])
+    _check(lib().domino_mlp_fwd_fp8(handle, ctypes.byref(cfg), _ptr(X8), _ptr(A8), _ptr(B8), sc, _ptr(Y),
+                                    _ptr(workspace), _nbytes(workspace, workspace_bytes), _stream(stream)))
 
 
 def domino_attn_fwd(handle, cfg, X, Wqkv, Wo, Y, workspace, workspace_bytes=None, stream=None) -> None:

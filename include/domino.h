@@ -100,7 +100,8 @@ typedef enum {
   DOMINO_PASS_STACK = 2,     /* domino_stack_fwd, domino_stack_fwd_train */
   DOMINO_PASS_STACK_BWD = 3, /* domino_stack_bwd */
   DOMINO_PASS_ATTN = 4,      /* domino_attn_fwd */
-  DOMINO_PASS_BLOCK = 5      /* domino_block_fwd */
+  DOMINO_PASS_BLOCK = 5,     /* domino_block_fwd */
+  DOMINO_PASS_FWD_FP8 = 6    /* domino_mlp_fwd_fp8 */
 } domino_pass;
 
 typedef struct {
@@ -202,6 +203,20 @@ DOMINO_API domino_status domino_stack_bwd(domino_handle handle, const domino_cfg
                                           const uint16_t* B, const void* save, size_t save_bytes,
                                           const uint16_t* gZ_out, uint16_t* gZ_in, float* gA, float* gB,
                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* FP8 variant of domino_mlp_fwd ("04 · TP/SP 的通信-计算 overlap 与工程优化" §4: FP8 halves what
+ * moves, the reduction accumulates in higher precision).  Operands are E4M3 codes (OCP FP8:
+ * 4 exponent bits, bias 7, 3 mantissa bits, largest finite 448, no infinities) with per-tensor
+ * scales, host array scales = {sx, sa, sb, sh}: the real operands are sx*X8, sa*A8, sb*B8.
+ *   Z = sx sa (X8 . A8^T) in fp32;  H = act(Z) (gated: glu);  H8 = e4m3(H / sh) (nearest, ties to
+ *   even, saturating at +-448) for the second linear;  partials P_i = sh sb (H8_i . B8_i^T) and
+ *   their shard-sum in fp32;  Y = bf16(sum), rounded once.
+ * Layouts as domino_mlp_fwd, one byte per element: X8 M x h, A8 the A shards, B8 the B shards.
+ * Needs h and ffn / t to be multiples of 16 (16-byte rows).  Power-of-two scales make the scaling
+ * exact.  Same chunking and schedules; workspace: domino_workspace_size(cfg, DOMINO_PASS_FWD_FP8). */
+DOMINO_API domino_status domino_mlp_fwd_fp8(domino_handle handle, const domino_cfg* cfg, const uint8_t* X8,
+                                            const uint8_t* A8, const uint8_t* B8, const float* scales, uint16_t* Y,
+                                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Attention sublayer of one Transformer block ("TP 的数据依赖：通信为何难以隐藏": for the attention
  * layer of XAB=Y, X is the input, A the multi-head attention and B a linear layer; the AllReduce
