@@ -3,18 +3,22 @@
 // XAB=Y, A is the multi-head attention, B the output projection).  Heads are split over the t
 // shards; shard i's query/key/value heads come from its own slice of the fused projection output.
 //
-// One CTA computes one (query block of 128 positions, head, sequence): O = softmax(Q K^T / sqrt(d)
-// + causal mask) V with an online softmax over key/value blocks of 128 positions (the running
-// maximum and sum are rescaled as blocks arrive, so the result equals the plain softmax up to
-// rounding).  Warp roles:
-//   warp 0 (one lane)  TMA producer: the Q tile once, then K and V tiles into two-deep rings.
-//   warp 1 (one lane)  MMA issuer: S_j = Q K_j^T into one of two TMEM score buffers (issued one
-//                      block ahead, so it overlaps the softmax of the previous block), then
-//                      O += P_j V_j into the TMEM output accumulator.
-//   warps 2-5          softmax, one query row per thread (TMEM lane quarter = warp % 4): scores
-//                      from TMEM, running max / sum in fp32, O rescaled in TMEM when the maximum
-//                      grows, P rounded to bf16 into shared memory (128-byte swizzled K-major
-//                      layout of the MMA's A operand); at the end O / sum -> bf16 -> TMA store.
+// One CTA computes two consecutive query blocks of 128 positions (tiles 0 and 1) of one head and
+// sequence: O = softmax(Q K^T / sqrt(d) + causal mask) V, with an online softmax over key/value
+// blocks of 128 positions (running maximum and sum rescaled as blocks arrive; equal to the plain
+// softmax up to rounding).  Both tiles use the same K_j, V_j, and their work alternates on the
+// tensor core so that one tile's softmax runs under the other tile's matrix products.
+// Warp roles:
+//   warp 0 (one lane)  TMA producer: both Q tiles once, then K and V tiles into two-deep rings.
+//   warp 1 (one lane)  MMA issuer, per block j and tile x: O_x += P_x V_j as soon as the softmax
+//                      handed P_x over, then S_x = Q_x K_{j+1}^T (in that order: P_x lives in the
+//                      columns of S_x, and tensor-core operations of one thread run in order).
+//   warps 2-5, 6-9     softmax of tile 0 and tile 1, one query row per thread (TMEM lane quarter =
+//                      warp % 4): scores from TMEM, running max / sum in fp32, O_x rescaled in TMEM
+//                      when a row maximum grew, P rounded to bf16 and stored into TMEM; at the end
+//                      O / sum -> bf16 -> TMA store (staged in the tile's Q buffer).
+// TMEM: S_0 = columns 0-127, S_1 = 128-255 (P_x in the first 64 columns of S_x as bf16 pairs),
+// O_0 = 256-383, O_1 = 384-511.
 // Every wait is bounded (ptx.cuh); on expiry the CTA drains what it has in flight, frees TMEM and
 // returns, leaving a code in this translation unit's error word.
 #include <cuda_bf16.h>
@@ -29,17 +33,17 @@ static __device__ int g_attn_err;
 
 constexpr int kAttnD = 128;                         // head dimension
 constexpr int kAttnBlk = 128;                       // query rows / key-value positions per block
-constexpr uint32_t kTile = kAttnBlk * kAttnD * 2;   // 32 KiB: one Q, K, V or P tile
+constexpr uint32_t kTile = kAttnBlk * kAttnD * 2;   // 32 KiB: one Q, K or V tile
 constexpr uint32_t kHalf = kTile / 2;               // one 64-column (128-byte) swizzle panel
-constexpr int kAttnThreads = 192;
-constexpr int kAttnSmem = 1024 /* alignment slack */ + 1024 /* control */ + 6 * kTile;  // Q, K[2], V[2], P
-constexpr uint32_t kAttnTmemCols = 512;             // S[2] (2 x 128) + O (128), rounded up
+constexpr int kAttnThreads = 320;
+constexpr int kAttnSmem = 1024 /* alignment slack */ + 1024 /* control */ + 6 * kTile;  // Q[2], K[2], V[2]
+constexpr uint32_t kAttnTmemCols = 512;
 constexpr uint64_t kAttnDrainNs = 200000000ull;
 
 // barrier indices
 enum : int {
-  B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = 3, B_V_FULL = 5, B_V_EMPTY = 7, B_S_FULL = 9, B_S_EMPTY = 11,
-  B_P_FULL = 13, B_PV_DONE = 14, B_DRAIN = 15, B_COUNT = 16
+  B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = 3, B_V_FULL = 5, B_V_EMPTY = 7, B_S_FULL = 9, B_P_FULL = 11,
+  B_PV_DONE = 13, B_DRAIN = 15, B_COUNT = 16
 };
 
 __device__ __forceinline__ void attn_wait_drain(uint32_t bar, uint32_t parity) {
@@ -59,21 +63,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
   const uint32_t bar0 = smem_u32(smem);
   auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const uint32_t sQ = smem_u32(smem + 1024), sK = sQ + kTile, sV = sQ + 3 * kTile, sP = sQ + 5 * kTile;
+  const uint32_t sQ = smem_u32(smem + 1024), sK = sQ + 2 * kTile, sV = sQ + 4 * kTile;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = a.n_qblk - 1 - static_cast<int>(blockIdx.x);  // longest (most key blocks) first
+  const int n_pairs = (a.n_qblk + 1) >> 1;
+  const int q0 = 2 * (n_pairs - 1 - static_cast<int>(blockIdx.x));  // longest (most key blocks) first
+  const int ntiles = (q0 + 1 < a.n_qblk) ? 2 : 1;
   const int hd = blockIdx.y, sq = blockIdx.z;
   const int shard = hd / a.nhi, jh = hd - shard * a.nhi;
   const int slot_q = (shard * 3 + 0) * a.nhi + jh, slot_k = (shard * 3 + 1) * a.nhi + jh,
             slot_v = (shard * 3 + 2) * a.nhi + jh;
-  const int nkv = qb + 1;  // causal: key/value blocks 0 .. qb
+  const int nblk = q0 + ntiles;  // key/value blocks 0 .. q0 + ntiles - 1 (tile x stops at q0 + x)
   int* err = &g_attn_err;
 
   if (threadIdx.x == 0) {
-    // the score buffers and P are released / filled by the four softmax warps
-    for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(bar(i), (i == B_S_EMPTY || i == B_S_EMPTY + 1 || i == B_P_FULL) ? 4 : 1);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_P_FULL || i == B_P_FULL + 1) ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -93,17 +97,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      const int p0 = qb * kAttnBlk;
-      mbar_arrive_expect_tx(bar(B_Q_FULL), kTile);
-      tma_load_4d(sQ, &tmQKV, bar(B_Q_FULL), 0, slot_q, p0, sq);
-      tma_load_4d(sQ + kHalf, &tmQKV, bar(B_Q_FULL), 64, slot_q, p0, sq);
-      // armed[b]: parity of the last phase armed on K/V full barrier b (bit set = armed)
+      mbar_arrive_expect_tx(bar(B_Q_FULL), kTile * static_cast<uint32_t>(ntiles));
+      for (int x = 0; x < ntiles; ++x) {
+        const int p0 = (q0 + x) * kAttnBlk;
+        tma_load_4d(sQ + x * kTile, &tmQKV, bar(B_Q_FULL), 0, slot_q, p0, sq);
+        tma_load_4d(sQ + x * kTile + kHalf, &tmQKV, bar(B_Q_FULL), 64, slot_q, p0, sq);
+      }
       uint32_t k_armed = 0, k_ph = 0, v_armed = 0, v_ph = 0;
       bool ok = true;
-      for (int kv = 0; kv < nkv && ok; ++kv) {
-        const int b = kv & 1;
-        const uint32_t use = static_cast<uint32_t>(kv >> 1) & 1u;
-        const int pos = kv * kAttnBlk;
+      for (int j = 0; j < nblk && ok; ++j) {
+        const int b = j & 1;
+        const uint32_t use = static_cast<uint32_t>(j >> 1) & 1u;
+        const int pos = j * kAttnBlk;
         if (!mbar_wait(bar(B_K_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 1)) {
           ok = false;
           break;
@@ -137,152 +142,150 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // ---------------- MMA issuer
       constexpr uint32_t kIdQK = idesc_bf16_f32(kAttnBlk, kAttnBlk, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(kAttnBlk, kAttnD, false, true);
-      const uint32_t tO = tmem_base + 256u;
-      auto issue_qk = [&](int kv) -> bool {
-        const int b = kv & 1;
-        const uint32_t use = static_cast<uint32_t>(kv >> 1) & 1u;
-        if (!mbar_wait(bar(B_K_FULL + b), use, abort_flag, err, a.err_site + 3)) return false;
-        if (!mbar_wait(bar(B_S_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 4)) return false;
+      const int last_tile = ntiles - 1;  // the tile with the most blocks: the last user of K_j, V_j
+      // S_x = Q_x K_j^T into TMEM columns 128 x
+      auto issue_qk = [&](int x, int j) -> bool {
+        const int b = j & 1;
+        if (!mbar_wait(bar(B_K_FULL + b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, err, a.err_site + 3))
+          return false;
         tc_fence_after();
-        const uint32_t kb = sK + b * kTile;
+        const uint32_t kb = sK + b * kTile, qb = sQ + x * kTile;
 #pragma unroll
         for (int kk = 0; kk < kAttnD / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>(kk >> 2) * kHalf + static_cast<uint32_t>(kk & 3) * 32u;
-          umma_bf16(tmem_base + b * 128u, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdQK,
+          umma_bf16(tmem_base + 128u * x, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdQK,
                     static_cast<uint32_t>(kk != 0));
         }
-        umma_commit(bar(B_K_EMPTY + b));
-        umma_commit(bar(B_S_FULL + b));
+        umma_commit(bar(B_S_FULL + x));
+        if (x == last_tile) umma_commit(bar(B_K_EMPTY + b));
         return true;
       };
       bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, err, a.err_site + 5);
-      if (ok) ok = issue_qk(0);
-      for (int kv = 0; kv < nkv && ok; ++kv) {
-        if (kv + 1 < nkv && !issue_qk(kv + 1)) {
-          ok = false;
-          break;
-        }
-        const int b = kv & 1;
-        const uint32_t use = static_cast<uint32_t>(kv >> 1) & 1u;
-        if (!mbar_wait(bar(B_P_FULL), static_cast<uint32_t>(kv & 1), abort_flag, err, a.err_site + 6) ||
-            !mbar_wait(bar(B_V_FULL + b), use, abort_flag, err, a.err_site + 7)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t vb = sV + b * kTile;
+      for (int x = 0; x < ntiles && ok; ++x) ok = issue_qk(x, 0);
+      for (int j = 0; j < nblk && ok; ++j) {
+        const int b = j & 1;
+        for (int x = 0; x < ntiles && ok; ++x) {
+          if (j > q0 + x) continue;  // tile x is done
+          if (!mbar_wait(bar(B_P_FULL + x), static_cast<uint32_t>(j & 1), abort_flag, err, a.err_site + 6) ||
+              !mbar_wait(bar(B_V_FULL + b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, err, a.err_site + 7)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = sV + b * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kAttnBlk / 16; ++kk) {
-          const uint32_t aoff = static_cast<uint32_t>(kk >> 2) * kHalf + static_cast<uint32_t>(kk & 3) * 32u;
-          // V is [position][d]: for the MMA's B operand (N = d, K = position) it is MN-major; the
-          // two 64-column panels of d sit kHalf apart, 8-row groups of positions 1024 bytes apart
-          umma_bf16(tO, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(vb + static_cast<uint32_t>(kk) * 2048u, kHalf, 1024),
-                    kIdPV, static_cast<uint32_t>((kv | kk) != 0));
+          for (int kk = 0; kk < kAttnBlk / 16; ++kk)
+            // A = P_x from TMEM (8 columns of bf16 pairs per K step of 16); B = V_j, MN-major: its
+            // two 64-column panels of d sit kHalf apart, 8-row groups of positions 1024 bytes apart
+            umma_bf16_tmem_a(tmem_base + 256u + 128u * x, tmem_base + 128u * x + 8u * kk,
+                             sdesc_sw128(vb + static_cast<uint32_t>(kk) * 2048u, kHalf, 1024), kIdPV,
+                             static_cast<uint32_t>((j | kk) != 0));
+          umma_commit(bar(B_PV_DONE + x));
+          if (x == last_tile) umma_commit(bar(B_V_EMPTY + b));
+          if (j + 1 <= q0 + x && !issue_qk(x, j + 1)) ok = false;
         }
-        umma_commit(bar(B_V_EMPTY + b));
-        umma_commit(bar(B_PV_DONE));
       }
       // every MMA this thread issued has completed once the drain barrier flips
       umma_commit(bar(B_DRAIN));
       attn_wait_drain(bar(B_DRAIN), 0);
     }
   } else {
-    // ---------------- softmax warps: query row `row` of the block
+    // ---------------- softmax warps: tile x, query row `row` of the tile
+    const int x = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int q_pos = qb * kAttnBlk + row;
-    const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int qblk = q0 + x;
+    const int q_pos = qblk * kAttnBlk + row;
+    const uint32_t lq = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem_base + lq + 128u * x, tO = tmem_base + lq + 256u + 128u * x;
     float m_run = -INFINITY, l_run = 0.0f;
-    bool ok = true;
-    for (int kv = 0; kv < nkv; ++kv) {
-      const int b = kv & 1;
-      const uint32_t use = static_cast<uint32_t>(kv >> 1) & 1u;
-      ok = mbar_wait(bar(B_S_FULL + b), use, abort_flag, err, a.err_site + 8);
+    bool ok = x < ntiles;
+    for (int j = 0; ok && j <= qblk; ++j) {
+      ok = mbar_wait(bar(B_S_FULL + x), static_cast<uint32_t>(j & 1), abort_flag, err, a.err_site + 8);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tq + b * 128u + 0u, r0);
-      tmem_ld32(tq + b * 128u + 32u, r1);
-      tmem_ld32(tq + b * 128u + 64u, r2);
-      tmem_ld32(tq + b * 128u + 96u, r3);
+      tmem_ld32(tS + 0u, r0);
+      tmem_ld32(tS + 32u, r1);
+      tmem_ld32(tS + 64u, r2);
+      tmem_ld32(tS + 96u, r3);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_S_EMPTY + b));  // the score buffer may be overwritten
-      float x[128];
+      float xs[128];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        x[e] = __uint_as_float(r0[e]) * a.scale_log2;
-        x[32 + e] = __uint_as_float(r1[e]) * a.scale_log2;
-        x[64 + e] = __uint_as_float(r2[e]) * a.scale_log2;
-        x[96 + e] = __uint_as_float(r3[e]) * a.scale_log2;
+        xs[e] = __uint_as_float(r0[e]) * a.scale_log2;
+        xs[32 + e] = __uint_as_float(r1[e]) * a.scale_log2;
+        xs[64 + e] = __uint_as_float(r2[e]) * a.scale_log2;
+        xs[96 + e] = __uint_as_float(r3[e]) * a.scale_log2;
       }
-      if (kv == qb) {  // diagonal block: key position kv*128 + c attends only if <= q_pos
-        const int lim = q_pos - kv * kAttnBlk;
+      if (j == qblk) {  // diagonal block: key position j*128 + c attends only if <= q_pos
+        const int lim = q_pos - j * kAttnBlk;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c > lim) x[c] = -INFINITY;
+          if (c > lim) xs[c] = -INFINITY;
       }
       float mx = m_run;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, xs[c]);
       const float alpha = exp2f(m_run - mx);  // 0 on the first block (m_run = -inf)
       float sum = 0.0f;
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
-        x[c] = exp2f(x[c] - mx);
-        sum += x[c];
+        xs[c] = exp2f(xs[c] - mx);
+        sum += xs[c];
       }
       l_run = l_run * alpha + sum;
       m_run = mx;
-      if (kv > 0) {
-        // P and O are free once the previous block's O += P V has completed
-        ok = mbar_wait(bar(B_PV_DONE), static_cast<uint32_t>((kv - 1) & 1), abort_flag, err, a.err_site + 9);
+      if (j > 0) {
+        // O_x and the P_x columns are free once the previous block's O_x += P_x V has completed
+        ok = mbar_wait(bar(B_PV_DONE + x), static_cast<uint32_t>((j - 1) & 1), abort_flag, err, a.err_site + 9);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tq + 256u + static_cast<uint32_t>(c * 32), o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tq + 256u + static_cast<uint32_t>(c * 32), o);
-          }
-          tmem_st_wait();
-        }
       }
-      // P row -> bf16, 16-byte unit u of panel (u >> 3) at position (u & 7) ^ (row & 7)
+      // P_x -> bf16 pairs into the first 64 columns of S_x (the scores are in registers)
+      {
+        uint32_t pk[32];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const uint32_t addr = sP + static_cast<uint32_t>(u >> 3) * kHalf + static_cast<uint32_t>(row) * 128u +
-                              ((static_cast<uint32_t>(u & 7) ^ (static_cast<uint32_t>(row) & 7u)) << 4);
-        st_shared_v4(addr, pack_bf16x2(x[8 * u], x[8 * u + 1]), pack_bf16x2(x[8 * u + 2], x[8 * u + 3]),
-                     pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(xs[2 * c], xs[2 * c + 1]);
+        tmem_st32(tS + 0u, pk);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(xs[64 + 2 * c], xs[64 + 2 * c + 1]);
+        tmem_st32(tS + 32u, pk);
       }
-      fence_proxy_async_smem();  // P visible to the tensor core
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL));
-    }
-    if (ok) {
-      ok = mbar_wait(bar(B_PV_DONE), static_cast<uint32_t>((nkv - 1) & 1), abort_flag, err, a.err_site + 10);
-      if (__all_sync(0xFFFFFFFFu, ok)) {
-        tc_fence_after();
-        const float inv = 1.0f / l_run;
-        // the P tile is free: each warp stages its 32 rows as two 32 x 64 boxes (128-byte swizzle)
-        const uint32_t stage = sP + static_cast<uint32_t>(warp - 2) * 8192u;
+      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tmem_ld32(tq + 256u + static_cast<uint32_t>(c * 32), o);
+          tmem_ld32(tO + static_cast<uint32_t>(c * 32), o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + static_cast<uint32_t>(c * 32), o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P_FULL + x));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(B_PV_DONE + x), static_cast<uint32_t>(qblk & 1), abort_flag, err, a.err_site + 10);
+      if (__all_sync(0xFFFFFFFFu, ok)) {
+        tc_fence_after();
+        const float inv = 1.0f / l_run;
+        // the tile's Q buffer is free (its last product has completed): each warp stages its 32
+        // rows as two 32 x 64 boxes (128-byte swizzle)
+        const uint32_t stage = sQ + x * kTile + static_cast<uint32_t>(quarter) * 8192u;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + static_cast<uint32_t>(c * 32), o);
           tmem_ld_wait();
           const uint32_t box = stage + static_cast<uint32_t>(c >> 1) * 4096u + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        const int p0 = qb * kAttnBlk + quarter * 32;  // rows past the sequence end are clipped
+        const int p0 = qblk * kAttnBlk + quarter * 32;  // rows past the sequence end are clipped
         if (lane == 0 && p0 < a.seq) {
           tma_store_4d(&tmO, stage, 0, hd, p0, sq);
           tma_store_4d(&tmO, stage + 4096u, 64, hd, p0, sq);
@@ -327,7 +330,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_qkv, const CUtensorMap& tm_o,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attention_kernel<<<dim3(a.n_qblk, a.heads, nseq), kAttnThreads, kAttnSmem, st>>>(tm_qkv, tm_o, a);
+  attention_kernel<<<dim3((a.n_qblk + 1) / 2, a.heads, nseq), kAttnThreads, kAttnSmem, st>>>(tm_qkv, tm_o, a);
   return cudaGetLastError();
 }
 
