@@ -143,18 +143,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       constexpr uint32_t kIdQK = idesc_bf16_f32(kAttnBlk, kAttnBlk, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(kAttnBlk, kAttnD, false, true);
       const int last_tile = ntiles - 1;  // the tile with the most blocks: the last user of K_j, V_j
+      // Shared-memory descriptors are built once; a K step adds its byte offset / 16 to the start
+      // address field (bits 0-13: shared addresses below 256 KiB never carry out of it).
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dK0 = sdesc_sw128(sK, 16, 1024),
+                     dV0 = sdesc_sw128(sV, kHalf, 1024);
       // S_x = Q_x K_j^T into TMEM columns 128 x
       auto issue_qk = [&](int x, int j) -> bool {
         const int b = j & 1;
         if (!mbar_wait(bar(B_K_FULL + b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, err, a.err_site + 3))
           return false;
         tc_fence_after();
-        const uint32_t kb = sK + b * kTile, qb = sQ + x * kTile;
+        const uint64_t dq = dQ0 + ((static_cast<uint64_t>(x) * kTile) >> 4),
+                       dk = dK0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kAttnD / 16; ++kk) {
-          const uint32_t off = static_cast<uint32_t>(kk >> 2) * kHalf + static_cast<uint32_t>(kk & 3) * 32u;
-          umma_bf16(tmem_base + 128u * x, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdQK,
-                    static_cast<uint32_t>(kk != 0));
+          const uint64_t off = (static_cast<uint64_t>(kk >> 2) * kHalf + static_cast<uint64_t>(kk & 3) * 32u) >> 4;
+          umma_bf16(tmem_base + 128u * x, dq + off, dk + off, kIdQK, static_cast<uint32_t>(kk != 0));
         }
         umma_commit(bar(B_S_FULL + x));
         if (x == last_tile) umma_commit(bar(B_K_EMPTY + b));
@@ -172,14 +176,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t vb = sV + b * kTile;
+          const uint64_t dv = dV0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kAttnBlk / 16; ++kk)
             // A = P_x from TMEM (8 columns of bf16 pairs per K step of 16); B = V_j, MN-major: its
             // two 64-column panels of d sit kHalf apart, 8-row groups of positions 1024 bytes apart
             umma_bf16_tmem_a(tmem_base + 256u + 128u * x, tmem_base + 128u * x + 8u * kk,
-                             sdesc_sw128(vb + static_cast<uint32_t>(kk) * 2048u, kHalf, 1024), kIdPV,
-                             static_cast<uint32_t>((j | kk) != 0));
+                             dv + ((static_cast<uint64_t>(kk) * 2048u) >> 4), kIdPV, static_cast<uint32_t>((j | kk) != 0));
           umma_commit(bar(B_PV_DONE + x));
           if (x == last_tile) umma_commit(bar(B_V_EMPTY + b));
           if (j + 1 <= q0 + x && !issue_qk(x, j + 1)) ok = false;
@@ -207,37 +210,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tS + 0u, r0);
-      tmem_ld32(tS + 32u, r1);
-      tmem_ld32(tS + 64u, r2);
-      tmem_ld32(tS + 96u, r3);
-      tmem_ld_wait();
-      float xs[128];
+      // raw scores stay in the registers of the TMEM loads; the reductions use 8 independent
+      // accumulators each so that they are not one long dependency chain
+      uint32_t sr[4][32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        xs[e] = __uint_as_float(r0[e]) * a.scale_log2;
-        xs[32 + e] = __uint_as_float(r1[e]) * a.scale_log2;
-        xs[64 + e] = __uint_as_float(r2[e]) * a.scale_log2;
-        xs[96 + e] = __uint_as_float(r3[e]) * a.scale_log2;
-      }
+      for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32u * i, sr[i]);
+      tmem_ld_wait();
       if (j == qblk) {  // diagonal block: key position j*128 + c attends only if <= q_pos
         const int lim = q_pos - j * kAttnBlk;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c > lim) xs[c] = -INFINITY;
+          if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      float mx = m_run;
+      float m8[8];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, xs[c]);
-      const float alpha = exp2f(m_run - mx);  // 0 on the first block (m_run = -inf)
-      float sum = 0.0f;
+      for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        xs[c] = exp2f(xs[c] - mx);
-        sum += xs[c];
+      for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+#pragma unroll
+      for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+        for (int i = 0; i < k; ++i) m8[i] = fmaxf(m8[i], m8[i + k]);
+      // Running maximum in the log2 domain (the scale log2(e) / sqrt(d) is positive).  It is raised
+      // only when some row of the warp would exceed it by more than 8 (p <= 2^8 otherwise, harmless
+      // in fp32 and bf16); O and the sum are then rescaled by alpha.  Numerator and denominator always
+      // use the same maximum, so the result is unchanged.
+      const float cand = fmaxf(m_run, m8[0] * a.scale_log2);
+      const bool raise = __any_sync(0xFFFFFFFFu, cand > m_run + 8.0f) || j == 0;
+      const float mx = raise ? cand : m_run;
+      const float alpha = raise ? ex2_approx(m_run - mx) : 1.0f;  // 0 on the first block (m_run = -inf)
+      const float nmx = -mx;
+      float l8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) l8[k] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {  // p replaces the score in place
+        const float pv = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), a.scale_log2, nmx));
+        sr[c >> 5][c & 31] = __float_as_uint(pv);
+        l8[c & 7] += pv;
       }
-      l_run = l_run * alpha + sum;
+#pragma unroll
+      for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+        for (int i = 0; i < k; ++i) l8[i] += l8[i + k];
+      l_run = l_run * alpha + l8[0];
       m_run = mx;
       if (j > 0) {
         // O_x and the P_x columns are free once the previous block's O_x += P_x V has completed
@@ -249,16 +265,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
       }
       // P_x -> bf16 pairs into the first 64 columns of S_x (the scores are in registers)
-      {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(xs[2 * c], xs[2 * c + 1]);
-        tmem_st32(tS + 0u, pk);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(xs[64 + 2 * c], xs[64 + 2 * c + 1]);
-        tmem_st32(tS + 32u, pk);
+        for (int c = 0; c < 32; ++c) {
+          const int e = 64 * h2 + 2 * c;
+          pk[c] = pack_bf16x2(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]));
+        }
+        tmem_st32(tS + 32u * h2, pk);
       }
-      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+      if (j > 0 && raise) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
