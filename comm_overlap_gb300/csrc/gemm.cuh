@@ -516,9 +516,11 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtens
 // warp's 32 rows, in 32-column chunks staged as in epilogue_f32_tma.  A unit visits the shards of
 // an output tile consecutively, so the warp that handles these rows for shard g handled them for
 // every earlier shard too.  Shard 0 stores its fp32 partial into the sum S (out0, map m[0]); shard
-// g > 0 has the TMA unit add its partial into S at L2, issued only after the warp's writes for
-// shard g-1 completed, so every element of S receives ((P_0 + P_1) + ...) + P_g in shard order,
-// each add rounded to nearest.  After the last shard's adds complete, the rows are handed to the
+// g > 0 has the TMA unit add its partial into S at L2.  Each 32-column chunk is one bulk group and
+// every shard of a tile has the same number of chunks (nch), so the same chunk of shard g-1 was
+// committed nch groups earlier: waiting until at most nch - 1 groups are pending before issuing a
+// chunk's add orders it after that chunk's previous write, and every element of S receives
+// ((P_0 + P_1) + ...) + P_g in shard order, each add rounded to nearest.  After the last shard's adds complete, the rows are handed to the
 // finaliser warp of the same lane quarter (two-slot mbarrier ring `fin_ready` / `fin_done`,
 // counted by `nfin`).  Returns false if a bounded wait gave up.
 template <int NC, bool SCALE>
@@ -527,10 +529,7 @@ __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const Epi
                                                     uint32_t fin_ready, uint32_t fin_done, uint32_t& nfin,
                                                     int lane, volatile int* abort_flag, int* err) {
   if (row0 >= a.M) return true;
-  if (g > 0) {
-    if (lane == 0) bulk_wait_group_all();  // the writes of shard g-1 to these rows have completed
-    __syncwarp();
-  }
+  const int nch = (min(NC, a.N - col0) + 31) / 32;  // chunks of this sub-tile (the same for every shard)
 #pragma unroll 1
   for (int cc = 0; cc < NC; cc += 32) {
     if (col0 + cc >= a.N) break;
@@ -554,10 +553,12 @@ __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const Epi
     if (lane == 0) {
       // the sum stays in L2 until its tile is finalised
       const uint64_t keep = l2_policy_evict_last();
-      if (g == 0)
+      if (g == 0) {
         tma_store_3d_hint(&em.m[0], buf, col0 + cc, row0, 0, keep);
-      else
+      } else {
+        bulk_wait_group_upto(nch - 1);  // this chunk's write for shard g-1 has completed
         tma_reduce_add_3d_hint(&em.m[0], buf, col0 + cc, row0, 0, keep);
+      }
       bulk_commit_group();
     }
     ++nchunk;

@@ -169,6 +169,27 @@ __device__ __forceinline__ void bulk_wait_group_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// Wait until at most N of the most recently committed bulk groups are still pending (the older
+// ones have completed, writes performed).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// bulk_wait_group<n> for a run-time n in [0, 7].
+__device__ __forceinline__ void bulk_wait_group_upto(int n) {
+  switch (n) {
+    case 0: bulk_wait_group<0>(); break;
+    case 1: bulk_wait_group<1>(); break;
+    case 2: bulk_wait_group<2>(); break;
+    case 3: bulk_wait_group<3>(); break;
+    case 4: bulk_wait_group<4>(); break;
+    case 5: bulk_wait_group<5>(); break;
+    case 6: bulk_wait_group<6>(); break;
+    default: bulk_wait_group<7>(); break;
+  }
+}
+
 // Wait until every committed bulk group has completed.
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
