@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -52,11 +53,20 @@ NCU_TRAFFIC = {
 }
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines, so that comment edits keep the hash."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_sha() -> str:
+    """SHA-256 (16 hex digits) of the code, comments excluded, of the kernel sources that the
+    bench's MLP workloads run."""
     h = hashlib.sha256()
     for f in ("gemm.cuh", "ptx.cuh", "actfn.cuh", "kernels.h", "elementwise.cu"):
-        with open(os.path.join(ROOT, "comm_overlap_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "comm_overlap_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

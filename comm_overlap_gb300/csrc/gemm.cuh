@@ -1,15 +1,19 @@
 // gemm.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a with fused epilogues.
 //
-// One CTA per SM loops over output tiles.  Warp roles:
-//   warp 0 (one lane)  TMA producer: loads the A tile (128 x 64) and B tile (256 x 64) of each
-//                      K step into a 4-stage shared-memory ring (128-byte swizzle).
-//   warp 1 (one lane)  MMA issuer: tcgen05.mma 128x256x16 into one of two TMEM accumulators
-//                      (2 x 256 fp32 columns), commits to the ring's "empty" barriers and to
-//                      the accumulator's "full" barrier.  Warp 1 also owns TMEM alloc/dealloc.
-//   warps 2-5          epilogue: tcgen05.ld of the accumulator (each warp reads its 32-lane
-//                      quarter, one row per thread), applies the epilogue and writes global
-//                      memory, then releases the accumulator so tile i+1's epilogue overlaps
-//                      tile i+2's main loop.
+// A CTA pair (cluster of 2, one CTA per SM) loops over 256 x 256 output tiles (128 x 256 per CTA;
+// the gated first linear: 256 x 128 outputs from 256 gate + up columns) with
+// tcgen05.mma.cta_group::2.  Warp roles in each CTA:
+//   warp 0 (one lane)  TMA producer: per K step, its 128 rows of A and its 128-row half of B
+//                      (128 bytes of K: 64 bf16 or 128 E4M3 codes) into a 6-stage shared-memory
+//                      ring (128-byte swizzle); both CTAs' copies complete on the leader's barrier.
+//   warp 1             TMEM alloc/dealloc (pair-wide); lane 0 of the leader issues the MMAs into
+//                      one of two TMEM accumulators (2 x 256 fp32 columns) and commits them,
+//                      multicast to both CTAs, to the ring's "empty" and the accumulator's "full"
+//                      barriers.
+//   warps 2-5          epilogue: tcgen05.ld of the accumulator (each warp its 32-lane quarter, one
+//                      row per thread), the variant's epilogue, then the accumulator is handed
+//                      back so tile i+1's epilogue overlaps tile i+2's main loop.
+//   warps 6-9          (fused shard-sum only) finalisers: sum -> bf16 output.
 // Every wait is bounded (ptx.cuh); on expiry the CTA drains what it has in flight, frees TMEM
 // and returns, leaving a code in the translation unit's error word.
 #pragma once
@@ -867,8 +871,8 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     finalize_sum_rows(args, unit, units, R::kTileM, static_cast<int>(rank) * kBM + quarter * 32,
                       bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), lane, abort_flag, err);
   } else {
-    // ---------------- epilogue warps 2..: TMEM lane quarter = warp % 4; with 8 epilogue warps,
-    // warps 2-5 take the first half of the accumulator's columns and warps 6-9 the second
+    // ---------------- epilogue warps 2-5: TMEM lane quarter = warp % 4 (the column split below
+    // generalises to more than one warp per quarter; every variant uses one)
     constexpr int kParts = epi_warps<EPI>() / 4;
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
