@@ -29,7 +29,7 @@ def lib():
     assert st == 0, f"device error word set: site {site:#x}"
 
 
-@pytest.mark.parametrize("sched", [dm.SCHED_SERIAL, dm.SCHED_INTRA])
+@pytest.mark.parametrize("sched", [dm.SCHED_SERIAL, dm.SCHED_INTRA, dm.SCHED_FUSED])
 def test_fwd_bwd_graph_replay_bit_identical(lib, sched):
     import torch
     M, h, Fi, t, p, q, act = 512, 256, 192, 4, 2, 2, synth.ACT_SWIGLU
@@ -92,3 +92,52 @@ def test_stack_graph_replay_bit_identical(lib):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(host_bits(out), ref)
+
+
+def replay_matches(fn, out):
+    """Eager call, then capture + replay on a side stream; the replayed output must match bit for bit."""
+    import torch
+    fn(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ref = host_bits(out) if out.dtype == torch.bfloat16 else out.cpu().numpy().copy()
+    out.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fn(side)
+    g.replay()
+    torch.cuda.synchronize()
+    got = host_bits(out) if out.dtype == torch.bfloat16 else out.cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("sched", [dm.SCHED_INTER, dm.SCHED_FUSED])
+def test_block_graph_replay_bit_identical(lib, sched):
+    """The Transformer block stack (attention kernel included) under capture."""
+    import torch
+    L, nseq, seq, h, heads, F, t, p, q = 2, 2, 128, 256, 2, 512, 2, 2, 2
+    s = synth.MlpShape("b", nseq * seq, h, F, synth.ACT_GELU, t, p, q, layers=L, layernorm=True, seq=seq,
+                       heads=heads, w_std=0.0625)
+    d = synth.make_inputs(s, seed=23)
+    Z, Wq, Wo, A, B = (dev_bf16(d[k]) for k in ("X", "Wqkv", "Wo", "A", "B"))
+    cfg = dm.make_cfg(s.M, h, F, t, p, q, synth.ACT_GELU, sched=sched, layers=L, heads=heads, seq=seq)
+    n = dm.domino_workspace_size(cfg, dm.PASS_BLOCK)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(Z)
+    replay_matches(lambda st: dm.domino_block_fwd(lib.h, cfg, Z, Wq, Wo, A, B, out, ws, n, st), out)
+
+
+def test_fp8_graph_replay_bit_identical(lib):
+    import torch
+    M, h, Fi, t, p, q = 512, 256, 128, 4, 2, 1
+    sc = (2.0 ** -6, 2.0 ** -11, 2.0 ** -11, 2.0 ** -7)
+    u8 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    X8 = u8(synth.e4m3_codes((M, h), 1.0, sc[0], 24, synth.TID_X))
+    A8 = u8(synth.e4m3_codes((2 * Fi * t, h), 0.02, sc[1], 24, synth.TID_A))
+    B8 = u8(synth.e4m3_codes((t, h, Fi), 0.02, sc[2], 24, synth.TID_B))
+    cfg = dm.make_cfg(M, h, Fi * t, t, p, q, synth.ACT_SWIGLU, sched=dm.SCHED_INTRA)
+    n = dm.domino_workspace_size(cfg, dm.PASS_FWD_FP8)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    Y = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+    replay_matches(lambda st: dm.domino_mlp_fwd_fp8(lib.h, cfg, X8, A8, B8, sc, Y, ws, n, st), Y)
