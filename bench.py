@@ -238,6 +238,27 @@ def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
     return flops, dt, what
 
 
+def reduction_roofline(kern: dict, work: dict, peaks: dict, workload: str, sha: str):
+    """The shard-sum (the AllReduce stand-in) against the HBM roofline: algorithmic bytes per launch
+    over its live event duration.  It runs concurrently with the GEMMs of the next chunk, so the
+    live figure shares HBM with them; null when the schedule fuses the reduction into the GEMM."""
+    k = kern.get("shard_sum")
+    if not k or not k["launches"]:
+        return None
+    avg_ms = k["total_ms"] / k["launches"]
+    gbs = work["shard_sum"][1] / (avg_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": "shard_sum", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": work["shard_sum"][1],
+            "avg_launch_ms": avg_ms, "concurrent_with_gemms": True,
+            "traffic": traffic_per_launch(workload, "shard_sum", sha)}
+
+
+def traffic_per_launch(workload: str, kernel: str, sha: str):
+    """ncu DRAM bytes per launch of a kernel on a workload, if captured on the current kernel code."""
+    t = NCU_TRAFFIC.get((workload, kernel))
+    return t["bytes_per_launch"] if t and t.get("src_sha") == sha else None
+
+
 def fp8_inputs(s: synth.MlpShape) -> dict:
     """E4M3 codes of the workload's draws with power-of-two per-tensor scales: X ~ N(0, 1) at 2^-6,
     the weights ~ N(0, 0.02) at 2^-11, and the first-linear output at 2^-6 (GeLU) or 2^-5 (SwiGLU),
@@ -464,8 +485,7 @@ def run_ours(args, rank, world, local_rank):
     bound, per_launch = work[dom]
     avg_ms = kern[dom]["total_ms"] / kern[dom]["launches"]
     sha = kernel_source_sha()
-    traffic = NCU_TRAFFIC.get((s.name, dom))
-    traffic_val = traffic["bytes_per_launch"] if traffic and traffic.get("src_sha") == sha else None
+    traffic_val = traffic_per_launch(s.name, dom, sha)
     # FP8 contractions: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25 = 2.  The
     # sustained (power-capped) peak applies when the run hit the power cap; a run that held its
     # clocks (short steps) is held to the burst figure.
@@ -503,6 +523,7 @@ def run_ours(args, rank, world, local_rank):
                            "of_burst": value / world / (peaks["bf16_tflops"] * peak_scale),
                            "peaks": peaks["source"] + (" x 2 for e4m3" if fp8 else "")},
            "roofline": roof,
+           "reduction": reduction_roofline(kern, work, peaks, s.name, sha),
            "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
            "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
     if fp8:

@@ -74,3 +74,26 @@ def test_reference_arm_only_rank0_reports():
     a = A()
     a.shape = synth.SHAPES["tiny_gelu"]
     assert bench.run_reference(a, rank=1) is None
+
+
+def test_reduction_roofline_and_traffic_lookup():
+    s = synth.SHAPES["llama3_8b_swiglu_fwdbwd"]
+    work = bench.kernel_work(s)
+    peaks = {"hbm_gbs": 6794.5}
+    kern = {"shard_sum": {"launches": 4, "total_ms": 4 * 0.34}}
+    r = bench.reduction_roofline(kern, work, peaks, s.name, bench.kernel_source_sha())
+    m, n = s.M // s.p, s.h // s.q
+    assert r["algorithmic_bytes_per_launch"] == s.t * m * n * 4 + m * n * 2
+    assert abs(r["achieved"] - r["algorithmic_bytes_per_launch"] / 0.34e-3 / 1e9) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 6794.5) < 1e-12
+    # the fused schedule launches no shard-sum: no reduction roofline
+    assert bench.reduction_roofline({}, work, peaks, s.name, "x") is None
+    # traffic is reported only for the kernel code it was captured on
+    assert bench.traffic_per_launch(s.name, "shard_sum", bench.kernel_source_sha()) is not None
+    assert bench.traffic_per_launch(s.name, "shard_sum", "0" * 16) is None
+    assert bench.traffic_per_launch("tiny_gelu", "shard_sum", bench.kernel_source_sha()) is None
+
+
+def test_kernel_hash_ignores_comments():
+    code = "int a; // note\n/* block\n comment */ int b;\n\n"
+    assert bench._code_only(code) == bench._code_only("int a;\n int b;")
