@@ -238,19 +238,48 @@ def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
     return flops, dt, what
 
 
-def reduction_roofline(kern: dict, work: dict, peaks: dict, workload: str, sha: str):
+def reduction_roofline(kern: dict, work: dict, peaks: dict, workload: str, sha: str, alone_ms=None):
     """The shard-sum (the AllReduce stand-in) against the HBM roofline: algorithmic bytes per launch
-    over its live event duration.  It runs concurrently with the GEMMs of the next chunk, so the
-    live figure shares HBM with them; null when the schedule fuses the reduction into the GEMM."""
+    over its event duration, live (concurrent with the GEMMs of the next chunk, sharing HBM with
+    them) and, when measured, alone on the same sizes.  Null when the schedule fuses the reduction
+    into the GEMM."""
     k = kern.get("shard_sum")
     if not k or not k["launches"]:
         return None
+    nbytes = work["shard_sum"][1]
     avg_ms = k["total_ms"] / k["launches"]
-    gbs = work["shard_sum"][1] / (avg_ms * 1e-3) / 1e9
-    return {"bound": "hbm", "kernel": "shard_sum", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": work["shard_sum"][1],
-            "avg_launch_ms": avg_ms, "concurrent_with_gemms": True,
-            "traffic": traffic_per_launch(workload, "shard_sum", sha)}
+    gbs = nbytes / (avg_ms * 1e-3) / 1e9
+    out = {"bound": "hbm", "kernel": "shard_sum", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": avg_ms,
+           "concurrent_with_gemms": True, "traffic": traffic_per_launch(workload, "shard_sum", sha)}
+    if alone_ms:
+        alone = nbytes / (alone_ms * 1e-3) / 1e9
+        out["alone"] = {"achieved": alone, "frac": alone / peaks["hbm_gbs"], "avg_launch_ms": alone_ms}
+    return out
+
+
+def shard_sum_alone(s: synth.MlpShape, stream, reps: int = 10):
+    """Average duration (ms) of the shard-sum alone, on the workload's partial size (t x m x n fp32
+    in, m x n bf16 out, plus the residual for layer stacks), timed with CUDA events."""
+    import torch
+
+    from comm_overlap_gb300 import domino as dm
+    m, n = s.M // s.p, s.h // s.q
+    P = torch.randn(s.t, m, n, device="cuda")
+    Y = torch.empty((m, s.h), dtype=torch.bfloat16, device="cuda")
+    res = torch.zeros((m, s.h), dtype=torch.bfloat16, device="cuda") if s.layernorm else None
+    for _ in range(3):
+        dm.domino_shard_sum(P, s.t, m, n, res, s.h, Y, s.h, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        dm.domino_shard_sum(P, s.t, m, n, res, s.h, Y, s.h, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    del P, Y, res
+    torch.cuda.empty_cache()
+    return ms
 
 
 def traffic_per_launch(workload: str, kernel: str, sha: str):
@@ -471,6 +500,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     ms_e2e = e0.elapsed_time(e1)
     dm.domino_destroy(h)
+    ss_alone = shard_sum_alone(s, stream) if "shard_sum" in kern and not fp8 else None
 
     ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, "cuda")
     if rank != 0:
@@ -523,7 +553,7 @@ def run_ours(args, rank, world, local_rank):
                            "of_burst": value / world / (peaks["bf16_tflops"] * peak_scale),
                            "peaks": peaks["source"] + (" x 2 for e4m3" if fp8 else "")},
            "roofline": roof,
-           "reduction": reduction_roofline(kern, work, peaks, s.name, sha),
+           "reduction": reduction_roofline(kern, work, peaks, s.name, sha, ss_alone),
            "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
            "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
     if fp8:
