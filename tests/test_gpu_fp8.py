@@ -118,3 +118,22 @@ def test_fp8_validation(handle):
     with pytest.raises(dm.DominoError) as e:
         dm.domino_mlp_fwd_fp8(handle, dm.make_cfg(64, 64, 64, 2), z, z, z, (1, 1, 0, 1), Y, None, 0)
     assert e.value.status == 1
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("workload", ["llama2_7b_swiglu", "gpt3_2.7b_mlp"])
+def test_fp8_full_size_sampled(handle, workload):
+    """The FP8 forward at the full size the bench times (its inputs and scales), fused schedule:
+    sampled rows against the oracle, and bit-identical to the two-stream schedule."""
+    import torch
+
+    import bench
+    s = synth.SHAPES[workload]
+    inp = bench.fp8_inputs(s)
+    X8, A8, B8, sc = inp["X"], inp["A"], inp["B"], inp["scales"]
+    Yf = run_fp8(handle, X8, A8, B8, s.t, s.act, sc, s.p, s.q, dm.SCHED_FUSED)
+    Yi = run_fp8(handle, X8, A8, B8, s.t, s.act, sc, s.p, s.q, dm.SCHED_INTRA)
+    assert np.array_equal(host_bits(Yf), host_bits(Yi))
+    rows = synth.sample_indices(s.M, 6, 73)
+    ref = oracle.mlp_fwd_fp8(X8, A8, B8, s.t, s.act, sc, rows=rows)
+    assert_tol(host_f64(Yf[torch.from_numpy(rows).cuda()]), ref, "FP8 forward, sampled rows")
