@@ -3,24 +3,30 @@
 // XAB=Y, A is the multi-head attention, B the output projection).  Heads are split over the t
 // shards; shard i's query/key/value heads come from its own slice of the fused projection output.
 //
-// One CTA computes two consecutive query blocks of 128 positions (tiles 0 and 1) of one head and
+// Work item: two consecutive query blocks of 128 positions (tiles 0 and 1) of one head and
 // sequence: O = softmax(Q K^T / sqrt(d) + causal mask) V, with an online softmax over key/value
 // blocks of 128 positions (running maximum and sum rescaled as blocks arrive; equal to the plain
 // softmax up to rounding).  Both tiles use the same K_j, V_j, and their work alternates on the
 // tensor core so that one tile's softmax runs under the other tile's matrix products.
+// The kernel is persistent: one CTA per SM walks a fixed list of units, a unit being the heaviest
+// and the lightest remaining item of one (head, sequence), so that all units cost about the same;
+// consecutive CTAs take consecutive units, which keeps the K/V of the heads in flight in L2.  The
+// next item's Q tiles are loaded as soon as the current item's last Q K^T products have been
+// issued, and its first products start while the current item's O is being written out.
 // Warp roles:
-//   warp 0 (one lane)  TMA producer: both Q tiles once, then K and V tiles into two-deep rings.
+//   warp 0 (one lane)  TMA producer: each item's Q tiles, then its K and V tiles into two-deep rings
+//                      (the rings run on across items).
 //   warp 1 (one lane)  MMA issuer, per block j and tile x: O_x += P_x V_j as soon as the softmax
 //                      handed P_x over, then S_x = Q_x K_{j+1}^T (in that order: P_x lives in the
 //                      columns of S_x, and tensor-core operations of one thread run in order).
 //   warps 2-5, 6-9     softmax of tile 0 and tile 1, one query row per thread (TMEM lane quarter =
 //                      warp % 4): scores from TMEM, running max / sum in fp32, O_x rescaled in TMEM
 //                      when a row maximum grew, P rounded to bf16 and stored into TMEM; at the end
-//                      O / sum -> bf16 -> TMA store (staged in the tile's Q buffer).
+//                      of an item O / sum -> bf16 -> TMA store through a per-warp staging box.
 // TMEM: S_0 = columns 0-127, S_1 = 128-255 (P_x in the first 64 columns of S_x as bf16 pairs),
 // O_0 = 256-383, O_1 = 384-511.
-// Every wait is bounded (ptx.cuh); on expiry the CTA drains what it has in flight, frees TMEM and
-// returns, leaving a code in this translation unit's error word.
+// Every wait is bounded (ptx.cuh); on expiry the CTA stops issuing work, lets what it has in
+// flight drain, frees TMEM and returns, leaving a code in this translation unit's error word.
 #include <cuda_bf16.h>
 
 #include "actfn.cuh"
@@ -35,15 +41,18 @@ constexpr int kAttnD = 128;                         // head dimension
 constexpr int kAttnBlk = 128;                       // query rows / key-value positions per block
 constexpr uint32_t kTile = kAttnBlk * kAttnD * 2;   // 32 KiB: one Q, K or V tile
 constexpr uint32_t kHalf = kTile / 2;               // one 64-column (128-byte) swizzle panel
+constexpr uint32_t kOBox = 32 * 64 * 2;             // 4 KiB: one warp's 32 rows x 64 columns of O
 constexpr int kAttnThreads = 320;
-constexpr int kAttnSmem = 1024 /* alignment slack */ + 1024 /* control */ + 6 * kTile;  // Q[2], K[2], V[2]
+// alignment slack, control, Q[2], K[2], V[2], one O staging box per softmax warp
+constexpr int kAttnSmem = 1024 + 1024 + 6 * static_cast<int>(kTile) + 8 * static_cast<int>(kOBox);
+static_assert(kAttnSmem <= 232448, "shared memory beyond the per-CTA limit");
 constexpr uint32_t kAttnTmemCols = 512;
 constexpr uint64_t kAttnDrainNs = 200000000ull;
 
-// barrier indices
+// barrier indices (pairs are per tile or per ring slot)
 enum : int {
-  B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = 3, B_V_FULL = 5, B_V_EMPTY = 7, B_S_FULL = 9, B_P_FULL = 11,
-  B_PV_DONE = 13, B_DRAIN = 15, B_COUNT = 16
+  B_Q_FULL = 0, B_Q_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 6, B_V_FULL = 8, B_V_EMPTY = 10, B_S_FULL = 12,
+  B_P_FULL = 14, B_PV_DONE = 16, B_O_FREE = 18, B_DRAIN = 20, B_COUNT = 21
 };
 
 __device__ __forceinline__ void attn_wait_drain(uint32_t bar, uint32_t parity) {
@@ -53,9 +62,43 @@ __device__ __forceinline__ void attn_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// The work list.  Items of one (head, sequence) group: query-block pairs ip = 0 .. n_pairs - 1
+// (query blocks 2 ip and 2 ip + 1, key blocks 0 .. 2 ip + 1).  Unit k of a group holds item
+// n_pairs - 1 - k and, if different, item k; groups are numbered head-fastest.
+struct AttnWork {
+  int n_pairs, upg, units;
+  __device__ AttnWork(const AttnArgs& a, int nseq) {
+    n_pairs = (a.n_qblk + 1) >> 1;
+    upg = (n_pairs + 1) >> 1;
+    units = upg * a.heads * nseq;
+  }
+};
+
+struct AttnItem {
+  int hd, sq, q0, ntiles, nblk;
+};
+
+__device__ __forceinline__ AttnItem attn_item(const AttnArgs& a, const AttnWork& w, int u, int half) {
+  const int g = u / w.upg, k = u - g * w.upg;
+  const int ip = half == 0 ? w.n_pairs - 1 - k : k;
+  AttnItem it;
+  it.hd = g % a.heads;
+  it.sq = g / a.heads;
+  it.q0 = 2 * ip;
+  it.ntiles = (it.q0 + 1 < a.n_qblk) ? 2 : 1;
+  it.nblk = it.q0 + it.ntiles;  // key/value blocks 0 .. nblk - 1 (tile x stops at q0 + x)
+  return it;
+}
+
+// items in unit u: 2, or 1 when its heaviest and lightest item coincide
+__device__ __forceinline__ int attn_unit_items(const AttnWork& w, int u) {
+  const int k = u % w.upg;
+  return (k < w.n_pairs - 1 - k) ? 2 : 1;
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmO,
-                     const AttnArgs a) {
+                     const AttnArgs a, const int nseq) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -63,21 +106,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
   const uint32_t bar0 = smem_u32(smem);
   auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const uint32_t sQ = smem_u32(smem + 1024), sK = sQ + 2 * kTile, sV = sQ + 4 * kTile;
+  const uint32_t sQ = smem_u32(smem + 1024), sK = sQ + 2 * kTile, sV = sQ + 4 * kTile, sO = sQ + 6 * kTile;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_pairs = (a.n_qblk + 1) >> 1;
-  const int q0 = 2 * (n_pairs - 1 - static_cast<int>(blockIdx.x));  // longest (most key blocks) first
-  const int ntiles = (q0 + 1 < a.n_qblk) ? 2 : 1;
-  const int hd = blockIdx.y, sq = blockIdx.z;
-  const int shard = hd / a.nhi, jh = hd - shard * a.nhi;
-  const int slot_q = (shard * 3 + 0) * a.nhi + jh, slot_k = (shard * 3 + 1) * a.nhi + jh,
-            slot_v = (shard * 3 + 2) * a.nhi + jh;
-  const int nblk = q0 + ntiles;  // key/value blocks 0 .. q0 + ntiles - 1 (tile x stops at q0 + x)
+  const AttnWork w(a, nseq);
   int* err = &g_attn_err;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_P_FULL || i == B_P_FULL + 1) ? 4 : 1);
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(bar(i), (i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_FREE || i == B_O_FREE + 1) ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -97,242 +134,299 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      mbar_arrive_expect_tx(bar(B_Q_FULL), kTile * static_cast<uint32_t>(ntiles));
-      for (int x = 0; x < ntiles; ++x) {
-        const int p0 = (q0 + x) * kAttnBlk;
-        tma_load_4d(sQ + x * kTile, &tmQKV, bar(B_Q_FULL), 0, slot_q, p0, sq);
-        tma_load_4d(sQ + x * kTile + kHalf, &tmQKV, bar(B_Q_FULL), 64, slot_q, p0, sq);
-      }
-      uint32_t k_armed = 0, k_ph = 0, v_armed = 0, v_ph = 0;
+      uint32_t gb = 0;          // ring position of the item's key block 0
+      int nq[2] = {0, 0};       // items so far in which tile x took part
       bool ok = true;
-      for (int j = 0; j < nblk && ok; ++j) {
-        const int b = j & 1;
-        const uint32_t use = static_cast<uint32_t>(j >> 1) & 1u;
-        const int pos = j * kAttnBlk;
-        if (!mbar_wait(bar(B_K_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 1)) {
-          ok = false;
-          break;
+      for (int u = blockIdx.x; u < w.units && ok; u += gridDim.x) {
+        const int nit = attn_unit_items(w, u);
+        for (int half = 0; half < nit && ok; ++half) {
+          const AttnItem it = attn_item(a, w, u, half);
+          const int slot_q = ((it.hd / a.nhi) * 3 + 0) * a.nhi + it.hd % a.nhi;
+          for (int x = 0; x < it.ntiles; ++x) {
+            // tile x's Q buffer is free once its previous item's last Q K^T has completed
+            if (nq[x] > 0 && !mbar_wait(bar(B_Q_EMPTY + x), static_cast<uint32_t>(nq[x] - 1) & 1u, abort_flag, err,
+                                        a.err_site + 11)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(B_Q_FULL + x), kTile);
+            const int p0 = (it.q0 + x) * kAttnBlk;
+            tma_load_4d(sQ + x * kTile, &tmQKV, bar(B_Q_FULL + x), 0, slot_q, p0, it.sq);
+            tma_load_4d(sQ + x * kTile + kHalf, &tmQKV, bar(B_Q_FULL + x), 64, slot_q, p0, it.sq);
+            ++nq[x];
+          }
+          const int slot_k = slot_q + a.nhi, slot_v = slot_q + 2 * a.nhi;
+          for (int j = 0; j < it.nblk && ok; ++j) {
+            const uint32_t r = gb + static_cast<uint32_t>(j);
+            const int b = static_cast<int>(r & 1u);
+            const uint32_t use = (r >> 1) & 1u;
+            const int pos = j * kAttnBlk;
+            if (!mbar_wait(bar(B_K_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 1)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(B_K_FULL + b), kTile);
+            tma_load_4d(sK + b * kTile, &tmQKV, bar(B_K_FULL + b), 0, slot_k, pos, it.sq);
+            tma_load_4d(sK + b * kTile + kHalf, &tmQKV, bar(B_K_FULL + b), 64, slot_k, pos, it.sq);
+            if (!mbar_wait(bar(B_V_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 2)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(B_V_FULL + b), kTile);
+            tma_load_4d(sV + b * kTile, &tmQKV, bar(B_V_FULL + b), 0, slot_v, pos, it.sq);
+            tma_load_4d(sV + b * kTile + kHalf, &tmQKV, bar(B_V_FULL + b), 64, slot_v, pos, it.sq);
+          }
+          gb += static_cast<uint32_t>(it.nblk);
         }
-        mbar_arrive_expect_tx(bar(B_K_FULL + b), kTile);
-        k_armed |= 1u << b;
-        k_ph = (k_ph & ~(1u << b)) | (use << b);
-        tma_load_4d(sK + b * kTile, &tmQKV, bar(B_K_FULL + b), 0, slot_k, pos, sq);
-        tma_load_4d(sK + b * kTile + kHalf, &tmQKV, bar(B_K_FULL + b), 64, slot_k, pos, sq);
-        if (!mbar_wait(bar(B_V_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 2)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar(B_V_FULL + b), kTile);
-        v_armed |= 1u << b;
-        v_ph = (v_ph & ~(1u << b)) | (use << b);
-        tma_load_4d(sV + b * kTile, &tmQKV, bar(B_V_FULL + b), 0, slot_v, pos, sq);
-        tma_load_4d(sV + b * kTile + kHalf, &tmQKV, bar(B_V_FULL + b), 64, slot_v, pos, sq);
       }
       if (!ok) {
         // let the copies still in flight land before the CTA leaves
-        attn_wait_drain(bar(B_Q_FULL), 0);
-        for (int b = 0; b < 2; ++b) {
-          if ((k_armed >> b) & 1u) attn_wait_drain(bar(B_K_FULL + b), (k_ph >> b) & 1u);
-          if ((v_armed >> b) & 1u) attn_wait_drain(bar(B_V_FULL + b), (v_ph >> b) & 1u);
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000ull) {
         }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
       constexpr uint32_t kIdQK = idesc_bf16_f32(kAttnBlk, kAttnBlk, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(kAttnBlk, kAttnD, false, true);
-      const int last_tile = ntiles - 1;  // the tile with the most blocks: the last user of K_j, V_j
       // Shared-memory descriptors are built once; a K step adds its byte offset / 16 to the start
       // address field (bits 0-13: shared addresses below 256 KiB never carry out of it).
       const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dK0 = sdesc_sw128(sK, 16, 1024),
                      dV0 = sdesc_sw128(sV, kHalf, 1024);
-      // S_x = Q_x K_j^T into TMEM columns 128 x
-      auto issue_qk = [&](int x, int j) -> bool {
-        const int b = j & 1;
-        if (!mbar_wait(bar(B_K_FULL + b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, err, a.err_site + 3))
-          return false;
-        tc_fence_after();
-        const uint64_t dq = dQ0 + ((static_cast<uint64_t>(x) * kTile) >> 4),
-                       dk = dK0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
+      uint32_t gb = 0;
+      int nq[2] = {0, 0};
+      uint32_t cbm[2] = {0u, 0u};  // key blocks of tile x handed over so far (phase of P_FULL)
+      bool ok = true;
+      for (int u = blockIdx.x; u < w.units && ok; u += gridDim.x) {
+        const int nit = attn_unit_items(w, u);
+        for (int half = 0; half < nit && ok; ++half) {
+          const AttnItem it = attn_item(a, w, u, half);
+          const int last_tile = it.ntiles - 1;  // the tile with the most blocks: the last user of K_j, V_j
+          // S_x = Q_x K_j^T into TMEM columns 128 x; after tile x's last one its Q buffer is free
+          auto issue_qk = [&](int x, int j) -> bool {
+            const uint32_t r = gb + static_cast<uint32_t>(j);
+            const int b = static_cast<int>(r & 1u);
+            if (!mbar_wait(bar(B_K_FULL + b), (r >> 1) & 1u, abort_flag, err, a.err_site + 3)) return false;
+            tc_fence_after();
+            const uint64_t dq = dQ0 + ((static_cast<uint64_t>(x) * kTile) >> 4),
+                           dk = dK0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kAttnD / 16; ++kk) {
-          const uint64_t off = (static_cast<uint64_t>(kk >> 2) * kHalf + static_cast<uint64_t>(kk & 3) * 32u) >> 4;
-          umma_bf16(tmem_base + 128u * x, dq + off, dk + off, kIdQK, static_cast<uint32_t>(kk != 0));
-        }
-        umma_commit(bar(B_S_FULL + x));
-        if (x == last_tile) umma_commit(bar(B_K_EMPTY + b));
-        return true;
-      };
-      bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, err, a.err_site + 5);
-      for (int x = 0; x < ntiles && ok; ++x) ok = issue_qk(x, 0);
-      for (int j = 0; j < nblk && ok; ++j) {
-        const int b = j & 1;
-        for (int x = 0; x < ntiles && ok; ++x) {
-          if (j > q0 + x) continue;  // tile x is done
-          if (!mbar_wait(bar(B_P_FULL + x), static_cast<uint32_t>(j & 1), abort_flag, err, a.err_site + 6) ||
-              !mbar_wait(bar(B_V_FULL + b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, err, a.err_site + 7)) {
-            ok = false;
-            break;
+            for (int kk = 0; kk < kAttnD / 16; ++kk) {
+              const uint64_t off = (static_cast<uint64_t>(kk >> 2) * kHalf + static_cast<uint64_t>(kk & 3) * 32u) >> 4;
+              umma_bf16(tmem_base + 128u * x, dq + off, dk + off, kIdQK, static_cast<uint32_t>(kk != 0));
+            }
+            umma_commit(bar(B_S_FULL + x));
+            if (x == last_tile) umma_commit(bar(B_K_EMPTY + b));
+            if (j == it.q0 + x) umma_commit(bar(B_Q_EMPTY + x));
+            return true;
+          };
+          for (int x = 0; x < it.ntiles && ok; ++x)
+            ok = mbar_wait(bar(B_Q_FULL + x), static_cast<uint32_t>(nq[x]) & 1u, abort_flag, err, a.err_site + 5) &&
+                 issue_qk(x, 0);
+          for (int j = 0; j < it.nblk && ok; ++j) {
+            const uint32_t r = gb + static_cast<uint32_t>(j);
+            const int b = static_cast<int>(r & 1u);
+            for (int x = 0; x < it.ntiles && ok; ++x) {
+              if (j > it.q0 + x) continue;  // tile x is done
+              // P_FULL of tile x completes once per key block the tile processes, in this order
+              if (!mbar_wait(bar(B_P_FULL + x), cbm[x] & 1u, abort_flag, err, a.err_site + 6) ||
+                  !mbar_wait(bar(B_V_FULL + b), (r >> 1) & 1u, abort_flag, err, a.err_site + 7)) {
+                ok = false;
+                break;
+              }
+              // O_x is overwritten by the item's first product: the previous item's O_x must be read
+              if (j == 0 && nq[x] > 0 &&
+                  !mbar_wait(bar(B_O_FREE + x), static_cast<uint32_t>(nq[x] - 1) & 1u, abort_flag, err,
+                             a.err_site + 12)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t dv = dV0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < kAttnBlk / 16; ++kk)
+                // A = P_x from TMEM (8 columns of bf16 pairs per K step of 16); B = V_j, MN-major: its
+                // two 64-column panels of d sit kHalf apart, 8-row groups of positions 1024 bytes apart
+                umma_bf16_tmem_a(tmem_base + 256u + 128u * x, tmem_base + 128u * x + 8u * kk,
+                                 dv + ((static_cast<uint64_t>(kk) * 2048u) >> 4), kIdPV,
+                                 static_cast<uint32_t>((j | kk) != 0));
+              umma_commit(bar(B_PV_DONE + x));
+              if (x == last_tile) umma_commit(bar(B_V_EMPTY + b));
+              ++cbm[x];
+              if (j + 1 <= it.q0 + x && !issue_qk(x, j + 1)) ok = false;
+            }
           }
-          tc_fence_after();
-          const uint64_t dv = dV0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kAttnBlk / 16; ++kk)
-            // A = P_x from TMEM (8 columns of bf16 pairs per K step of 16); B = V_j, MN-major: its
-            // two 64-column panels of d sit kHalf apart, 8-row groups of positions 1024 bytes apart
-            umma_bf16_tmem_a(tmem_base + 256u + 128u * x, tmem_base + 128u * x + 8u * kk,
-                             dv + ((static_cast<uint64_t>(kk) * 2048u) >> 4), kIdPV, static_cast<uint32_t>((j | kk) != 0));
-          umma_commit(bar(B_PV_DONE + x));
-          if (x == last_tile) umma_commit(bar(B_V_EMPTY + b));
-          if (j + 1 <= q0 + x && !issue_qk(x, j + 1)) ok = false;
+          for (int x = 0; x < it.ntiles; ++x) ++nq[x];
+          gb += static_cast<uint32_t>(it.nblk);
         }
       }
       // every MMA this thread issued has completed once the drain barrier flips
       umma_commit(bar(B_DRAIN));
       attn_wait_drain(bar(B_DRAIN), 0);
     }
+    __syncwarp();
   } else {
     // ---------------- softmax warps: tile x, query row `row` of the tile
     const int x = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int qblk = q0 + x;
-    const int q_pos = qblk * kAttnBlk + row;
     const uint32_t lq = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem_base + lq + 128u * x, tO = tmem_base + lq + 256u + 128u * x;
-    float m_run = -INFINITY, l_run = 0.0f;
-    bool ok = x < ntiles;
-    for (int j = 0; ok && j <= qblk; ++j) {
-      ok = mbar_wait(bar(B_S_FULL + x), static_cast<uint32_t>(j & 1), abort_flag, err, a.err_site + 8);
-      if (!__all_sync(0xFFFFFFFFu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // raw scores stay in the registers of the TMEM loads; the reductions use 8 independent
-      // accumulators each so that they are not one long dependency chain
-      uint32_t sr[4][32];
+    const uint32_t obox = sO + static_cast<uint32_t>(warp - 2) * kOBox;
+    uint32_t cb = 0;  // key blocks this tile has processed (phase of S_FULL, P_FULL, PV_DONE)
+    bool ok = true;
+    for (int u = blockIdx.x; u < w.units && ok; u += gridDim.x) {
+      const int nit = attn_unit_items(w, u);
+      for (int half = 0; half < nit && ok; ++half) {
+        const AttnItem it = attn_item(a, w, u, half);
+        if (x >= it.ntiles) continue;
+        const int qblk = it.q0 + x;
+        const int q_pos = qblk * kAttnBlk + row;
+        float m_run = -INFINITY, l_run = 0.0f;
+        for (int j = 0; ok && j <= qblk; ++j, ++cb) {
+          ok = mbar_wait(bar(B_S_FULL + x), cb & 1u, abort_flag, err, a.err_site + 8);
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // raw scores stay in the registers of the TMEM loads; the reductions use 8 independent
+          // accumulators each so that they are not one long dependency chain
+          uint32_t sr[4][32];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32u * i, sr[i]);
-      tmem_ld_wait();
-      if (j == qblk) {  // diagonal block: key position j*128 + c attends only if <= q_pos
-        const int lim = q_pos - j * kAttnBlk;
+          for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32u * i, sr[i]);
+          tmem_ld_wait();
+          if (j == qblk) {  // diagonal block: key position j*128 + c attends only if <= q_pos
+            const int lim = q_pos - j * kAttnBlk;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-      }
-      float m8[8];
+            for (int c = 0; c < 128; ++c)
+              if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          }
+          float m8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+          for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+          for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
 #pragma unroll
-      for (int k = 4; k > 0; k >>= 1)
+          for (int k = 4; k > 0; k >>= 1)
 #pragma unroll
-        for (int i = 0; i < k; ++i) m8[i] = fmaxf(m8[i], m8[i + k]);
-      // Running maximum in the log2 domain (the scale log2(e) / sqrt(d) is positive).  It is raised
-      // only when some row of the warp would exceed it by more than 8 (p <= 2^8 otherwise, harmless
-      // in fp32 and bf16); O and the sum are then rescaled by alpha.  Numerator and denominator always
-      // use the same maximum, so the result is unchanged.
-      const float cand = fmaxf(m_run, m8[0] * a.scale_log2);
-      const bool raise = __any_sync(0xFFFFFFFFu, cand > m_run + 8.0f) || j == 0;
-      const float mx = raise ? cand : m_run;
-      const float alpha = raise ? ex2_approx(m_run - mx) : 1.0f;  // 0 on the first block (m_run = -inf)
-      const float nmx = -mx;
-      float l8[8];
+            for (int i = 0; i < k; ++i) m8[i] = fmaxf(m8[i], m8[i + k]);
+          // Running maximum in the log2 domain (the scale log2(e) / sqrt(d) is positive).  It is
+          // raised only when some row of the warp would exceed it by more than 8 (p <= 2^8
+          // otherwise, harmless in fp32 and bf16); O and the sum are then rescaled by alpha.
+          // Numerator and denominator always use the same maximum, so the result is unchanged.
+          const float cand = fmaxf(m_run, m8[0] * a.scale_log2);
+          const bool raise = __any_sync(0xFFFFFFFFu, cand > m_run + 8.0f) || j == 0;
+          const float mx = raise ? cand : m_run;
+          const float alpha = raise ? ex2_approx(m_run - mx) : 1.0f;  // 0 on the first block (m_run = -inf)
+          const float nmx = -mx;
+          // p = 2^(s scale - max), summed in fp32 and rounded to bf16 pairs as it is produced, so
+          // that only the 64 packed registers stay live across the wait below
+          float l8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) l8[k] = 0.0f;
+          for (int k = 0; k < 8; ++k) l8[k] = 0.0f;
+          uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {  // p replaces the score in place
-        const float pv = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), a.scale_log2, nmx));
-        sr[c >> 5][c & 31] = __float_as_uint(pv);
-        l8[c & 7] += pv;
-      }
+          for (int c = 0; c < 64; ++c) {
+            const int e = 2 * c;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[e >> 5][e & 31]), a.scale_log2, nmx));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]), a.scale_log2, nmx));
+            l8[e & 7] += p0;
+            l8[(e + 1) & 7] += p1;
+            pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+          }
 #pragma unroll
-      for (int k = 4; k > 0; k >>= 1)
+          for (int k = 4; k > 0; k >>= 1)
 #pragma unroll
-        for (int i = 0; i < k; ++i) l8[i] += l8[i + k];
-      l_run = l_run * alpha + l8[0];
-      m_run = mx;
-      if (j > 0) {
-        // O_x and the P_x columns are free once the previous block's O_x += P_x V has completed
-        ok = mbar_wait(bar(B_PV_DONE + x), static_cast<uint32_t>((j - 1) & 1), abort_flag, err, a.err_site + 9);
+            for (int i = 0; i < k; ++i) l8[i] += l8[i + k];
+          l_run = l_run * alpha + l8[0];
+          m_run = mx;
+          if (j > 0) {
+            // O_x and the P_x columns are free once the previous block's O_x += P_x V has completed
+            ok = mbar_wait(bar(B_PV_DONE + x), (cb - 1u) & 1u, abort_flag, err, a.err_site + 9);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          // P_x -> the first 64 columns of S_x
+          tmem_st32(tS, pk[0]);
+          tmem_st32(tS + 32u, pk[1]);
+          if (j > 0 && raise) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + static_cast<uint32_t>(c * 32), o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(tO + static_cast<uint32_t>(c * 32), o);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_P_FULL + x));
+        }
+        if (!ok) break;
+        // ---- end of the item: O_x / sum -> bf16, written out 64 columns at a time through this
+        // warp's staging box (32 rows x 64 columns, 128-byte swizzle)
+        ok = mbar_wait(bar(B_PV_DONE + x), (cb - 1u) & 1u, abort_flag, err, a.err_site + 10);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      // P_x -> bf16 pairs into the first 64 columns of S_x (the scores are in registers)
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int e = 64 * h2 + 2 * c;
-          pk[c] = pack_bf16x2(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]));
-        }
-        tmem_st32(tS + 32u * h2, pk);
-      }
-      if (j > 0 && raise) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + static_cast<uint32_t>(c * 32), o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + static_cast<uint32_t>(c * 32), o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL + x));
-    }
-    if (ok) {
-      ok = mbar_wait(bar(B_PV_DONE + x), static_cast<uint32_t>(qblk & 1), abort_flag, err, a.err_site + 10);
-      if (__all_sync(0xFFFFFFFFu, ok)) {
-        tc_fence_after();
         const float inv = 1.0f / l_run;
-        // the tile's Q buffer is free (its last product has completed): each warp stages its 32
-        // rows as two 32 x 64 boxes (128-byte swizzle)
-        const uint32_t stage = sQ + x * kTile + static_cast<uint32_t>(quarter) * 8192u;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + static_cast<uint32_t>(c * 32), o);
-          tmem_ld_wait();
-          const uint32_t box = stage + static_cast<uint32_t>(c >> 1) * 4096u + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t unit = static_cast<uint32_t>((c & 1) * 4 + k);
-            st_shared_v4(box + ((unit ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
-                         pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
-                         pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
-                         pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
-                         pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
         const int p0 = qblk * kAttnBlk + quarter * 32;  // rows past the sequence end are clipped
-        if (lane == 0 && p0 < a.seq) {
-          tma_store_4d(&tmO, stage, 0, hd, p0, sq);
-          tma_store_4d(&tmO, stage + 4096u, 64, hd, p0, sq);
-          bulk_commit_group();
-          bulk_wait_group_all();
+        const int slot_o = it.hd;
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t o[2][32];
+          tmem_ld32(tO + static_cast<uint32_t>(h2 * 64), o[0]);
+          tmem_ld32(tO + static_cast<uint32_t>(h2 * 64 + 32), o[1]);
+          tmem_ld_wait();
+          if (h2 == 1) {
+            // O_x is read: the next item's first product may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_O_FREE + x));
+          }
+          if (lane == 0) bulk_wait_group_read<0>();  // the box's previous store has read it
+          __syncwarp();
+          const uint32_t box = obox + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t unit = static_cast<uint32_t>(c * 4 + k);
+              st_shared_v4(box + ((unit ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
+                           pack_bf16x2(__uint_as_float(o[c][8 * k]) * inv, __uint_as_float(o[c][8 * k + 1]) * inv),
+                           pack_bf16x2(__uint_as_float(o[c][8 * k + 2]) * inv, __uint_as_float(o[c][8 * k + 3]) * inv),
+                           pack_bf16x2(__uint_as_float(o[c][8 * k + 4]) * inv, __uint_as_float(o[c][8 * k + 5]) * inv),
+                           pack_bf16x2(__uint_as_float(o[c][8 * k + 6]) * inv, __uint_as_float(o[c][8 * k + 7]) * inv));
+            }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && p0 < a.seq) {
+            tma_store_4d(&tmO, obox, h2 * 64, slot_o, p0, it.sq);
+            bulk_commit_group();
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
+    if (lane == 0) bulk_wait_group<0>();  // every store of this warp has completed
+    __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kAttnTmemCols);
   }
@@ -341,13 +435,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 cudaError_t launch_attention(const CUtensorMap& tm_qkv, const CUtensorMap& tm_o, const AttnArgs& a, int nseq,
                              cudaStream_t st) {
   if (nseq == 0 || a.n_qblk == 0 || a.heads == 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  static int sms = 0;
+  if (sms == 0) {
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    int dev = 0, n = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    configured = true;
+    sms = n;
   }
-  attention_kernel<<<dim3((a.n_qblk + 1) / 2, a.heads, nseq), kAttnThreads, kAttnSmem, st>>>(tm_qkv, tm_o, a);
+  const int n_pairs = (a.n_qblk + 1) / 2;
+  const int64_t units = int64_t((n_pairs + 1) / 2) * a.heads * nseq;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  attention_kernel<<<grid, kAttnThreads, kAttnSmem, st>>>(tm_qkv, tm_o, a, nseq);
   return cudaGetLastError();
 }
 
