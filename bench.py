@@ -181,12 +181,15 @@ def kernel_work(s: synth.MlpShape):
     }
 
 
-def config_json(s: synth.MlpShape, sched: str, n_gpus: int):
-    return {"workload": s.name, "M": s.M, "batch": s.batch, "seq": s.seq, "h": s.h, "ffn": s.F,
-            "act": ACT_NAMES[s.act], "t": s.t, "p": s.p, "q": s.q, "layers": s.layers, "heads": s.heads,
-            "layernorm": s.layernorm, "pass": "fwd+bwd" if s.backward else "fwd", "sched": sched,
-            "seed": 0, "l2": "inputs larger than L2 (129 MB); no flush needed",
-            "parallelism": "replicas" if n_gpus > 1 else "single GPU, t shards emulated in HBM"}
+def config_json(s: synth.MlpShape, sched: str, n_gpus: int, reduce_ctas: int = 0):
+    c = {"workload": s.name, "M": s.M, "batch": s.batch, "seq": s.seq, "h": s.h, "ffn": s.F,
+         "act": ACT_NAMES[s.act], "t": s.t, "p": s.p, "q": s.q, "layers": s.layers, "heads": s.heads,
+         "layernorm": s.layernorm, "pass": "fwd+bwd" if s.backward else "fwd", "sched": sched,
+         "seed": 0, "l2": "inputs larger than L2 (129 MB); no flush needed",
+         "parallelism": "replicas" if n_gpus > 1 else "single GPU, t shards emulated in HBM"}
+    if reduce_ctas:
+        c["reduce_ctas"] = reduce_ctas
+    return c
 
 
 # ------------------------------------------------------------------------------ CPU baseline
@@ -340,7 +343,7 @@ def run_ours(args, rank, world, local_rank):
     gY = dev(inp["gY"]) if s.backward else None
     h = dm.domino_create()
     cfg = dm.make_cfg(s.M, s.h, s.F, s.t, s.p, s.q, s.act, sched=sched, layers=s.layers, ln_eps=1e-5,
-                      heads=s.heads, seq=s.seq if s.attention else 0)
+                      heads=s.heads, seq=s.seq if s.attention else 0, reduce_ctas=args.reduce_ctas)
     Wqkv = dev(inp["Wqkv"]) if s.attention else None
     Wo = dev(inp["Wo"]) if s.attention else None
     if fp8:
@@ -548,7 +551,7 @@ def run_ours(args, rank, world, local_rank):
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
-           "config": config_json(s, args.sched, world),
+           "config": config_json(s, args.sched, world, args.reduce_ctas),
            "pct_of_peak": {"of_sustained": value / world / (peaks["bf16_tflops_sustained"] * peak_scale),
                            "of_burst": value / world / (peaks["bf16_tflops"] * peak_scale),
                            "peaks": peaks["source"] + (" x 2 for e4m3" if fp8 else "")},
@@ -590,7 +593,7 @@ def run_reference(args, rank):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_json(s, args.sched, 1),
+            "config": config_json(s, args.sched, 1, getattr(args, "reduce_ctas", 0)),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": "per step: " + what},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -612,6 +615,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="time replays of one step captured as a CUDA graph")
     ap.add_argument("--fp8", action="store_true", help="E4M3 operands (domino_mlp_fwd_fp8), forward MLP workloads")
+    ap.add_argument("--reduce-ctas", dest="reduce_ctas", type=int, default=0,
+                    help="CTAs per shard-sum launch (cfg.reduce_ctas; 0 = the library default)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

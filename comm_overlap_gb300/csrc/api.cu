@@ -65,6 +65,7 @@ struct Plan {
   int64_t M, h, F, Fi, m, n, a_rows, Ri;
   int t, p, q, act, sched, layers, nslots;
   int heads = 0, seq = 0;  // attention passes
+  int reduce_ctas = 0;     // shard-sum grid cap, 0 = default
   float eps;
   bool gated;
   // workspace offsets
@@ -78,6 +79,7 @@ struct Plan {
 domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   if (!c) return fail(DOMINO_ERR_INVALID_ARG, "cfg is NULL");
   if (c->flags != 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->flags must be 0");
+  if (c->reduce_ctas < 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->reduce_ctas must be >= 0");
   if (c->M < 0 || c->h <= 0 || (pass != DOMINO_PASS_ATTN && c->ffn <= 0) || c->t < 1 || c->p < 1 || c->q < 1)
     return fail(DOMINO_ERR_INVALID_ARG, "need M >= 0, h > 0, ffn > 0, t >= 1, p >= 1, q >= 1");
   if (c->act < DOMINO_ACT_NONE || c->act > DOMINO_ACT_BILINEAR)
@@ -101,8 +103,11 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
     if (c->h / c->heads != 128) return fail(DOMINO_ERR_UNSUPPORTED, "head dimension h / heads must be 128");
     if ((c->M / c->p) % c->seq != 0)
       return fail(DOMINO_ERR_INVALID_ARG, "row chunks must hold whole sequences: M % (p * seq) == 0");
-    if (c->heads > 65535 || (c->M / c->p) / c->seq > 65535)
-      return fail(DOMINO_ERR_UNSUPPORTED, "more heads or sequences per chunk than one launch covers");
+    // work units of one attention launch (pairs of query-block pairs x heads x sequences) must
+    // fit a 32-bit index
+    const int64_t n_qblk = cdiv(c->seq, 128), units = ((n_qblk + 1) / 2 + 1) / 2 * c->heads * ((c->M / c->p) / c->seq);
+    if (units > (int64_t(1) << 31) - 1)
+      return fail(DOMINO_ERR_UNSUPPORTED, "more attention work per row chunk than one launch covers");
   }
   if (c->M > (int64_t(1) << 31) - 1 || c->h > (int64_t(1) << 20) || c->ffn > (int64_t(1) << 24))
     return fail(DOMINO_ERR_UNSUPPORTED, "size beyond the supported range");
@@ -118,6 +123,7 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   Plan& p = *P;
   p.M = c->M; p.h = c->h; p.F = c->ffn; p.Fi = Fi; p.t = c->t; p.p = c->p; p.q = c->q;
   p.act = c->act; p.sched = c->sched; p.layers = c->layers; p.eps = c->ln_eps;
+  p.reduce_ctas = c->reduce_ctas;
   if (attn) {
     p.heads = c->heads;
     p.seq = c->seq;
@@ -350,8 +356,8 @@ domino_status run_fused_reduce(domino_handle H, int kind, int variant, const Pla
 
 domino_status run_shard_sum(domino_handle H, const float* P, int t, int64_t rows, int64_t cols,
                             const uint16_t* res, int64_t ld_res, uint16_t* Y, int64_t ld_y,
-                            cudaStream_t st) {
-  const int cap = H->num_sms * 4;
+                            int reduce_ctas, cudaStream_t st) {
+  const int cap = reduce_ctas > 0 ? reduce_ctas : H->num_sms * 4;
   return launch(H, DOMINO_K_SHARD_SUM, st, "shard-sum launch",
                 [&] { return dm::launch_shard_sum(P, t, rows, cols, res, ld_res, Y, ld_y, cap, st); });
 }
@@ -469,7 +475,7 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
     DM_TRY(run_gemm(H, kind, v_partial, mapH, mapB, a, S.comp, &em));
     DM_TRY(slot_handoff(H, S, slot));
     DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, res_c ? res_c + qc * P.n : nullptr, P.h,
-                         Yc + qc * P.n, P.h, S.red));
+                         Yc + qc * P.n, P.h, P.reduce_ctas, S.red));
     DM_TRY(slot_release(H, S, R, slot));
   }
   return DOMINO_OK;
@@ -663,7 +669,7 @@ domino_status mlp_chunk_bwd(domino_handle H, const Plan& P, const Streams& S, Sl
     DM_TRY(map_f32_out(&em.m[0], part, P.n, P.m, P.t));
     DM_TRY(run_gemm(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_PARTIAL, C.mapDZk, C.mapAmn, a, S.comp, &em));
     DM_TRY(slot_handoff(H, S, slot));
-    DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, nullptr, 0, gX_c + qc * P.n, P.h, S.red));
+    DM_TRY(run_shard_sum(H, part, P.t, P.m, P.n, nullptr, 0, gX_c + qc * P.n, P.h, P.reduce_ctas, S.red));
     DM_TRY(slot_release(H, S, R, slot));
   }
   // gA_i += dZ_i^T . X_c (D = R_i x h, K = tokens), overlapping the gX reduction

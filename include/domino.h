@@ -118,6 +118,9 @@ typedef struct {
   int32_t flags;  /* reserved, must be 0 */
   int32_t heads;  /* attention passes only: attention heads, h / heads == 128, heads % t == 0 */
   int32_t seq;    /* attention passes only: tokens per sequence; M % (p * seq) == 0 */
+  int32_t reduce_ctas; /* CTAs of each shard-sum launch (the AllReduce stand-in), >= 0; 0 = 4 per
+                          SM.  A small budget leaves more of the SMs to the GEMMs it overlaps
+                          (schedules INTRA / INTER); results do not depend on it. */
 } domino_cfg;
 
 typedef struct domino_handle_s* domino_handle;

@@ -118,6 +118,17 @@ def test_schedules_bit_identical(lib):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
+def test_reduction_cta_budget_bit_identical(lib):
+    """cfg.reduce_ctas caps the shard-sum grid (grid-stride loop): any budget gives the same Y."""
+    M, h, Fi, t, act = 512, 256, 128, 4, synth.ACT_SWIGLU
+    X, A, B = real_inputs(M, h, Fi, t, act, seed=8)
+    dX, dA, dB = dev_bf16(X), dev_bf16(A), dev_bf16(B)
+    base = host_bits(lib.fwd(dm.make_cfg(M, h, Fi * t, t, 2, 2, act), dX, dA, dB)[0])
+    for n in (1, 3, 16, 1000):
+        Y = lib.fwd(dm.make_cfg(M, h, Fi * t, t, 2, 2, act, reduce_ctas=n), dX, dA, dB)[0]
+        assert np.array_equal(host_bits(Y), base), n
+
+
 def test_repeat_runs_bit_identical(lib):
     M, h, Fi, t, act = 384, 256, 128, 4, synth.ACT_SWIGLU
     X, A, B = real_inputs(M, h, Fi, t, act, seed=6)
