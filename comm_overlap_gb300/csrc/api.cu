@@ -66,6 +66,7 @@ struct Plan {
   int t, p, q, act, sched, layers, nslots;
   int heads = 0, seq = 0;  // attention passes
   int reduce_ctas = 0;     // shard-sum grid cap, 0 = default
+  int attn_ctas = 0;       // attention grid cap, 0 = one CTA per SM
   float eps;
   bool gated;
   // workspace offsets
@@ -80,6 +81,7 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   if (!c) return fail(DOMINO_ERR_INVALID_ARG, "cfg is NULL");
   if (c->flags != 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->flags must be 0");
   if (c->reduce_ctas < 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->reduce_ctas must be >= 0");
+  if (c->attn_ctas < 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->attn_ctas must be >= 0");
   if (c->M < 0 || c->h <= 0 || (pass != DOMINO_PASS_ATTN && c->ffn <= 0) || c->t < 1 || c->p < 1 || c->q < 1)
     return fail(DOMINO_ERR_INVALID_ARG, "need M >= 0, h > 0, ffn > 0, t >= 1, p >= 1, q >= 1");
   if (c->act < DOMINO_ACT_NONE || c->act > DOMINO_ACT_BILINEAR)
@@ -124,6 +126,7 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   p.M = c->M; p.h = c->h; p.F = c->ffn; p.Fi = Fi; p.t = c->t; p.p = c->p; p.q = c->q;
   p.act = c->act; p.sched = c->sched; p.layers = c->layers; p.eps = c->ln_eps;
   p.reduce_ctas = c->reduce_ctas;
+  p.attn_ctas = c->attn_ctas;
   if (attn) {
     p.heads = c->heads;
     p.seq = c->seq;
@@ -802,7 +805,7 @@ domino_status attn_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, S
     aa.scale_log2 = float(1.4426950408889634 / std::sqrt(128.0));
     aa.err_site = 8 << 4;
     DM_TRY(launch(H, DOMINO_K_ATTN, S.comp, "attention launch",
-                  [&] { return dm::launch_attention(tq, to, aa, int(P.m / P.seq), S.comp); }));
+                  [&] { return dm::launch_attention(tq, to, aa, int(P.m / P.seq), P.attn_ctas, S.comp); }));
   }
   const int64_t Kc = P.h / P.t;
   CUtensorMap mapO;

@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 cudaError_t launch_attention(const CUtensorMap& tm_qkv, const CUtensorMap& tm_o, const AttnArgs& a, int nseq,
-                             cudaStream_t st) {
+                             int max_ctas, cudaStream_t st) {
   if (nseq == 0 || a.n_qblk == 0 || a.heads == 0) return cudaSuccess;
   static int sms = 0;
   if (sms == 0) {
@@ -446,7 +446,8 @@ cudaError_t launch_attention(const CUtensorMap& tm_qkv, const CUtensorMap& tm_o,
   }
   const int n_pairs = (a.n_qblk + 1) / 2;
   const int64_t units = int64_t((n_pairs + 1) / 2) * a.heads * nseq;
-  const int grid = static_cast<int>(units < sms ? units : sms);
+  const int cap = max_ctas > 0 ? max_ctas : sms;
+  const int grid = static_cast<int>(units < cap ? units : cap);
   attention_kernel<<<grid, kAttnThreads, kAttnSmem, st>>>(tm_qkv, tm_o, a, nseq);
   return cudaGetLastError();
 }

@@ -118,8 +118,9 @@ struct AttnArgs {
   float scale_log2;  // log2(e) / sqrt(head dimension)
   int32_t err_site;
 };
+// max_ctas: grid cap of the persistent kernel (0 = one CTA per SM).
 cudaError_t launch_attention(const CUtensorMap& tm_qkv, const CUtensorMap& tm_o, const AttnArgs& a, int nseq,
-                             cudaStream_t st);
+                             int max_ctas, cudaStream_t st);
 cudaError_t take_attn_error(int* code);
 
 // Shard-sum (AllReduce stand-in) and LayerNorm.

@@ -36,12 +36,13 @@ class domino_cfg(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("h", ctypes.c_int64), ("ffn", ctypes.c_int64), ("t", ctypes.c_int32),
                 ("p", ctypes.c_int32), ("q", ctypes.c_int32), ("act", ctypes.c_int32), ("sched", ctypes.c_int32),
                 ("layers", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("flags", ctypes.c_int32),
-                ("heads", ctypes.c_int32), ("seq", ctypes.c_int32), ("reduce_ctas", ctypes.c_int32)]
+                ("heads", ctypes.c_int32), ("seq", ctypes.c_int32), ("reduce_ctas", ctypes.c_int32),
+                ("attn_ctas", ctypes.c_int32)]
 
 
 def make_cfg(M, h, ffn, t, p=1, q=1, act=ACT_GELU, sched=SCHED_INTRA, layers=1, ln_eps=1e-5, flags=0, heads=0,
-             seq=0, reduce_ctas=0) -> domino_cfg:
-    return domino_cfg(M, h, ffn, t, p, q, act, sched, layers, ln_eps, flags, heads, seq, reduce_ctas)
+             seq=0, reduce_ctas=0, attn_ctas=0) -> domino_cfg:
+    return domino_cfg(M, h, ffn, t, p, q, act, sched, layers, ln_eps, flags, heads, seq, reduce_ctas, attn_ctas)
 
 
 _lib = None

@@ -121,6 +121,9 @@ typedef struct {
   int32_t reduce_ctas; /* CTAs of each shard-sum launch (the AllReduce stand-in), >= 0; 0 = 4 per
                           SM.  A small budget leaves more of the SMs to the GEMMs it overlaps
                           (schedules INTRA / INTER); results do not depend on it. */
+  int32_t attn_ctas;   /* attention passes only: CTAs of each attention launch, >= 0; 0 = one per
+                          SM (the kernel is persistent over its work units); results do not
+                          depend on it. */
 } domino_cfg;
 
 typedef struct domino_handle_s* domino_handle;

@@ -90,6 +90,7 @@ def test_workspace_size_formula(dlib):
     (dict(M=96, h=64, ffn=64, t=2, sched=7), 1),
     (dict(M=96, h=64, ffn=64, t=2, flags=1), 1),
     (dict(M=96, h=64, ffn=64, t=2, reduce_ctas=-1), 1),
+    (dict(M=96, h=64, ffn=64, t=2, attn_ctas=-1), 1),
 ])
 def test_validation_errors(dlib, kw, status):
     if kw.get("h") == 48:

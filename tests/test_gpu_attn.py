@@ -39,10 +39,10 @@ def attn_inputs(nseq, seq, h, t, seed):
     return X, Wqkv, Wo
 
 
-def run_attn(handle, X, Wqkv, Wo, h, heads, seq, t, p=1, q=1, sched=dm.SCHED_INTRA):
+def run_attn(handle, X, Wqkv, Wo, h, heads, seq, t, p=1, q=1, sched=dm.SCHED_INTRA, attn_ctas=0):
     import torch
     M = X.shape[0]
-    cfg = dm.make_cfg(M, h, 0, t, p, q, sched=sched, heads=heads, seq=seq)
+    cfg = dm.make_cfg(M, h, 0, t, p, q, sched=sched, heads=heads, seq=seq, attn_ctas=attn_ctas)
     Y = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
     n = dm.domino_workspace_size(cfg, dm.PASS_ATTN)
     ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
@@ -78,6 +78,22 @@ def test_attention_splits_and_schedules_bit_identical(handle):
         for p, q in ((2, 1), (4, 2), (1, 4)):
             got = host_bits(run_attn(handle, X, Wqkv, Wo, h, heads, seq, t, p, q, sched))
             assert np.array_equal(got, base), (sched, p, q)
+
+
+@pytest.mark.parametrize("nseq,seq", [(3, 1000), (2, 640), (4, 100)])
+def test_attention_grid_budget_bit_identical(handle, nseq, seq):
+    """The persistent kernel on a capped grid: a few CTAs walk all work units in turn (Q reloads,
+    K/V rings and O hand-backs carried across items and units), bit-identical to one unit per CTA;
+    the one-CTA run is also held to the oracle.  Units: pairs of query-block pairs (odd pair counts
+    leave a one-item unit; a single block leaves one-tile items)."""
+    h, heads, t = 512, 4, 2
+    X, Wqkv, Wo = attn_inputs(nseq, seq, h, t, 64)
+    base = host_bits(run_attn(handle, X, Wqkv, Wo, h, heads, seq, t))
+    for ctas in (1, 2, 5, 23):
+        Y = run_attn(handle, X, Wqkv, Wo, h, heads, seq, t, attn_ctas=ctas)
+        assert np.array_equal(host_bits(Y), base), ctas
+        if ctas == 1:
+            assert_tol(host_f64(Y), oracle.attn_fwd(X, Wqkv, Wo, t, heads, seq), "attention on one CTA")
 
 
 def test_attention_validation(handle):
