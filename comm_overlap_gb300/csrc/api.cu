@@ -113,6 +113,10 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   }
   if (c->M > (int64_t(1) << 31) - 1 || c->h > (int64_t(1) << 20) || c->ffn > (int64_t(1) << 24))
     return fail(DOMINO_ERR_UNSUPPORTED, "size beyond the supported range");
+  // one shard-sum launch covers m x n outputs as 16-byte vectors counted in 32 bits (see
+  // domino_shard_sum)
+  if ((c->M / c->p) * ((c->h / c->q) / 8) >= (int64_t(1) << 31))
+    return fail(DOMINO_ERR_UNSUPPORTED, "row chunk x column chunk too large for one reduction launch");
   if (pass == DOMINO_PASS_STACK || pass == DOMINO_PASS_STACK_BWD) {
     if (c->layers < 1) return fail(DOMINO_ERR_INVALID_ARG, "layers must be >= 1");
     if (!(c->ln_eps > 0.0f)) return fail(DOMINO_ERR_INVALID_ARG, "ln_eps must be > 0");
@@ -1200,7 +1204,8 @@ domino_status domino_shard_sum(const float* Pp, int32_t t, int64_t rows, int64_t
                                void* stream) {
   if (t < 1 || rows < 0 || cols < 0) return fail(DOMINO_ERR_INVALID_ARG, "need t >= 1, rows, cols >= 0");
   if (cols % 8 != 0) return fail(DOMINO_ERR_ALIGNMENT, "cols must be a multiple of 8");
-  if (rows * (cols / 8) >= (int64_t(1) << 32)) return fail(DOMINO_ERR_UNSUPPORTED, "too many elements");
+  // the kernel's grid-stride loop counts 16-byte vectors in 32 bits: below 2^31 it cannot wrap
+  if (rows * (cols / 8) >= (int64_t(1) << 31)) return fail(DOMINO_ERR_UNSUPPORTED, "too many elements");
   if (ld_y < cols || (ld_y % 8) != 0) return fail(DOMINO_ERR_ALIGNMENT, "ld_y must be >= cols and a multiple of 8");
   if (residual && (ld_res < cols || (ld_res % 8) != 0))
     return fail(DOMINO_ERR_ALIGNMENT, "ld_res must be >= cols and a multiple of 8");

@@ -91,6 +91,7 @@ def test_workspace_size_formula(dlib):
     (dict(M=96, h=64, ffn=64, t=2, flags=1), 1),
     (dict(M=96, h=64, ffn=64, t=2, reduce_ctas=-1), 1),
     (dict(M=96, h=64, ffn=64, t=2, attn_ctas=-1), 1),
+    (dict(M=1 << 26, h=1 << 15, ffn=64, t=2), 2),  # m x n / 8 = 2^38 vectors in one reduction
 ])
 def test_validation_errors(dlib, kw, status):
     if kw.get("h") == 48:
@@ -118,6 +119,9 @@ def test_shard_sum_host_validation(dlib):
     with pytest.raises(dlib.DominoError) as e:
         dlib.domino_shard_sum(0x1000, 0, 4, 16, None, 0, 0x2000, 16, stream=0)
     assert e.value.status == 1
+    with pytest.raises(dlib.DominoError) as e:  # 2^31 16-byte vectors: beyond a 32-bit loop count
+        dlib.domino_shard_sum(0x1000, 2, 1 << 20, 1 << 14, None, 0, 0x2000, 1 << 14, stream=0)
+    assert e.value.status == 2
 
 
 def test_create_without_gpu_fails_cleanly(dlib):
