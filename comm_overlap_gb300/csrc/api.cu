@@ -6,9 +6,12 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/domino.h"
 #include "kernels.h"
@@ -57,6 +60,33 @@ domino_status cuda_fail(cudaError_t e, const char* what) {
 
 constexpr size_t kAlign = 1024;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+// NVTX ranges (header-only NVTX v3: no cost unless a profiler is attached) around every entry
+// point, row chunk and kernel enqueue, so a timeline shows the schedule.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+struct NvtxChunk {
+  explicit NvtxChunk(int pc) {
+    char b[32];
+    std::snprintf(b, sizeof b, "row chunk %d", pc);
+    nvtxRangePushA(b);
+  }
+  ~NvtxChunk() { nvtxRangePop(); }
+  NvtxChunk(const NvtxChunk&) = delete;
+  NvtxChunk& operator=(const NvtxChunk&) = delete;
+};
+
+const char* kernel_kind_name(int kind) {
+  static const char* const names[DOMINO_K_COUNT] = {"gemm_fwd1", "gemm_fwd2", "shard_sum", "layernorm",
+                                                     "gemm_dgrad_h", "gemm_wgrad_b", "gemm_dgrad_x", "gemm_wgrad_a",
+                                                     "layernorm_bwd", "gemm_qkv", "attention", "gemm_oproj"};
+  return (kind >= 0 && kind < DOMINO_K_COUNT) ? names[kind] : "kernel";
+}
+
 bool gated(int act) { return act == DOMINO_ACT_SWIGLU || act == DOMINO_ACT_BILINEAR; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -77,7 +107,7 @@ struct Plan {
   size_t save_n = 0, save_act = 0, save_rstd = 0, save_layer = 0;
 };
 
-domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
+domino_status make_plan_impl(const domino_cfg* c, int pass, Plan* P) {
   if (!c) return fail(DOMINO_ERR_INVALID_ARG, "cfg is NULL");
   if (c->flags != 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->flags must be 0");
   if (c->reduce_ctas < 0) return fail(DOMINO_ERR_INVALID_ARG, "cfg->reduce_ctas must be >= 0");
@@ -194,6 +224,29 @@ domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
   return DOMINO_OK;
 }
 
+// With DOMINO_LOG=1 in the environment every validated plan is printed to stderr: the pass, the
+// problem and chunk sizes, the schedule and the workspace layout.
+void log_plan(const Plan& P, int pass) {
+  const char* v = std::getenv("DOMINO_LOG");
+  if (!v || std::strcmp(v, "1") != 0) return;
+  static const char* const passes[] = {"fwd", "bwd", "stack", "stack_bwd", "attn", "block", "fwd_fp8"};
+  static const char* const scheds[] = {"serial", "intra", "inter", "fused"};
+  std::fprintf(stderr,
+               "domino plan: pass=%s M=%lld h=%lld ffn=%lld t=%d p=%d q=%d (chunk %lld x %lld) act=%d sched=%s "
+               "layers=%d heads=%d seq=%d partial slots=%d x %zu B workspace=%zu B [h@%zu ln@%zu dz@%zu hb@%zu "
+               "gn@%zu qkv@%zu o@%zu partials@%zu]\n",
+               passes[pass], static_cast<long long>(P.M), static_cast<long long>(P.h), static_cast<long long>(P.F),
+               P.t, P.p, P.q, static_cast<long long>(P.m), static_cast<long long>(P.n), P.act, scheds[P.sched],
+               P.layers, P.heads, P.seq, P.nslots, P.part_slot, P.total, P.off_h, P.off_ln, P.off_dz, P.off_hb,
+               P.off_gn, P.off_qkv, P.off_o, P.off_part);
+}
+
+domino_status make_plan(const domino_cfg* c, int pass, Plan* P) {
+  const domino_status st = make_plan_impl(c, pass, P);
+  if (st == DOMINO_OK) log_plan(*P, pass);
+  return st;
+}
+
 domino_status check_ws(const Plan& P, void* ws, size_t bytes) {
   if (P.total == 0) return DOMINO_OK;
   if (!ws) return fail(DOMINO_ERR_WORKSPACE, "workspace is NULL");
@@ -299,7 +352,11 @@ domino_status launch(domino_handle H, int kind, cudaStream_t st, const char* wha
     b = timing_event(H);
     DM_CUDA(cudaEventRecord(a, st), "cudaEventRecord");
   }
-  const cudaError_t e = fn();
+  cudaError_t e;
+  {
+    NvtxRange r(kernel_kind_name(kind));
+    e = fn();
+  }
   if (e != cudaSuccess) return cuda_fail(e, what);
   H->launches++;
   if (H->timing) {
@@ -732,6 +789,7 @@ domino_status stack_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_i
       const uint16_t* src = (l == 0) ? Z_in : Z_out;
       uint8_t* sl = save ? save + l * P.save_layer : nullptr;
       for (int pc = 0; pc < P.p; ++pc) {
+        NvtxChunk chunk_range_(pc);
         const int64_t r0 = pc * P.m;
         if (l > 0) DM_TRY(wait_previous_layer(H, P, S, pc, pc == 0));
         uint16_t* n_c = sl ? reinterpret_cast<uint16_t*>(sl + P.save_n) + r0 * P.h : lnbuf;
@@ -843,6 +901,7 @@ domino_status block_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_i
       for (int sub = 0; sub < 2; ++sub) {
         const uint16_t* src = (l == 0 && sub == 0) ? Z_in : Z_out;
         for (int pc = 0; pc < P.p; ++pc) {
+          NvtxChunk chunk_range_(pc);
           const int64_t r0 = pc * P.m;
           if (l > 0 || sub > 0) DM_TRY(wait_previous_layer(H, P, S, pc, pc == 0));
           DM_TRY(launch(H, DOMINO_K_LAYERNORM, S.comp, "LayerNorm launch", [&] {
@@ -951,6 +1010,7 @@ domino_status domino_mlp_fwd(domino_handle H, const domino_cfg* cfg, const uint1
                              const uint16_t* A, const uint16_t* B, uint16_t* Y, uint16_t* act_save,
                              void* ws, size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_mlp_fwd");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_FWD, &P));
   DM_TRY(check_ptr(X, "X"));
@@ -971,6 +1031,7 @@ domino_status domino_mlp_fwd(domino_handle H, const domino_cfg* cfg, const uint1
   const domino_status st = [&]() -> domino_status {
     SlotRing R;
     for (int pc = 0; pc < P.p; ++pc) {
+      NvtxChunk chunk_range_(pc);
       const int64_t r0 = pc * P.m;
       DM_TRY(mlp_chunk_fwd(H, P, S, R, X + r0 * P.h, mapA, mapB, Hbuf, parts,
                            act_save ? act_save + r0 * P.a_rows : nullptr, nullptr, Y + r0 * P.h, 1));
@@ -984,6 +1045,7 @@ domino_status domino_stack_fwd(domino_handle H, const domino_cfg* cfg, const uin
                                const uint16_t* A, const uint16_t* B, uint16_t* Z_out, void* ws,
                                size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_stack_fwd");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_STACK, &P));
   DM_TRY(check_ptr(Z_in, "Z_in"));
@@ -1007,6 +1069,7 @@ domino_status domino_stack_fwd_train(domino_handle H, const domino_cfg* cfg, con
                                      const uint16_t* A, const uint16_t* B, uint16_t* Z_out, void* save,
                                      size_t save_bytes, void* ws, size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_stack_fwd_train");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_STACK, &P));
   DM_TRY(check_ptr(Z_in, "Z_in"));
@@ -1027,6 +1090,7 @@ domino_status domino_stack_bwd(domino_handle H, const domino_cfg* cfg, const uin
                                const void* save, size_t save_bytes, const uint16_t* gZ_out, uint16_t* gZ_in,
                                float* gA, float* gB, void* ws, size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_stack_bwd");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_STACK_BWD, &P));
   DM_TRY(check_ptr(A, "A"));
@@ -1062,6 +1126,7 @@ domino_status domino_stack_bwd(domino_handle H, const domino_cfg* cfg, const uin
       // running gradient kept in gZ_in
       const uint16_t* g = (l == P.layers - 1) ? gZ_out : gZ_in;
       for (int pc = P.p - 1; pc >= 0; --pc) {
+        NvtxChunk chunk_range_(pc);
         const int64_t r0 = pc * P.m;
         if (l < P.layers - 1) DM_TRY(wait_previous_layer(H, P, S, pc, pc == P.p - 1));
         DM_TRY(mlp_chunk_bwd(H, P, S, R, C, n_l + r0 * P.h, act_l + r0 * P.a_rows, g + r0 * P.h, gn + r0 * P.h,
@@ -1084,6 +1149,7 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
                              const uint16_t* gY, uint16_t* gX, float* gA, float* gB, void* ws,
                              size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_mlp_bwd");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_BWD, &P));
   DM_TRY(check_ptr(X, "X"));
@@ -1105,6 +1171,7 @@ domino_status domino_mlp_bwd(domino_handle H, const domino_cfg* cfg, const uint1
     SlotRing R;
     // row chunks in reverse order, as the backward pass runs the forward schedule backwards
     for (int pc = P.p - 1; pc >= 0; --pc) {
+      NvtxChunk chunk_range_(pc);
       const int64_t r0 = pc * P.m;
       DM_TRY(mlp_chunk_bwd(H, P, S, R, C, X + r0 * P.h, act_save + r0 * P.a_rows, gY + r0 * P.h, gX + r0 * P.h,
                            gA, gB));
@@ -1118,6 +1185,7 @@ domino_status domino_mlp_fwd_fp8(domino_handle H, const domino_cfg* cfg, const u
                                  const uint8_t* B8, const float* scales, uint16_t* Y, void* ws, size_t ws_bytes,
                                  void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_mlp_fwd_fp8");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_FWD_FP8, &P));
   DM_TRY(check_ptr(X8, "X8"));
@@ -1142,6 +1210,7 @@ domino_status domino_mlp_fwd_fp8(domino_handle H, const domino_cfg* cfg, const u
   const domino_status st = [&]() -> domino_status {
     SlotRing R;
     for (int pc = 0; pc < P.p; ++pc) {
+      NvtxChunk chunk_range_(pc);
       const int64_t r0 = pc * P.m;
       DM_TRY(mlp_chunk_fwd_fp8(H, P, S, R, X8 + r0 * P.h, mapA, mapB, H8, parts, Y + r0 * P.h, sc));
     }
@@ -1153,6 +1222,7 @@ domino_status domino_mlp_fwd_fp8(domino_handle H, const domino_cfg* cfg, const u
 domino_status domino_attn_fwd(domino_handle H, const domino_cfg* cfg, const uint16_t* X, const uint16_t* Wqkv,
                               const uint16_t* Wo, uint16_t* Y, void* ws, size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_attn_fwd");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_ATTN, &P));
   DM_TRY(check_ptr(X, "X"));
@@ -1173,6 +1243,7 @@ domino_status domino_attn_fwd(domino_handle H, const domino_cfg* cfg, const uint
   const domino_status st = [&]() -> domino_status {
     SlotRing R;
     for (int pc = 0; pc < P.p; ++pc) {
+      NvtxChunk chunk_range_(pc);
       const int64_t r0 = pc * P.m;
       DM_TRY(attn_chunk_fwd(H, P, S, R, X + r0 * P.h, mapW, mapWo, QKV, O, parts, nullptr, Y + r0 * P.h));
     }
@@ -1185,6 +1256,7 @@ domino_status domino_block_fwd(domino_handle H, const domino_cfg* cfg, const uin
                                const uint16_t* Wo, const uint16_t* A, const uint16_t* B, uint16_t* Z_out, void* ws,
                                size_t ws_bytes, void* stream) {
   DM_TRY(ready(H));
+  NvtxRange range_("domino_block_fwd");
   Plan P;
   DM_TRY(make_plan(cfg, DOMINO_PASS_BLOCK, &P));
   DM_TRY(check_ptr(Z_in, "Z_in"));

@@ -139,3 +139,17 @@ def test_binding_refuses_missing_library(tmp_path, monkeypatch):
     monkeypatch.setattr(domino, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(domino.DominoError):
         domino.lib()
+
+
+def test_plan_log(dlib, capfd, monkeypatch):
+    """DOMINO_LOG=1 prints each validated plan (pass, sizes, schedule, workspace layout) to stderr;
+    unset, nothing is printed."""
+    cfg = dlib.make_cfg(M=512, h=256, ffn=512, t=2, p=2, q=1, sched=dlib.SCHED_INTRA)
+    monkeypatch.delenv("DOMINO_LOG", raising=False)
+    n = dlib.domino_workspace_size(cfg, dlib.PASS_FWD)
+    assert "domino plan" not in capfd.readouterr().err
+    monkeypatch.setenv("DOMINO_LOG", "1")
+    assert dlib.domino_workspace_size(cfg, dlib.PASS_FWD) == n
+    err = capfd.readouterr().err
+    assert "domino plan: pass=fwd M=512 h=256 ffn=512 t=2 p=2 q=1 (chunk 256 x 256)" in err
+    assert f"workspace={n} B" in err and "sched=intra" in err
