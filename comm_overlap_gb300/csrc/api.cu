@@ -499,6 +499,9 @@ domino_status ready(domino_handle H) {
   int dev = -1;
   DM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   if (dev != H->device) return fail(DOMINO_ERR_INVALID_ARG, "handle belongs to another device");
+  // Bind the device's primary context to the calling thread: a thread that has not used CUDA yet
+  // (e.g. an autograd worker) has none current, and the tensor-map encoder is a driver-API call.
+  DM_CUDA(cudaSetDevice(dev), "cudaSetDevice");
   return DOMINO_OK;
 }
 

@@ -1,0 +1,118 @@
+"""The PyTorch module around the library (comm_overlap_gb300.torch_mlp.DominoMLP) against the CPU
+oracle: forward output, input gradient through autograd, weight gradients accumulated into fp32
+main_grad (twice: accumulation) or returned as bf16 .grad."""
+import numpy as np
+import pytest
+
+import oracle
+from comm_overlap_gb300 import domino as dm
+from comm_overlap_gb300 import synth
+from gpu_helpers import assert_tol, dev_bf16, host_f64
+from test_gpu_bwd import shard_major_dA, shard_major_dB
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from comm_overlap_gb300 import build
+    build.build()
+
+
+def make(act, fuse, sched=dm.SCHED_INTRA):
+    import torch
+    from comm_overlap_gb300.torch_mlp import DominoMLP
+    M, h, Fi, t, p, q = 384, 256, 136, 2, 2, 2
+    s = synth.MlpShape("tm", M, h, Fi * t, act, t, p, q, backward=True)
+    d = synth.make_inputs(s, seed=51)
+    mod = DominoMLP(h, Fi * t, t, p, q, act, sched=sched, fuse_wgrad=fuse)
+    with torch.no_grad():
+        mod.A.copy_(dev_bf16(d["A"][0]))
+        mod.B.copy_(dev_bf16(d["B"][0]))
+    return mod, d, s
+
+
+@pytest.mark.parametrize("act", [synth.ACT_GELU, synth.ACT_SWIGLU])
+def test_module_fused_main_grad(built, act):
+    import torch
+    mod, d, s = make(act, True)
+    X = dev_bf16(d["X"]).requires_grad_(True)
+    gY = dev_bf16(d["gY"])
+    Y = mod(X)
+    ref_y = oracle.mlp_fwd(d["X"], d["A"][0], d["B"][0], s.t, act)
+    assert_tol(host_f64(Y), ref_y, "module forward")
+    Y.backward(gY)
+    dX, dA, dB = oracle.mlp_bwd(d["X"], d["A"][0], d["B"][0], d["gY"], s.t, act)
+    gated = act in synth.GATED
+    assert_tol(host_f64(X.grad), dX, "module input gradient")
+    assert mod.A.grad is None and mod.B.grad is None
+    gA1 = mod.A.main_grad.cpu().numpy().astype(np.float64)
+    gB1 = mod.B.main_grad.cpu().numpy().astype(np.float64)
+    assert_tol(gA1, shard_major_dA(dA, s.t, s.Fi, gated), "main_grad of A")
+    assert_tol(gB1, shard_major_dB(dB, s.t, s.Fi), "main_grad of B")
+    # a second micro-batch accumulates into the same fp32 buffers
+    X.grad = None
+    mod(X).backward(gY)
+    torch.cuda.synchronize()
+    assert_tol(mod.A.main_grad.cpu().numpy().astype(np.float64), 2 * gA1, "accumulated main_grad of A",
+               rel=1e-5, abs_=1e-6)
+    assert_tol(mod.B.main_grad.cpu().numpy().astype(np.float64), 2 * gB1, "accumulated main_grad of B",
+               rel=1e-5, abs_=1e-6)
+    mod.close()
+
+
+def test_module_plain_grad_and_schedules(built):
+    import torch
+    act = synth.ACT_SWIGLU
+    outs = []
+    for sched in (dm.SCHED_INTRA, dm.SCHED_FUSED, dm.SCHED_SERIAL):
+        mod, d, s = make(act, False, sched)
+        X = dev_bf16(d["X"]).requires_grad_(True)
+        Y = mod(X)
+        Y.backward(dev_bf16(d["gY"]))
+        torch.cuda.synchronize()
+        outs.append((Y.detach().clone(), X.grad.clone(), mod.A.grad.clone(), mod.B.grad.clone()))
+        if sched == dm.SCHED_INTRA:
+            _, dA, dB = oracle.mlp_bwd(d["X"], d["A"][0], d["B"][0], d["gY"], s.t, act, want_dx=False)
+            assert mod.A.grad.dtype == torch.bfloat16
+            assert_tol(host_f64(mod.A.grad), shard_major_dA(dA, s.t, s.Fi, True), ".grad of A")
+            assert_tol(host_f64(mod.B.grad), shard_major_dB(dB, s.t, s.Fi), ".grad of B")
+        mod.close()
+    for o in outs[1:]:  # every schedule gives the same bits
+        for a, b in zip(o, outs[0]):
+            assert torch.equal(a, b)
+
+
+def test_library_call_from_a_fresh_thread(built):
+    """A thread that has not used CUDA yet (no current context, like PyTorch's autograd workers)
+    can call the library: the entry points bind the device's context before encoding tensor maps."""
+    import threading
+    import torch
+    M, h, Fi, t = 256, 256, 128, 2
+    s = synth.MlpShape("th", M, h, Fi * t, synth.ACT_GELU, t, 2, 1)
+    d = synth.make_inputs(s, seed=52)
+    X, A, B = dev_bf16(d["X"]), dev_bf16(d["A"][0]), dev_bf16(d["B"][0])
+    cfg = dm.make_cfg(M, h, Fi * t, t, 2, 1, synth.ACT_GELU)
+    n = dm.domino_workspace_size(cfg, dm.PASS_FWD)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    Y = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+    h_ = dm.domino_create()
+    stream = torch.cuda.current_stream().cuda_stream
+    errors = []
+
+    def run():
+        try:
+            dm.domino_mlp_fwd(h_, cfg, X, A, B, Y, None, ws, n, stream)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    th = threading.Thread(target=run)
+    th.start()
+    th.join()
+    torch.cuda.synchronize()
+    dm.domino_destroy(h_)
+    assert not errors, errors
+    assert_tol(host_f64(Y), oracle.mlp_fwd(d["X"], d["A"][0], d["B"][0], t, synth.ACT_GELU), "forward from a thread")
