@@ -29,6 +29,8 @@
 // flight drain, frees TMEM and returns, leaving a code in this translation unit's error word.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "actfn.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -435,14 +437,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 cudaError_t launch_attention(const CUtensorMap& tm_qkv, const CUtensorMap& tm_o, const AttnArgs& a, int nseq,
                              int max_ctas, cudaStream_t st) {
   if (nseq == 0 || a.n_qblk == 0 || a.heads == 0) return cudaSuccess;
-  static int sms = 0;
+  // per device: the shared-memory opt-in is an attribute of the kernel on one device (0 = not set up)
+  static std::atomic<int> sms_of[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int sms = sms_of[dev].load(std::memory_order_acquire);
   if (sms == 0) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-    int dev = 0, n = 0;
-    if (e == cudaSuccess) e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    sms = n;
+    sms_of[dev].store(sms, std::memory_order_release);
   }
   const int n_pairs = (a.n_qblk + 1) / 2;
   const int64_t units = int64_t((n_pairs + 1) / 2) * a.heads * nseq;

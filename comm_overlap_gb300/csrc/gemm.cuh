@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "actfn.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -953,9 +955,16 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ep
   auto fn = gemm_kernel<EPI, A_MN, B_MN, P, F8>;
   constexpr int smem = smem_bytes<P, EPI>();
   static_assert(smem <= 232448, "shared memory beyond the per-CTA limit");
-  static int max_units = 0;  // co-resident CTAs (single) or clusters (pair)
+  // Co-resident CTAs (single) or clusters (pair), per device: the shared-memory opt-in is an
+  // attribute of the function on one device and the occupancy is queried there.  0 = not set up.
+  static std::atomic<int> max_units_of[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int max_units = max_units_of[dev].load(std::memory_order_acquire);
   if (max_units == 0) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if constexpr (P) {
       cudaLaunchConfig_t cfg = {};
@@ -975,12 +984,12 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ep
       if (n < 1) return cudaErrorInvalidConfiguration;
       max_units = n;
     } else {
-      int dev = 0, sms = 0;
-      e = cudaGetDevice(&dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      int sms = 0;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
       max_units = sms;
     }
+    max_units_of[dev].store(max_units, std::memory_order_release);
   }
   // units own whole output tiles (with all their shards) in the fused shard-sum
   const int64_t tiles = int64_t(EPI == EPI_F32_REDUCE ? 1 : args.batches) * args.m_tiles * args.n_tiles;

@@ -8,6 +8,10 @@
 
 namespace dm {
 
+// Devices a process may drive; launch facts (shared-memory opt-in, co-resident grid) are cached
+// per device ordinal below this bound.
+constexpr int kMaxDevices = 64;
+
 // Activation codes (same values as domino_act).
 enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2, ACT_SWIGLU = 3, ACT_BILINEAR = 4 };
 
