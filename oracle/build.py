@@ -21,14 +21,20 @@ def needs_build() -> bool:
     return any(os.path.getmtime(os.path.join(HERE, s)) > t for s in SOURCES)
 
 
+def compile_library(src_dir: str, out: str) -> str:
+    """Compiles the oracle sources found in `src_dir` into the shared library `out`."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=gnu11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+           "-Wall", "-o", tmp, os.path.join(src_dir, "oracle.c"), os.path.join(src_dir, "oracle_attn.c"),
+           os.path.join(src_dir, "oracle_fp8.c"), "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     if force or needs_build():
-        tmp = LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=gnu11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-               "-Wall", "-o", tmp, os.path.join(HERE, "oracle.c"), os.path.join(HERE, "oracle_attn.c"),
-               os.path.join(HERE, "oracle_fp8.c"), "-lm"]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
+        compile_library(HERE, LIB)
     return LIB
 
 
