@@ -39,17 +39,17 @@ ACT_NAMES = {0: "none", 1: "relu", 2: "gelu", 3: "swiglu", 4: "bilinear"}
 # DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by workload and
 # kernel, with the SHA-256 of the GEMM kernel source at capture time; reported only while the
 # source is unchanged.  See profiles/ for the capture commands and summaries.
-_SHA_CUR = "a733c27772151f80"
+_SHA_CUR = "6a3ed4a161879960"
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum (1 pass) on
     # the full-size forward+backward workload; bytes per launch, mean of the captured launches
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.304e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.834e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2.261e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 4.631e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 3.333e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.816e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 8.093e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.607e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.856e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2.260e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 4.690e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 3.808e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.770e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 8.321e9, "src_sha": _SHA_CUR},
 }
 
 

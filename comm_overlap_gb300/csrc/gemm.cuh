@@ -219,6 +219,38 @@ __device__ __forceinline__ void epilogue_cols(const GemmArgs& a, uint32_t tacc, 
   }
 }
 
+// Arithmetic of one 32-column chunk of the activation-backward epilogue for the calling thread's row,
+// with the activation fixed at compile time: from the accumulator dH (r, fp32) and the saved
+// pre-activation (zi: Z or G, ui: U, bf16 pairs), dZ = dH act'(Z) (gated: dG, dU) and the
+// recomputed H = act(Z), as bf16 pairs.  The caller picks the activation once per chunk, so the
+// 32 independent evaluations form one branch-free block whose latency chains overlap.
+template <bool kGlu, int ACT>
+__device__ __forceinline__ void bwd_act_chunk(const uint32_t (&zi)[16], const uint32_t (&ui)[16],
+                                              const uint32_t (&r)[32], uint32_t (&o1)[16], uint32_t (&o2)[16],
+                                              uint32_t (&oh)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const uint32_t zw = zi[e >> 1];
+    float d1a, d1b, d2a = 0.f, d2b = 0.f, ha, hb;
+    const float z0 = bf16lo(zw), z1 = bf16hi(zw);
+    const float g0 = __uint_as_float(r[e]), g1 = __uint_as_float(r[e + 1]);
+    if constexpr (kGlu) {
+      const uint32_t uw = ui[e >> 1];
+      glu_bwd(ACT, z0, bf16lo(uw), g0, d1a, d2a, ha);
+      glu_bwd(ACT, z1, bf16hi(uw), g1, d1b, d2b, hb);
+    } else {
+      float da, db;
+      act_fwd_grad(ACT, z0, ha, da);
+      act_fwd_grad(ACT, z1, hb, db);
+      d1a = g0 * da;
+      d1b = g1 * db;
+    }
+    o1[e >> 1] = pack_bf16x2(d1a, d1b);
+    o2[e >> 1] = pack_bf16x2(d2a, d2b);
+    oh[e >> 1] = pack_bf16x2(ha, hb);
+  }
+}
+
 // Activation-backward epilogue (EPI_ACT_BWD / EPI_GLU_BWD) for all tiles of one warp (32 rows x 256
 // columns of each tile, in 32-column chunks), with every global access a TMA box:
 //  * the saved first-linear output of the chunk (Z, or G and U) is loaded into the warp's input
@@ -317,26 +349,17 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
       tmem_ld_wait();
       if (!valid) continue;
       uint32_t o1[16], o2[16], oh[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const uint32_t zw = zi[e >> 1];
-        float d1a, d1b, d2a = 0.f, d2b = 0.f, ha, hb;
-        const float z0 = bf16lo(zw), z1 = bf16hi(zw);
-        const float g0 = __uint_as_float(r[e]), g1 = __uint_as_float(r[e + 1]);
-        if constexpr (kGlu) {
-          const uint32_t uw = ui[e >> 1];
-          glu_bwd(a.act, z0, bf16lo(uw), g0, d1a, d2a, ha);
-          glu_bwd(a.act, z1, bf16hi(uw), g1, d1b, d2b, hb);
-        } else {
-          float da, db;
-          act_fwd_grad(a.act, z0, ha, da);
-          act_fwd_grad(a.act, z1, hb, db);
-          d1a = g0 * da;
-          d1b = g1 * db;
-        }
-        o1[e >> 1] = pack_bf16x2(d1a, d1b);
-        o2[e >> 1] = pack_bf16x2(d2a, d2b);
-        oh[e >> 1] = pack_bf16x2(ha, hb);
+      if constexpr (kGlu) {
+        if (a.act == ACT_SWIGLU)
+          bwd_act_chunk<true, ACT_SWIGLU>(zi, ui, r, o1, o2, oh);
+        else
+          bwd_act_chunk<true, ACT_BILINEAR>(zi, ui, r, o1, o2, oh);
+      } else if (a.act == ACT_GELU) {
+        bwd_act_chunk<false, ACT_GELU>(zi, ui, r, o1, o2, oh);
+      } else if (a.act == ACT_RELU) {
+        bwd_act_chunk<false, ACT_RELU>(zi, ui, r, o1, o2, oh);
+      } else {
+        bwd_act_chunk<false, ACT_NONE>(zi, ui, r, o1, o2, oh);
       }
       if (lane == 0 && n_stored > 0) bulk_wait_group_read<0>();  // previous stores done reading
       __syncwarp();
