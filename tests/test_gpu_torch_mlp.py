@@ -116,3 +116,59 @@ def test_library_call_from_a_fresh_thread(built):
     dm.domino_destroy(h_)
     assert not errors, errors
     assert_tol(host_f64(Y), oracle.mlp_fwd(d["X"], d["A"][0], d["B"][0], t, synth.ACT_GELU), "forward from a thread")
+
+
+def make_stack(act, fuse, L=2, M=256, h=128, F=256, t=2, p=2, q=2, seed=53):
+    import torch
+    from comm_overlap_gb300.torch_mlp import DominoStack
+    s = synth.MlpShape("ts", M, h, F, act, t, p, q, layers=L, layernorm=True, backward=True)
+    d = synth.make_inputs(s, seed=seed)
+    mod = DominoStack(L, h, F, t, p, q, act, fuse_wgrad=fuse)
+    with torch.no_grad():
+        mod.A.copy_(dev_bf16(d["A"]))
+        mod.B.copy_(dev_bf16(d["B"]))
+    return mod, d, s
+
+
+@pytest.mark.parametrize("act", [synth.ACT_GELU, synth.ACT_SWIGLU])
+def test_stack_module_against_oracle(built, act):
+    """DominoStack: output, input gradient through autograd and the fp32 main_grad of every layer
+    against the oracle's stack forward and backward; the no-grad forward gives the same bits."""
+    import torch
+    mod, d, s = make_stack(act, True)
+    Z = dev_bf16(d["X"]).requires_grad_(True)
+    out = mod(Z)
+    assert_tol(host_f64(out), oracle.stack_fwd(d["X"], d["A"], d["B"], s.t, act, 1e-5), "stack module output")
+    out.backward(dev_bf16(d["gY"]))
+    gZ0, dA, dB = oracle.stack_bwd(d["X"], d["A"], d["B"], d["gY"], s.t, act, 1e-5, want_w=True)
+    assert_tol(host_f64(Z.grad), gZ0, "stack module input gradient")
+    assert mod.A.grad is None and mod.B.grad is None
+    gA = mod.A.main_grad.cpu().numpy().astype(np.float64)
+    gB = mod.B.main_grad.cpu().numpy().astype(np.float64)
+    for layer in range(s.layers):
+        assert_tol(gA[layer], dA[layer], f"main_grad of A, layer {layer}")
+        assert_tol(gB[layer], dB[layer], f"main_grad of B, layer {layer}")
+    with torch.no_grad():
+        inference = mod(Z.detach())
+    assert torch.equal(inference, out.detach())
+    mod.close()
+
+
+def test_stack_module_plain_grad(built):
+    """fuse_wgrad=False: the weight gradients come back as bf16 .grad, equal to the rounded fp32
+    gradients of the fused module."""
+    import torch
+    fused, d, s = make_stack(synth.ACT_GELU, True)
+    plain, _, _ = make_stack(synth.ACT_GELU, False)
+    outs = []
+    for mod in (fused, plain):
+        Z = dev_bf16(d["X"]).requires_grad_(True)
+        mod(Z).backward(dev_bf16(d["gY"]))
+        torch.cuda.synchronize()
+        outs.append(Z.grad.clone())
+    assert torch.equal(outs[0], outs[1])
+    assert plain.A.grad.dtype == torch.bfloat16
+    assert torch.equal(plain.A.grad, fused.A.main_grad.to(torch.bfloat16))
+    assert torch.equal(plain.B.grad, fused.B.main_grad.to(torch.bfloat16))
+    fused.close()
+    plain.close()
