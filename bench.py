@@ -84,9 +84,16 @@ def load_peaks():
 # ------------------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    """nvidia-smi sampled every 50 ms while the timed region runs.  Each row carries nvidia-smi's own
+    timestamp; `stop(t0, t1)` keeps the rows whose time falls inside the host-side window of the
+    timed loop (the GPU is busy for all of it: the host only enqueues, then waits at the barrier),
+    so an idle lead-in or tail does not enter the median."""
+
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -99,12 +106,17 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # let nvidia-smi initialise before the timed region starts
+        deadline = time.time() + 3.0
+        while time.time() < deadline and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+            time.sleep(0.05)
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -112,24 +124,55 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) == len(self.FIELDS):
-                rows.append(parts)
+        with open(self.path) as fh:
+            text = fh.read()
         os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
-        reasons = set()
-        for r in rows:
-            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": float(rows[0][2]),
-                "reasons": sorted(reasons), "samples": len(rows),
-                "power_w_max": max(power) if power else None}
+        return summarize_clocks(text, t0, t1)
+
+
+def _smi_time(stamp: str):
+    """Seconds since the epoch of an nvidia-smi timestamp ("2026/12/02 11:25:03.123", local time)."""
+    import datetime
+    try:
+        return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    except ValueError:
+        return None
+
+
+def _num(v: str):
+    try:
+        return float(v)
+    except ValueError:
+        return None
+
+
+def summarize_clocks(text: str, t0=None, t1=None) -> dict:
+    """Median SM clock, maximum clock, throttle reasons and peak power of the nvidia-smi rows in
+    `text` (ClockSampler.FIELDS, csv, no header) whose timestamps fall in [t0, t1] (all rows when no
+    window is given).  `samples` counts the rows used; `in_window` says whether the window held any
+    (if not, every row is used and the record says so)."""
+    rows = []
+    for line in text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) == len(ClockSampler.FIELDS):
+            rows.append(dict(zip(ClockSampler.FIELDS, parts)))
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    use, in_window = rows, None
+    if t0 is not None and t1 is not None:
+        win = [r for r in rows if (_smi_time(r["timestamp"]) or -1.0) >= t0 and (_smi_time(r["timestamp"]) or 1e30) <= t1]
+        in_window = bool(win)
+        if win:
+            use = win
+    sm = sorted(v for v in (_num(r["clocks.sm"]) for r in use) if v is not None)
+    power = [v for v in (_num(r["power.draw"]) for r in use) if v is not None]
+    reasons = sorted({name for r in use for name in ClockSampler.REASONS
+                      if r["clocks_event_reasons." + name].lower() == "active"})
+    out = {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": _num(use[0]["clocks.max.sm"]),
+           "reasons": reasons, "samples": len(use), "power_w_max": max(power) if power else None}
+    if in_window is not None:
+        out["in_window"] = in_window
+    return out
 
 
 def physical_gpu(local_rank: int) -> int:
@@ -402,18 +445,19 @@ def run_ours(args, rank, world, local_rank):
     # ---- device-resident timing (the `value`), per-kernel events on their own streams
     clocks = ClockSampler(physical_gpu(local_rank))
     clocks.start()
-    time.sleep(0.3)
     dm.domino_timing_reset(h)
     dm.domino_timing_enable(h, True)
     n_launch0 = dm.domino_launch_count(h)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    t_loop0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
         step(X, gY)
     e1.record(stream)
     barrier()
-    clk = clocks.stop()
+    t_loop1 = time.time()
+    clk = clocks.stop(t_loop0, t_loop1)
     dm.domino_timing_enable(h, False)
     launches = dm.domino_launch_count(h) - n_launch0
     ms = e0.elapsed_time(e1)

@@ -97,3 +97,31 @@ def test_reduction_roofline_and_traffic_lookup():
 def test_kernel_hash_ignores_comments():
     code = "int a; // note\n/* block\n comment */ int b;\n\n"
     assert bench._code_only(code) == bench._code_only("int a;\n int b;")
+
+
+def test_clock_summary_keeps_the_timed_window():
+    """Only nvidia-smi rows stamped inside the timed loop's window count: an idle lead-in at a high
+    clock and low power must not enter the median, and throttle reasons outside it are ignored."""
+    import datetime
+    import bench
+
+    def row(sec, mhz, watts, cap="Not Active", thermal="Not Active"):
+        ts = datetime.datetime(2026, 12, 2, 11, 25, 0) + datetime.timedelta(seconds=sec)
+        return ", ".join([ts.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3], "0", str(mhz), "2070", str(watts), "0x0",
+                          "Not Active", thermal, "Not Active", cap])
+
+    lines = [row(0.00, 2070, 180.0, thermal="Active"), row(0.05, 2070, 185.0),         # idle lead-in
+             row(0.10, 1500, 1390.0, cap="Active"), row(0.15, 1470, 1400.0, cap="Active"),
+             row(0.20, 1485, 1395.0, cap="Active"),                                      # timed loop
+             row(0.30, 2070, 300.0)]                                                     # after it
+    text = "\n".join(lines) + "\n"
+    t0 = datetime.datetime(2026, 12, 2, 11, 25, 0).timestamp() + 0.08
+    c = bench.summarize_clocks(text, t0, t0 + 0.15)
+    assert c["samples"] == 3 and c["in_window"]
+    assert c["sm_mhz"] == 1485.0 and c["power_w_max"] == 1400.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+    every = bench.summarize_clocks(text)
+    assert every["samples"] == 6 and "in_window" not in every
+    assert "hw_thermal_slowdown" in every["reasons"]
+    empty = bench.summarize_clocks(text, t0 + 10.0, t0 + 11.0)
+    assert empty["in_window"] is False and empty["samples"] == 6
