@@ -471,6 +471,9 @@ domino_status finish(domino_handle H, const Streams& S, cudaStream_t caller, dom
 // stream; before chunk k + nslots reuses the slot, the compute stream waits for that reduction.
 struct SlotRing {
   int64_t k = 0;
+  // set by the caller for the call's last chunk: its last reduction has no later GEMM of the call
+  // to overlap, so the overlapped schedules fold it into the GEMM (second_linear)
+  bool tail = false;
 };
 
 domino_status slot_acquire(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, int* slot) {
@@ -529,6 +532,22 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
     int slot;
     DM_TRY(slot_acquire(H, P, S, R, &slot));
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
+    if (S.overlap && R.tail && qc == P.q - 1) {
+      // The call's last reduction would run with nothing left to overlap: the fused kernel adds the
+      // shard partials tile by tile inside the GEMM instead (same order, same single rounding, so the
+      // same bits), its fp32 sum in the slot's memory; the reduction stream then waits for it, so the
+      // row events and the join that follow on that stream cover it.
+      GemmArgs a = gemm_args(v_reduce, P.t, P.m, P.n, Kc, site);
+      a.a_bmul = 1;
+      a.b_row_off = int32_t(qc * P.n);
+      a.b_bmul = 1;
+      a.alpha = alpha;
+      DM_TRY(run_fused_reduce(H, kind, v_reduce, P, mapH, mapB, a, part, res_c ? res_c + qc * P.n : nullptr,
+                              Yc + qc * P.n, P.h, S.comp));
+      DM_TRY(slot_handoff(H, S, slot));
+      DM_TRY(slot_release(H, S, R, slot));
+      continue;
+    }
     GemmArgs a = gemm_args(v_partial, P.t, P.m, P.n, Kc, site);
     a.alpha = alpha;
     a.a_bmul = 1;
@@ -801,6 +820,7 @@ domino_status stack_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_i
         DM_TRY(launch(H, DOMINO_K_LAYERNORM, S.comp, "LayerNorm launch", [&] {
           return dm::launch_layernorm(src + r0 * P.h, P.m, P.h, P.eps, n_c, rstd_c, S.comp);
         }));
+        R.tail = l == P.layers - 1 && pc == P.p - 1;
         DM_TRY(mlp_chunk_fwd(H, P, S, R, n_c, mapA, mapB, Hbuf, parts, act_c, src + r0 * P.h, Z_out + r0 * P.h, 2));
         if (S.overlap) DM_CUDA(cudaEventRecord(H->ev_row[pc], S.red), "cudaEventRecord(row)");
       }
@@ -910,6 +930,7 @@ domino_status block_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_i
           DM_TRY(launch(H, DOMINO_K_LAYERNORM, S.comp, "LayerNorm launch", [&] {
             return dm::launch_layernorm(src + r0 * P.h, P.m, P.h, P.eps, lnbuf, nullptr, S.comp);
           }));
+          R.tail = l == P.layers - 1 && sub == 1 && pc == P.p - 1;
           if (sub == 0)
             DM_TRY(attn_chunk_fwd(H, P, S, R, lnbuf, mapW, mapWo, QKV, O, parts, src + r0 * P.h, Z_out + r0 * P.h));
           else
@@ -1036,6 +1057,7 @@ domino_status domino_mlp_fwd(domino_handle H, const domino_cfg* cfg, const uint1
     for (int pc = 0; pc < P.p; ++pc) {
       NvtxChunk chunk_range_(pc);
       const int64_t r0 = pc * P.m;
+      R.tail = pc == P.p - 1;
       DM_TRY(mlp_chunk_fwd(H, P, S, R, X + r0 * P.h, mapA, mapB, Hbuf, parts,
                            act_save ? act_save + r0 * P.a_rows : nullptr, nullptr, Y + r0 * P.h, 1));
     }
@@ -1215,6 +1237,7 @@ domino_status domino_mlp_fwd_fp8(domino_handle H, const domino_cfg* cfg, const u
     for (int pc = 0; pc < P.p; ++pc) {
       NvtxChunk chunk_range_(pc);
       const int64_t r0 = pc * P.m;
+      R.tail = pc == P.p - 1;
       DM_TRY(mlp_chunk_fwd_fp8(H, P, S, R, X8 + r0 * P.h, mapA, mapB, H8, parts, Y + r0 * P.h, sc));
     }
     return DOMINO_OK;
@@ -1248,6 +1271,7 @@ domino_status domino_attn_fwd(domino_handle H, const domino_cfg* cfg, const uint
     for (int pc = 0; pc < P.p; ++pc) {
       NvtxChunk chunk_range_(pc);
       const int64_t r0 = pc * P.m;
+      R.tail = pc == P.p - 1;
       DM_TRY(attn_chunk_fwd(H, P, S, R, X + r0 * P.h, mapW, mapWo, QKV, O, parts, nullptr, Y + r0 * P.h));
     }
     return DOMINO_OK;

@@ -75,7 +75,9 @@ typedef enum {
 
 /* How chunks are pipelined ("Domino 核心设计" and "实现与优化", figure 9):
  *  SERIAL: every kernel on the caller's stream, no overlap (the naive TP order).
- *  INTRA : reduction of chunk k on a side stream, overlapping the GEMMs of chunk k+1.
+ *  INTRA : reduction of chunk k on a side stream, overlapping the GEMMs of chunk k+1.  The
+ *          call's last chunk has no chunk k+1: its last column block is reduced inside its GEMM
+ *          as in FUSED (same arithmetic and bits).
  *  INTER : as INTRA; in the layer stack, row chunk j of layer l+1 starts as soon as the
  *          reductions of row chunk j of layer l finish (no wait for the whole layer).
  *  FUSED : the reduction is overlapped at tile granularity inside the second linear (and the
