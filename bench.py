@@ -43,13 +43,13 @@ _SHA_CUR = "6a3ed4a161879960"
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum (1 pass) on
     # the full-size forward+backward workload; bytes per launch, mean of the captured launches
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.607e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.856e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.897e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.590e9, "src_sha": _SHA_CUR},
     ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2.260e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 4.690e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 3.808e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.770e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 8.321e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 4.683e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 3.924e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.852e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 10.415e9, "src_sha": _SHA_CUR},
 }
 
 
