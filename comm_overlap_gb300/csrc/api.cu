@@ -518,15 +518,19 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
                             const uint16_t* res_c, uint16_t* Yc, int site, bool fp8 = false, float alpha = 1.0f) {
   const int v_reduce = fp8 ? dm::GV_F8_FWD_REDUCE : dm::GV_FWD_REDUCE;
   const int v_partial = fp8 ? dm::GV_F8_FWD_PARTIAL : dm::GV_FWD_PARTIAL;
+  // column chunk qc with the shard-sum folded into the GEMM, its fp32 sum in `sum`
+  auto fused = [&](int qc, float* sum) {
+    GemmArgs a = gemm_args(v_reduce, P.t, P.m, P.n, Kc, site);
+    a.a_bmul = 1;
+    a.b_row_off = int32_t(qc * P.n);
+    a.b_bmul = 1;
+    a.alpha = alpha;
+    return run_fused_reduce(H, kind, v_reduce, P, mapH, mapB, a, sum, res_c ? res_c + qc * P.n : nullptr,
+                            Yc + qc * P.n, P.h, S.comp);
+  };
   for (int qc = 0; qc < P.q; ++qc) {
     if (P.sched == DOMINO_SCHED_FUSED) {
-      GemmArgs a = gemm_args(v_reduce, P.t, P.m, P.n, Kc, site);
-      a.a_bmul = 1;
-      a.b_row_off = int32_t(qc * P.n);
-      a.b_bmul = 1;
-      a.alpha = alpha;
-      DM_TRY(run_fused_reduce(H, kind, v_reduce, P, mapH, mapB, a, parts, res_c ? res_c + qc * P.n : nullptr,
-                              Yc + qc * P.n, P.h, S.comp));
+      DM_TRY(fused(qc, parts));
       continue;
     }
     int slot;
@@ -537,13 +541,7 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
       // shard partials tile by tile inside the GEMM instead (same order, same single rounding, so the
       // same bits), its fp32 sum in the slot's memory; the reduction stream then waits for it, so the
       // row events and the join that follow on that stream cover it.
-      GemmArgs a = gemm_args(v_reduce, P.t, P.m, P.n, Kc, site);
-      a.a_bmul = 1;
-      a.b_row_off = int32_t(qc * P.n);
-      a.b_bmul = 1;
-      a.alpha = alpha;
-      DM_TRY(run_fused_reduce(H, kind, v_reduce, P, mapH, mapB, a, part, res_c ? res_c + qc * P.n : nullptr,
-                              Yc + qc * P.n, P.h, S.comp));
+      DM_TRY(fused(qc, part));
       DM_TRY(slot_handoff(H, S, slot));
       DM_TRY(slot_release(H, S, R, slot));
       continue;
