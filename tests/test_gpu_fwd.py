@@ -195,3 +195,19 @@ def test_shard_sum_matches_ordered_fp32_sum(lib, t):
     dm.domino_shard_sum(Pd, t, rows, cols, R, ld, Y, ld)
     torch.cuda.synchronize()
     assert np.array_equal(host_bits(Y)[:, :cols], synth.f32_to_bf16_bits(with_res))
+
+
+@pytest.mark.parametrize("act", [synth.ACT_GELU, synth.ACT_SWIGLU])
+def test_last_chunk_reduced_in_gemm_matches_serial(lib, act):
+    """The overlapped schedules reduce a call's last chunk inside its GEMM (the fused kernel) and the
+    other chunks with the shard-sum kernel; SERIAL uses the shard-sum kernel throughout.  On ragged
+    shapes (F_i and M not multiples of the tile sizes) every split gives the same bits, including a
+    single chunk (p = q = 1), which is reduced in its GEMM alone."""
+    M, h, Fi, t = 384, 256, 136, 2
+    X, A, B = real_inputs(M, h, Fi, t, act, seed=9)
+    dX, dA, dB = dev_bf16(X), dev_bf16(A), dev_bf16(B)
+    for p, q in [(1, 1), (2, 1), (1, 2), (3, 2)]:
+        serial = host_bits(lib.fwd(dm.make_cfg(M, h, Fi * t, t, p, q, act, sched=dm.SCHED_SERIAL), dX, dA, dB)[0])
+        for sched in (dm.SCHED_INTRA, dm.SCHED_INTER):
+            got = host_bits(lib.fwd(dm.make_cfg(M, h, Fi * t, t, p, q, act, sched=sched), dX, dA, dB)[0])
+            assert np.array_equal(got, serial), (p, q, sched)
