@@ -1,6 +1,7 @@
 // api.cu -- the C ABI (include/domino.h): argument validation, workspace layout, TMA maps and
 // the chunk scheduler that pipelines the shard-sum of chunk k (reduction stream) against the
-// GEMMs of chunk k+1 (compute stream).
+// GEMMs of chunk k+1 (compute stream); a call's last chunk, which has no chunk k+1, is reduced
+// inside its GEMM.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -511,8 +512,8 @@ domino_status ready(domino_handle H) {
 // ---- the row-parallel second linear of a sublayer for one row chunk: per column chunk the t shard
 // partials P_i = H_i . B_i^T (reduction length Kc per shard) into a partial slot on the compute
 // stream and their shard-sum (+ residual res_c) into Yc on the reduction stream, or both in one
-// kernel with the fused schedule.  mapH: (Kc, m, t) view of the chunk's shard inputs; mapB: the
-// shards' weights (Kc, h, t).
+// kernel with the fused schedule and for the last column chunk of a call's last row chunk
+// (R.tail).  mapH: (Kc, m, t) view of the chunk's shard inputs; mapB: the shards' weights (Kc, h, t).
 domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, SlotRing& R, int kind,
                             const CUtensorMap& mapH, const CUtensorMap& mapB, int64_t Kc, float* parts,
                             const uint16_t* res_c, uint16_t* Yc, int site, bool fp8 = false, float alpha = 1.0f) {
@@ -566,7 +567,7 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
 }
 
 // ---- forward of one MLP for row chunk pc: first linear into H, then the q column chunks of the
-// second linear into partial slots, each followed by its shard-sum on the reduction stream.
+// second linear (second_linear: partial slots reduced on the reduction stream, or fused).
 domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, SlotRing& R,
                             const uint16_t* Xc, const CUtensorMap& mapA, const CUtensorMap& mapB,
                             uint16_t* Hbuf, float* parts, uint16_t* save_c, const uint16_t* res_c,
