@@ -540,11 +540,16 @@ def run_ours(args, rank, world, local_rank):
         stream.wait_stream(cs_out)
 
     e2e_steps(max(2, args.warmup // 2))
+    clocks_e2e = ClockSampler(physical_gpu(local_rank))
+    clocks_e2e.start()
     barrier()
+    t_e2e0 = time.time()
     e0.record(stream)
     e2e_steps(args.steps)
     e1.record(stream)
     barrier()
+    t_e2e1 = time.time()
+    clk_e2e = clocks_e2e.stop(t_e2e0, t_e2e1)
     ms_e2e = e0.elapsed_time(e1)
     dm.domino_destroy(h)
     ss_alone = shard_sum_alone(s, stream) if "shard_sum" in kern and not fp8 else None
@@ -601,7 +606,8 @@ def run_ours(args, rank, world, local_rank):
                            "peaks": peaks["source"] + (" x 2 for e4m3" if fp8 else "")},
            "roofline": roof,
            "reduction": reduction_roofline(kern, work, peaks, s.name, sha, ss_alone),
-           "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+           "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "sm_mhz": clk_e2e.get("sm_mhz"), "clock_reasons": clk_e2e.get("reasons")},
            "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
     if fp8:
         out["config"]["operands"] = "e4m3 with per-tensor scales (sx, sa, sb, sh) = " + str(inp["scales"])
