@@ -56,6 +56,9 @@ INT_SHAPES = [
     (384, 208, 136, 3, 2, 2),
     (256, 64, 64, 1, 1, 1),
     (264, 72, 40, 4, 3, 3),
+    # 8190 tokens in one chunk: weight gradients over a long token range (128 K steps, the last
+    # one ragged), still exact in fp32
+    (8190, 64, 64, 2, 1, 1),
 ]
 
 
@@ -93,6 +96,7 @@ def test_bwd_integer_bit_exact(lib, shape, act):
 REAL_SHAPES = [
     (256, 256, 128, 2, 2, 1),
     (320, 192, 200, 3, 2, 2),
+    (16380, 128, 64, 2, 2, 1),  # two row chunks of 8190 tokens: long-K weight gradients
 ]
 
 
