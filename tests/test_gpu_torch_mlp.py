@@ -172,3 +172,33 @@ def test_stack_module_plain_grad(built):
     assert torch.equal(plain.B.grad, fused.B.main_grad.to(torch.bfloat16))
     fused.close()
     plain.close()
+
+
+def test_stack_module_schedules_and_splits_bit_identical(built):
+    """DominoStack under every overlapped schedule and row split gives the same bits for the output,
+    the input gradient and the fp32 weight gradients (row splits change only the order in which
+    tokens are summed into the weight gradients, so those are compared across schedules at p = 2)."""
+    import torch
+    from comm_overlap_gb300.torch_mlp import DominoStack
+    L, M, h, F, t = 2, 512, 128, 256, 2
+    s = synth.MlpShape("tss", M, h, F, synth.ACT_SWIGLU, t, 2, 2, layers=L, layernorm=True, backward=True)
+    d = synth.make_inputs(s, seed=54)
+    results = {}
+    for sched in (dm.SCHED_INTER, dm.SCHED_INTRA, dm.SCHED_FUSED, dm.SCHED_SERIAL):
+        for p in (1, 2, 4):
+            mod = DominoStack(L, h, F, t, p, 2, synth.ACT_SWIGLU, sched=sched)
+            with torch.no_grad():
+                mod.A.copy_(dev_bf16(d["A"]))
+                mod.B.copy_(dev_bf16(d["B"]))
+            Z = dev_bf16(d["X"]).requires_grad_(True)
+            out = mod(Z)
+            out.backward(dev_bf16(d["gY"]))
+            torch.cuda.synchronize()
+            results[(sched, p)] = (out.detach().clone(), Z.grad.clone(), mod.A.main_grad.clone(),
+                                   mod.B.main_grad.clone())
+            mod.close()
+    ref = results[(dm.SCHED_INTER, 2)]
+    for key, r in results.items():
+        assert torch.equal(r[0], ref[0]) and torch.equal(r[1], ref[1]), key
+        if key[1] == 2:
+            assert torch.equal(r[2], ref[2]) and torch.equal(r[3], ref[3]), key
