@@ -36,20 +36,32 @@ METRIC = "TFLOP/s of chunked TP-shard MLP fwd+bwd on 1 GB300; % of dense BF16 pe
 DEFAULT_WORKLOAD = "llama3_8b_swiglu_fwdbwd"
 ACT_NAMES = {0: "none", 1: "relu", 2: "gelu", 3: "swiglu", 4: "bilinear"}
 
-# DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by workload and
-# kernel, with the SHA-256 of the GEMM kernel source at capture time; reported only while the
-# source is unchanged.  See profiles/ for the capture commands and summaries.
-_SHA_CUR = "6a3ed4a161879960"
+# The sources each kernel kind is built from: a kind's ncu traffic (below) is reported only while
+# the code of these files (comments excluded) hashes as it did when the traffic was captured.
+KIND_SOURCES = {"gemm": ("gemm.cuh", "ptx.cuh", "actfn.cuh"), "elementwise": ("elementwise.cu", "actfn.cuh"),
+                "attention": ("attention.cu", "ptx.cuh")}
+
+
+def source_group(kernel: str) -> str:
+    if kernel.startswith("gemm_"):
+        return "gemm"
+    return "attention" if kernel == "attention" else "elementwise"
+
+
+# DRAM traffic per launch from ncu captures, keyed by workload and kernel kind, with the hash of
+# the kind's sources at capture time.  See profiles/ for the capture commands and summaries.
+_SHA_GEMM = "7ec84fc9782f21d5"
+_SHA_ELEM = "a7ed1f2e50e41e65"
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum (1 pass) on
     # the full-size forward+backward workload; bytes per launch, mean of the captured launches
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.897e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.590e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2.260e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 4.683e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 3.924e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.852e9, "src_sha": _SHA_CUR},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 10.415e9, "src_sha": _SHA_CUR},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.897e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.590e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2.260e9, "src_sha": _SHA_ELEM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 4.683e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 3.924e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.852e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 10.415e9, "src_sha": _SHA_GEMM},
 }
 
 
@@ -60,11 +72,11 @@ def _code_only(text: str) -> str:
     return "\n".join(line for line in lines if line)
 
 
-def kernel_source_sha() -> str:
-    """SHA-256 (16 hex digits) of the code, comments excluded, of the kernel sources that the
-    bench's MLP workloads run."""
+def kernel_source_sha(group: str = "gemm") -> str:
+    """SHA-256 (16 hex digits) of the code, comments excluded, of the sources of one kernel group
+    (KIND_SOURCES)."""
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "ptx.cuh", "actfn.cuh", "kernels.h", "elementwise.cu"):
+    for f in KIND_SOURCES[group]:
         with open(os.path.join(ROOT, "comm_overlap_gb300", "csrc", f), encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -116,9 +128,10 @@ class ClockSampler:
         while time.time() < deadline and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
             time.sleep(0.05)
 
-    def stop(self, t0=None, t1=None):
+    def stop_raw(self):
+        """Stops sampling; the rows taken (csv text, None when nvidia-smi could not be started)."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return None
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -127,6 +140,12 @@ class ClockSampler:
         with open(self.path) as fh:
             text = fh.read()
         os.unlink(self.path)
+        return text
+
+    def stop(self, t0=None, t1=None):
+        text = self.stop_raw()
+        if text is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         return summarize_clocks(text, t0, t1)
 
 
@@ -237,20 +256,24 @@ def config_json(s: synth.MlpShape, sched: str, n_gpus: int, reduce_ctas: int = 0
 
 # ------------------------------------------------------------------------------ CPU baseline
 
-def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
-    """Times the CPU oracle on a bounded sample of the workload; returns (flops, seconds, what)."""
-    import numpy as np
-
+def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0, min_units: int = 1):
+    """Times the CPU oracle on a bounded sample of the workload; returns (flops, seconds, what).
+    Every sampled quantity (token rows, gradient rows, ffn features) counts at least `min_units`
+    items, so that with min_units = the oracle's thread count no thread sits idle."""
     import oracle
     X, A, B = inp["X"], inp["A"], inp["B"]
     fwd_row = 2.0 * s.h * s.a_rows + 2.0 * s.F * s.h
-    n_fwd = max(2, int(round(24 * scale)))
+
+    def count(k):
+        return max(min_units, int(round(k * scale)))
+
+    n_fwd = max(2, count(24))
     rows = synth.sample_indices(s.M, n_fwd, 1)
     flops = 0.0
     t0 = time.perf_counter()
     if s.attention:
         # causality: the first positions of one sequence do not depend on the rest of it
-        upto = max(2, int(round(12 * scale)))
+        upto = max(2, count(12))
         oracle.block_fwd(X, inp["Wqkv"], inp["Wo"], A, B, s.t, s.heads, s.seq, s.act, 1e-5, seqs=[0], upto=upto)
         attn_row = 2.0 * s.h * 4 * s.h + 4.0 * s.h * (upto + 1) / 2.0
         flops += upto * (fwd_row + attn_row) * s.layers
@@ -264,15 +287,15 @@ def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
         flops += len(rows) * fwd_row
         what = f"forward of {len(rows)} token rows"
     if s.backward and s.layernorm:
-        n_b = max(1, int(round(4 * scale)))
+        n_b = count(4)
         rows_b = synth.sample_indices(s.M, n_b, 2)
         oracle.stack_bwd(X, A, B, inp["gY"], s.t, s.act, 1e-5, rows=rows_b)
         # forward again (the row backward recomputes it) plus dH and dX per layer
         flops += len(rows_b) * s.layers * (fwd_row + 2.0 * s.h * s.F + 2.0 * s.h * s.a_rows)
         what += f"; input gradient of {len(rows_b)} rows through all {s.layers} layers"
     elif s.backward:
-        n_dx = max(1, int(round(8 * scale)))
-        n_ft = max(1, int(round(24 * scale)))
+        n_dx = count(8)
+        n_ft = count(24)
         rows_b = synth.sample_indices(s.M, n_dx, 2)
         feats = synth.sample_indices(s.F, n_ft, 3)
         oracle.mlp_bwd(X, A[0], B[0], inp["gY"], s.t, s.act, rows=rows_b, want_dw=False)
@@ -284,7 +307,7 @@ def oracle_sample(s: synth.MlpShape, inp: dict, scale: float = 1.0):
     return flops, dt, what
 
 
-def reduction_roofline(kern: dict, work: dict, peaks: dict, workload: str, sha: str, alone_ms=None):
+def reduction_roofline(kern: dict, work: dict, peaks: dict, workload: str, alone_ms=None):
     """The shard-sum (the AllReduce stand-in) against the HBM roofline: algorithmic bytes per launch
     over its event duration, live (concurrent with the GEMMs of the next chunk, sharing HBM with
     them) and, when measured, alone on the same sizes.  Null when the schedule fuses the reduction
@@ -297,7 +320,7 @@ def reduction_roofline(kern: dict, work: dict, peaks: dict, workload: str, sha: 
     gbs = nbytes / (avg_ms * 1e-3) / 1e9
     out = {"bound": "hbm", "kernel": "shard_sum", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": avg_ms,
-           "concurrent_with_gemms": True, "traffic": traffic_per_launch(workload, "shard_sum", sha)}
+           "concurrent_with_gemms": True, "traffic": traffic_per_launch(workload, "shard_sum")}
     if alone_ms:
         alone = nbytes / (alone_ms * 1e-3) / 1e9
         out["alone"] = {"achieved": alone, "frac": alone / peaks["hbm_gbs"], "avg_launch_ms": alone_ms}
@@ -328,10 +351,15 @@ def shard_sum_alone(s: synth.MlpShape, stream, reps: int = 10):
     return ms
 
 
-def traffic_per_launch(workload: str, kernel: str, sha: str):
-    """ncu DRAM bytes per launch of a kernel on a workload, if captured on the current kernel code."""
+def traffic_per_launch(workload: str, kernel: str, sha: str | None = None):
+    """ncu DRAM bytes per launch of a kernel on a workload, if captured on the current code of the
+    kernel's sources (`sha`: that code's hash, computed when not given)."""
     t = NCU_TRAFFIC.get((workload, kernel))
-    return t["bytes_per_launch"] if t and t.get("src_sha") == sha else None
+    if t is None:
+        return None
+    if sha is None:
+        sha = kernel_source_sha(source_group(kernel))
+    return t["bytes_per_launch"] if t.get("src_sha") == sha else None
 
 
 def fp8_inputs(s: synth.MlpShape) -> dict:
@@ -346,14 +374,59 @@ def fp8_inputs(s: synth.MlpShape) -> dict:
             "scales": (sx, sw, sw, sh)}
 
 
-def oracle_sample_fp8(s: synth.MlpShape, inp: dict, scale: float = 1.0):
+def oracle_sample_fp8(s: synth.MlpShape, inp: dict, scale: float = 1.0, min_units: int = 1):
     import oracle
-    rows = synth.sample_indices(s.M, max(2, int(round(24 * scale))), 1)
+    rows = synth.sample_indices(s.M, max(2, min_units, int(round(24 * scale))), 1)
     t0 = time.perf_counter()
     oracle.mlp_fwd_fp8(inp["X"], inp["A"], inp["B"], s.t, s.act, inp["scales"], rows=rows)
     dt = time.perf_counter() - t0
     flops = len(rows) * (2.0 * s.h * s.a_rows + 2.0 * s.F * s.h)
     return flops, dt, f"FP8 forward of {len(rows)} token rows"
+
+
+# ------------------------------------------------------------------------------ exposed reduction
+
+def reduction_alone_ms(trace, reduce_kind: int) -> tuple[float, float]:
+    """From a launch timeline [(kind, start_ms, end_ms), ...]: the summed time of the `reduce_kind`
+    launches, and the part of it during which no launch of another kind ran (the reduction left
+    exposed on the timeline)."""
+    others = sorted((a, b) for k, a, b in trace if k != reduce_kind and b > a)
+    merged = []
+    for a, b in others:
+        if merged and a <= merged[-1][1]:
+            merged[-1][1] = max(merged[-1][1], b)
+        else:
+            merged.append([a, b])
+    total = alone = 0.0
+    for k, a, b in trace:
+        if k != reduce_kind or b <= a:
+            continue
+        total += b - a
+        covered = sum(max(0.0, min(b, y) - max(a, x)) for x, y in merged if x < b and y > a)
+        alone += (b - a) - covered
+    return total, alone
+
+
+def exposure_summary(windows: list, steps: int) -> dict:
+    """Exposed reduction from alternating timed windows: `windows` holds (arm, ms for `steps` steps,
+    median SM MHz) with arm "normal" or "noreduce".  The exposed time is the step-time difference of
+    the medians; `frac` divides it by the normal step time.  `frac_equal_clock` compares SM cycles
+    (time x median MHz) instead, removing the part of the difference that comes from the clock the
+    power cap allowed each arm."""
+    import statistics
+
+    def med(arm, i):
+        v = [w[i] for w in windows if w[0] == arm and w[i] is not None]
+        return statistics.median(v) if v else None
+
+    t_n, t_0 = med("normal", 1) / steps, med("noreduce", 1) / steps
+    f_n, f_0 = med("normal", 2), med("noreduce", 2)
+    out = {"frac": (t_n - t_0) / t_n, "ms": t_n - t_0, "ms_per_step_normal": t_n, "ms_per_step_noreduce": t_0,
+           "sm_mhz_normal": f_n, "sm_mhz_noreduce": f_0, "steps_per_window": steps,
+           "windows": [{"arm": a, "ms_per_step": ms / steps, "sm_mhz": f} for a, ms, f in windows]}
+    if f_n and f_0:
+        out["frac_equal_clock"] = (t_n * f_n - t_0 * f_0) / (t_n * f_n)
+    return out
 
 
 # ------------------------------------------------------------------------------ our arm
@@ -484,6 +557,51 @@ def run_ours(args, rank, world, local_rank):
         n, tot = dm.domino_timing_read(h, k)
         if n:
             kern[name] = {"launches": n, "total_ms": tot}
+    # the timed steps' launch timeline: how much of the shard-sum time ran with no other kernel
+    timeline = None
+    if "shard_sum" in kern:
+        tot, alone = reduction_alone_ms(dm.domino_timing_trace(h), dm.K_SHARD_SUM)
+        timeline = {"shard_sum_ms_per_step": tot / args.steps, "alone_ms_per_step": alone / args.steps,
+                    "hidden_frac": 1.0 - alone / tot if tot > 0 else None,
+                    "source": "CUDA events around every launch on its own stream (domino_timing_trace), "
+                              "timed steps of the value"}
+
+    # ---- exposed reduction: the same schedule with every shard-sum replaced by a kernel that does
+    # no reduction (domino_debug_skip_reduce), in windows of >= exposure_s seconds alternating with
+    # the normal path, clocks sampled in each window
+    exposed = None
+    if args.exposure and args.sched == "fused":
+        exposed = {"frac": None, "why": "FUSED reduces inside the GEMMs; the no-reduce variant applies to the "
+                                        "stream schedules"}
+    elif args.exposure:
+        per_step = max_over_ranks([ms_eager], world, "cuda")[0] / args.steps   # the same count on every rank
+        n_win = max(3, int(-(-args.exposure_s * 1e3 // per_step)))
+        sampler = ClockSampler(physical_gpu(local_rank))
+        sampler.start()
+        spans = []
+        for arm in ("normal", "noreduce") * args.exposure_pairs:
+            dm.domino_debug_skip_reduce(h, arm == "noreduce")
+            for _ in range(3):
+                step(X, gY)
+            barrier()
+            w0 = time.time()
+            e0.record(stream)
+            for _ in range(n_win):
+                step(X, gY)
+            e1.record(stream)
+            barrier()
+            spans.append((arm, e0.elapsed_time(e1), w0, time.time()))
+        dm.domino_debug_skip_reduce(h, False)
+        raw = sampler.stop_raw()
+        wins = [(a, max_over_ranks([w_ms], world, "cuda")[0],
+                 summarize_clocks(raw, w0, w1).get("sm_mhz") if raw else None) for a, w_ms, w0, w1 in spans]
+        exposed = exposure_summary(wins, n_win)
+        exposed["method"] = ("T_step - T_step(no-reduce): the same schedule with every shard-sum launch replaced "
+                             "by a same-grid kernel that does no reduction (residual copy in layer stacks) and the "
+                             "call's last chunk on the plain partial GEMM; medians of alternating windows")
+    if exposed is not None or timeline is not None:
+        exposed = dict(exposed or {})
+        exposed["timeline"] = timeline
     st, site = dm.domino_device_status(h)
     if st != 0:
         raise RuntimeError(f"device error word set during the benchmark: {site:#x}")
@@ -566,8 +684,8 @@ def run_ours(args, rank, world, local_rank):
     dom = max(kern, key=lambda k: kern[k]["total_ms"])
     bound, per_launch = work[dom]
     avg_ms = kern[dom]["total_ms"] / kern[dom]["launches"]
-    sha = kernel_source_sha()
-    traffic_val = traffic_per_launch(s.name, dom, sha)
+    sha = {g: kernel_source_sha(g) for g in KIND_SOURCES}
+    traffic_val = traffic_per_launch(s.name, dom)
     # FP8 contractions: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25 = 2.  The
     # sustained (power-capped) peak applies when the run hit the power cap; a run that held its
     # clocks (short steps) is held to the burst figure.
@@ -605,7 +723,7 @@ def run_ours(args, rank, world, local_rank):
                            "of_burst": value / world / (peaks["bf16_tflops"] * peak_scale),
                            "peaks": peaks["source"] + (" x 2 for e4m3" if fp8 else "")},
            "roofline": roof,
-           "reduction": reduction_roofline(kern, work, peaks, s.name, sha, ss_alone),
+           "reduction": reduction_roofline(kern, work, peaks, s.name, ss_alone),
            "e2e": {"value": e2e, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                    "sm_mhz": clk_e2e.get("sm_mhz"), "clock_reasons": clk_e2e.get("reasons")},
            "gpu_launches": launches, "clocks": clk, "kernels": kern, "kernel_src_sha": sha}
@@ -619,6 +737,7 @@ def run_ours(args, rank, world, local_rank):
         import oracle
         out["cpu_baseline"] = {"value": flops_s / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                                "kind": "oracle", "sample": what, "seconds": dt}
+    out["exposed"] = exposed
     return out
 
 
@@ -631,11 +750,14 @@ def run_reference(args, rank):
     inp = synth.make_inputs(s, seed=0)
     import oracle
     oracle.lib()
+    # each step: one item per oracle thread of every sampled quantity (rows, ffn features), so the
+    # host's cores all work; about a second per step on 16 cores for the fwd+bwd workload
+    threads = oracle.num_threads()
     for _ in range(args.warmup):
-        oracle_sample(s, inp, scale=0.1)
+        oracle_sample(s, inp, scale=0.1, min_units=threads)
     total_f, total_t, what = 0.0, 0.0, ""
     for _ in range(args.steps):
-        f, dt, what = oracle_sample(s, inp, scale=0.1)
+        f, dt, what = oracle_sample(s, inp, scale=0.1, min_units=threads)
         total_f += f
         total_t += dt
     value = total_f / total_t / 1e12
@@ -665,6 +787,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="time replays of one step captured as a CUDA graph")
     ap.add_argument("--fp8", action="store_true", help="E4M3 operands (domino_mlp_fwd_fp8), forward MLP workloads")
+    ap.add_argument("--no-exposure", dest="exposure", action="store_false",
+                    help="skip the exposed-reduction leg (normal vs no-reduce windows)")
+    ap.add_argument("--exposure-s", dest="exposure_s", type=float, default=1.1,
+                    help="seconds per timed window of the exposed-reduction leg")
+    ap.add_argument("--exposure-pairs", dest="exposure_pairs", type=int, default=2,
+                    help="normal / no-reduce window pairs of the exposed-reduction leg")
     ap.add_argument("--reduce-ctas", dest="reduce_ctas", type=int, default=0,
                     help="CTAs per shard-sum launch (cfg.reduce_ctas; 0 = the library default)")
     args = ap.parse_args()

@@ -38,6 +38,7 @@ struct domino_handle_s {
   std::vector<cudaEvent_t> timing_pool;
   int64_t launches = 0;
   int64_t fail_countdown = 0;  // > 0: the launch attempt that brings it to 0 fails (test hook)
+  bool skip_reduce = false;    // timing hook: shard-sums replaced by a kernel that does no reduction
 };
 
 namespace {
@@ -423,6 +424,9 @@ domino_status run_shard_sum(domino_handle H, const float* P, int t, int64_t rows
                             const uint16_t* res, int64_t ld_res, uint16_t* Y, int64_t ld_y,
                             int reduce_ctas, cudaStream_t st) {
   const int cap = reduce_ctas > 0 ? reduce_ctas : H->num_sms * 4;
+  if (H->skip_reduce)
+    return launch(H, DOMINO_K_SHARD_SUM, st, "no-reduce launch",
+                  [&] { return dm::launch_noreduce(rows, cols, res, ld_res, Y, ld_y, cap, st); });
   return launch(H, DOMINO_K_SHARD_SUM, st, "shard-sum launch",
                 [&] { return dm::launch_shard_sum(P, t, rows, cols, res, ld_res, Y, ld_y, cap, st); });
 }
@@ -435,6 +439,8 @@ struct Streams {
 };
 
 domino_status fork(domino_handle H, const Plan& P, cudaStream_t caller, Streams* S) {
+  if (H->skip_reduce && P.sched == DOMINO_SCHED_FUSED)
+    return fail(DOMINO_ERR_UNSUPPORTED, "domino_debug_skip_reduce applies to the stream schedules, not FUSED");
   // the fused schedule overlaps inside its kernels and runs on the caller's stream
   S->overlap = P.sched != DOMINO_SCHED_SERIAL && P.sched != DOMINO_SCHED_FUSED;
   if (!S->overlap) {
@@ -537,7 +543,7 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
     int slot;
     DM_TRY(slot_acquire(H, P, S, R, &slot));
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(parts) + P.part_slot * slot);
-    if (S.overlap && R.tail && qc == P.q - 1) {
+    if (S.overlap && R.tail && qc == P.q - 1 && !H->skip_reduce) {
       // The call's last reduction would run with nothing left to overlap: the fused kernel adds the
       // shard partials tile by tile inside the GEMM instead (same order, same single rounding, so the
       // same bits), its fp32 sum in the slot's memory; the reduction stream then waits for it, so the
@@ -949,6 +955,9 @@ domino_status block_fwd_impl(domino_handle H, const Plan& P, const uint16_t* Z_i
 namespace dm {
 // Lets other translation units of the library report a message through domino_last_error().
 void set_last_error(const std::string& msg) { t_last_error = msg; }
+// The handle checks every entry point starts with (non-null, bound to the current device), for
+// other translation units of the library.
+domino_status check_handle(domino_handle H) { return ready(H); }
 }  // namespace dm
 
 // =============================================================================================
@@ -1377,6 +1386,34 @@ domino_status domino_timing_read(domino_handle H, int32_t kind, int64_t* launche
   }
   *launches = n;
   *total_ms = ms;
+  return DOMINO_OK;
+}
+
+domino_status domino_timing_trace(domino_handle H, int64_t capacity, int32_t* kinds, double* start_ms,
+                                  double* end_ms, int64_t* count) {
+  if (!H || !count) return fail(DOMINO_ERR_INVALID_ARG, "NULL argument");
+  if (capacity < 0 || (capacity > 0 && (!kinds || !start_ms || !end_ms)))
+    return fail(DOMINO_ERR_INVALID_ARG, "capacity must be >= 0 and the arrays non-NULL");
+  *count = int64_t(H->timed.size());
+  if (H->timed.empty()) return DOMINO_OK;
+  const cudaEvent_t t0 = H->timed.front().a;
+  const int64_t n = std::min<int64_t>(capacity, *count);
+  for (int64_t i = 0; i < n; ++i) {
+    const TimedLaunch& t = H->timed[size_t(i)];
+    DM_CUDA(cudaEventSynchronize(t.b), "cudaEventSynchronize");
+    float a = 0.0f, b = 0.0f;
+    DM_CUDA(cudaEventElapsedTime(&a, t0, t.a), "cudaEventElapsedTime");
+    DM_CUDA(cudaEventElapsedTime(&b, t0, t.b), "cudaEventElapsedTime");
+    kinds[i] = t.kind;
+    start_ms[i] = a;
+    end_ms[i] = b;
+  }
+  return DOMINO_OK;
+}
+
+domino_status domino_debug_skip_reduce(domino_handle H, int32_t enable) {
+  if (!H) return fail(DOMINO_ERR_INVALID_ARG, "handle is NULL");
+  H->skip_reduce = enable != 0;
   return DOMINO_OK;
 }
 

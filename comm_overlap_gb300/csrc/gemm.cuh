@@ -80,7 +80,10 @@ constexpr int smem_bytes() {
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kGroupM = 8;  // tiles are visited in groups of 8 M-tiles for L2 reuse of B tiles
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;
-constexpr uint64_t kPeerCopyGraceNs = 100000ull;  // time given to in-flight copies after an abort
+// How long the leader's producer waits for its peer's count of issued stages: longer than any single
+// bounded wait, so the peer has left its loop by then unless its GPU stopped making progress.
+constexpr uint64_t kPeerCountTimeoutNs = 4000000000ull;
+constexpr uint64_t kPeerCopyGraceNs = 100000ull;  // last resort when the peer's count never came
 
 __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, int& g, int& mt, int& nt) {
   const int per_batch = a.m_tiles * a.n_tiles;
@@ -120,6 +123,31 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kDrainTimeoutNs) return;
+  }
+}
+
+// CTA-pair operand ring after the producers stopped: the leader CTA's producer makes sure every
+// stage copy either CTA issued has landed before the pair leaves.  Both CTAs' copies of ring use j
+// (stage j % S, phase parity (j / S) & 1) complete on the leader's full barrier, armed by the leader
+// for both CTAs' bytes.  `own` and `peer` count the uses each producer issued.  A stage is reused
+// only after its previous use was consumed, which needed both CTAs' bytes, so per stage only the
+// last use below max(own, peer) can still be pending; for it, bytes that will never come are
+// balanced first (issued by the leader only: the peer's share is marked done; by the peer only: the
+// leader arrives expecting the peer's share), then the phase is awaited (bounded).
+template <int S>
+__device__ __forceinline__ void drain_pair_ring(uint32_t full_bar0, uint32_t own, uint32_t peer,
+                                                uint32_t stage_bytes) {
+  const uint32_t end = own > peer ? own : peer;
+#pragma unroll 1
+  for (uint32_t s = 0; s < static_cast<uint32_t>(S) && s < end; ++s) {
+    const uint32_t j = s + (end - 1u - s) / S * S;  // last use of stage s below `end`
+    const uint32_t bar = full_bar0 + 8u * s;
+    const bool by_own = j < own, by_peer = j < peer;
+    if (by_own && !by_peer)
+      mbar_complete_tx(bar, stage_bytes);
+    else if (!by_own && by_peer)
+      mbar_arrive_expect_tx(bar, stage_bytes);
+    mbar_wait_drain(bar, (j / S) & 1u);
   }
 }
 
@@ -695,7 +723,9 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
                 kBarDrain = 2 * S + 4, kBarEpiIn = 2 * S + 5;  // kBarEpiIn: one per epilogue warp
   // fused shard-sum hand-off, two slots per lane quarter: ready (epilogue -> finaliser), done (back)
   constexpr int kBarFinReady = kBarEpiIn + epi_warps<EPI>(), kBarFinDone = kBarFinReady + 8;
-  static_assert(8 * (kBarFinDone + 8) <= 512, "barriers overlap the TMEM slot");
+  // the peer CTA's producer reports how many ring uses it issued (CTA pair, leader's barrier)
+  constexpr int kBarPeerCount = kBarFinDone + 8;
+  static_assert(8 * (kBarPeerCount + 1) <= 512, "barriers overlap the TMEM slot");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -703,6 +733,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
+  volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(smem + 520);  // written by the peer
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t stage0 = smem_u32(smem + kCtrlBytes);
   auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -727,6 +758,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     for (int e = 0; e < epi_warps<EPI>(); ++e) mbar_init(bar(kBarEpiIn + e), 1);
     if constexpr (EPI == EPI_F32_REDUCE)
       for (int i = 0; i < 16; ++i) mbar_init(bar(kBarFinReady + i), 1);
+    mbar_init(bar(kBarPeerCount), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -765,7 +797,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs of a pair load their own halves)
-      uint32_t s = 0, ph = 0, armed = 0, armed_ph = 0;
+      uint32_t s = 0, ph = 0, armed = 0, armed_ph = 0, issued = 0;
       bool ok = true;
       int g, mt, nt;
       for (int sq = 0; ok && tile_at<EPI>(sq, args, unit, units, g, mt, nt); ++sq) {
@@ -818,22 +850,34 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
               for (int j = 0; j < 4; ++j) tma_load_3d(sb + 8192 * j, &tmB, fb_local, n0 + 64 * j, k0, gb);
             }
           }
+          ++issued;
           if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
-      if (!ok) {
-        // let this CTA's copies still in flight land before the CTA leaves
-        if constexpr (PAIR) {
+      if constexpr (PAIR) {
+        // Both CTAs' copies complete on the leader's barriers: the peer tells the leader how many ring
+        // uses it issued, and the leader, if anything was left unconsumed (an abort on either side),
+        // waits until every copy of both CTAs has landed before the pair leaves at the final
+        // cluster barrier.
+        if (!leader) {
+          st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_issued)), 0), issued);
+          mbar_arrive_cluster(mapa_shared(bar(kBarPeerCount), 0));
+        } else if (mbar_wait_cluster_acquire(bar(kBarPeerCount), 0, kPeerCountTimeoutNs)) {
+          const uint32_t peer = *peer_issued;
+          if (!ok || peer != issued || *abort_flag) drain_pair_ring<S>(bar(kBarFull), issued, peer, R::kStageBytes);
+        } else {
+          // the peer never reported (its GPU side stopped making progress): give its copies time
           const uint64_t t0 = global_timer_ns();
           while (global_timer_ns() - t0 < kPeerCopyGraceNs) {
           }
-        } else {
-          for (int i = 0; i < S; ++i)
-            if ((armed >> i) & 1u) mbar_wait_drain(bar(kBarFull + i), (armed_ph >> i) & 1u);
         }
+      } else if (!ok) {
+        // let this CTA's copies still in flight land before the CTA leaves
+        for (int i = 0; i < S; ++i)
+          if ((armed >> i) & 1u) mbar_wait_drain(bar(kBarFull + i), (armed_ph >> i) & 1u);
       }
     }
   } else if (warp == 1) {

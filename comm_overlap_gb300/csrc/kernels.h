@@ -131,6 +131,10 @@ cudaError_t take_attn_error(int* code);
 cudaError_t launch_shard_sum(const float* P, int t, int64_t rows, int64_t cols,
                              const uint16_t* res, int64_t ld_res, uint16_t* Y, int64_t ld_y,
                              int grid_cap, cudaStream_t st);
+// Same grid as launch_shard_sum, no reduction: copies res into Y when res is given, else does
+// nothing (the timing stand-in of domino_debug_skip_reduce).
+cudaError_t launch_noreduce(int64_t rows, int64_t cols, const uint16_t* res, int64_t ld_res, uint16_t* Y,
+                            int64_t ld_y, int grid_cap, cudaStream_t st);
 cudaError_t launch_layernorm(const uint16_t* Z, int64_t rows, int64_t h, float eps, uint16_t* out,
                              float* rstd, cudaStream_t st);
 cudaError_t launch_act_eval(int act, const float* a, const float* b, float* out, float* da, float* db, int64_t n,

@@ -20,12 +20,13 @@
 
 namespace dm {
 void set_last_error(const std::string& msg);
+domino_status check_handle(domino_handle H);
 }
 
 static constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB
 
 // File-scope scratch.  Host code must not use its name as a pointer: on the host the symbol is
-// only a handle, so the device address is looked up once per device below.
+// only a handle, so the device address is looked up per device below.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
@@ -35,16 +36,26 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_static_scratch on the current device (looked up on first use).
-cudaError_t scratch_address(int dev, void** out) {
+// Device address of g_static_scratch on the current device `dev`.  Outside stream capture it is
+// looked up on every call (cheap once the module is loaded), so a device reset that moved the
+// array cannot leave a stale address behind; while `stream` is being captured into a graph the
+// address of the last uncaptured call on this device is used, since the lookup may have to load
+// the module, which capture does not allow.
+cudaError_t scratch_address(int dev, cudaStream_t stream, void** out) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+  if (cap != cudaStreamCaptureStatusNone) {
+    if (g_scratch_ptr[dev] == nullptr) return cudaErrorStreamCaptureUnsupported;
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
   }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return e;
+  g_scratch_ptr[dev] = p;
+  *out = p;
   return cudaSuccess;
 }
 
@@ -55,8 +66,11 @@ extern "C" {
 domino_status domino_mlp_fwd_noalloc(domino_handle handle, const domino_cfg* cfg, const uint16_t* X,
                                      const uint16_t* A, const uint16_t* B, uint16_t* Y,
                                      uint16_t* act_save, void* stream) {
+  // the cheap checks come first: nothing touches the device for a bad handle or problem
+  domino_status s = dm::check_handle(handle);
+  if (s != DOMINO_OK) return s;
   size_t need = 0;
-  const domino_status s = domino_workspace_size(cfg, DOMINO_PASS_FWD, &need);
+  s = domino_workspace_size(cfg, DOMINO_PASS_FWD, &need);
   if (s != DOMINO_OK) return s;
   if (need > kStaticScratchBytes) {
     dm::set_last_error("domino_mlp_fwd_noalloc: this problem needs " + std::to_string(need) +
@@ -68,9 +82,10 @@ domino_status domino_mlp_fwd_noalloc(domino_handle handle, const domino_cfg* cfg
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess && (dev < 0 || dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
   void* scratch = nullptr;
-  if (e == cudaSuccess) e = scratch_address(dev, &scratch);
+  if (e == cudaSuccess) e = scratch_address(dev, static_cast<cudaStream_t>(stream), &scratch);
   if (e != cudaSuccess) {
-    dm::set_last_error(std::string("domino_mlp_fwd_noalloc: scratch set-up failed: ") + cudaGetErrorString(e));
+    dm::set_last_error(std::string("domino_mlp_fwd_noalloc: scratch set-up failed (the first call on a device "
+                                   "must come before any stream capture): ") + cudaGetErrorString(e));
     return DOMINO_ERR_CUDA;
   }
   // The forward overwrites every scratch byte it reads (H and the partials), so nothing from a

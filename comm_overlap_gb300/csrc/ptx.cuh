@@ -244,6 +244,35 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// 32-bit store to a shared::cluster address (possibly in the peer CTA).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Wait on a local mbarrier with acquire at cluster scope (a peer CTA's writes released by its
+// remote arrive are visible afterwards); gives up after timeout_ns.
+__device__ __forceinline__ bool mbar_wait_cluster_acquire(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Marks `bytes` of the current phase's expected transactions as done without a copy (balances
+// bytes that were expected but will never arrive).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 // Relaxed arrive (no ordering of this thread's earlier memory operations): used to hand a TMEM
 // accumulator back to the MMA issuer once tcgen05.wait::ld has completed the reads of it, so the
 // arrive does not wait for the epilogue's global stores to drain.

@@ -77,6 +77,8 @@ _SIGS = {
     "domino_launch_count": [_P, ctypes.POINTER(ctypes.c_int64)],
     "domino_selftest_wait_timeout": [_P, ctypes.c_uint32, _P],
     "domino_debug_fail_launch": [_P, ctypes.c_int32],
+    "domino_debug_skip_reduce": [_P, ctypes.c_int32],
+    "domino_timing_trace": [_P, ctypes.c_int64, _P, _P, _P, ctypes.POINTER(ctypes.c_int64)],
     "domino_status_string": [ctypes.c_int32],
     "domino_last_error": [],
 }
@@ -255,6 +257,22 @@ def domino_selftest_wait_timeout(handle, timeout_us: int, stream=None) -> None:
 
 def domino_debug_fail_launch(handle, nth: int) -> None:
     _check(lib().domino_debug_fail_launch(handle, nth))
+
+
+def domino_debug_skip_reduce(handle, enable: bool) -> None:
+    _check(lib().domino_debug_skip_reduce(handle, int(bool(enable))))
+
+
+def domino_timing_trace(handle):
+    """Timed launches since the last reset, in issue order: list of (kind, start_ms, end_ms)."""
+    n = ctypes.c_int64()
+    _check(lib().domino_timing_trace(handle, 0, None, None, None, ctypes.byref(n)))
+    cap = n.value
+    kinds = (ctypes.c_int32 * max(cap, 1))()
+    t0 = (ctypes.c_double * max(cap, 1))()
+    t1 = (ctypes.c_double * max(cap, 1))()
+    _check(lib().domino_timing_trace(handle, cap, kinds, t0, t1, ctypes.byref(n)))
+    return [(int(kinds[i]), float(t0[i]), float(t1[i])) for i in range(min(cap, n.value))]
 
 
 def domino_launch_count(handle) -> int:

@@ -25,8 +25,12 @@
  *        B : t contiguous shards; shard i is h x F_i.
  *        gA, gB : fp32, same shapes as A and B.
  *  - Every pointer must be 16-byte aligned; h, F_i and h/q must be multiples of 8.
- *  - The library allocates no device memory.  Scratch space is the caller's workspace,
- *    whose size domino_workspace_size() returns; it must be 256-byte aligned.
+ *  - The library allocates no device memory at run time.  Scratch space is the caller's
+ *    workspace, whose size domino_workspace_size() returns; it must be 256-byte aligned.  The
+ *    one exception is the fixed 64 MiB scratch array of domino_mlp_fwd_noalloc, a static device
+ *    array of the library's module: every device that loads the module holds it until the
+ *    process exits (reserved when the module loads, at context creation under eager module
+ *    loading, else on first use, which may be the first domino_mlp_fwd_noalloc call).
  *  - Calls are asynchronous with respect to the host: work is ordered after prior work on
  *    `stream` (a cudaStream_t; NULL is the legacy default stream) and, on return, every
  *    launch is enqueued and joined back into `stream`.  Inputs must stay valid and outputs
@@ -170,8 +174,11 @@ DOMINO_API domino_status domino_mlp_bwd(domino_handle handle, const domino_cfg* 
  * loads the library holds until the process exits; nothing is allocated.  Problems whose
  * domino_workspace_size(cfg, DOMINO_PASS_FWD) exceeds 64 MiB are rejected with
  * DOMINO_ERR_WORKSPACE and nothing is launched.
- * The first call on each device looks up the array's device address (the device current at the
- * call); make that first call before any stream capture.  All calls share the one array: calls
+ * Each call outside stream capture looks up the array's device address on the current device
+ * (the first such call may load the module and so reserve the array); a call made while `stream`
+ * is being captured reuses the address the last uncaptured call on that device found, so make one
+ * call on each device before any stream capture, else it fails with DOMINO_ERR_CUDA.  The handle
+ * and the problem are checked before anything touches the device.  All calls share the one array: calls
  * whose work overlaps on the GPU (other streams, other host threads, other handles on the same
  * device) race on it and must be serialised by the caller.  The array keeps the last call's
  * contents; the forward overwrites every scratch byte it reads, so nothing needs clearing. */
@@ -304,6 +311,28 @@ DOMINO_API domino_status domino_timing_enable(domino_handle handle, int32_t enab
 DOMINO_API domino_status domino_timing_reset(domino_handle handle);
 DOMINO_API domino_status domino_timing_read(domino_handle handle, int32_t kind, int64_t* launches,
                                  double* total_ms);
+
+/* Launch timeline of the timed launches since the last domino_timing_reset (timing enabled), in
+ * issue order: for launch i its kernel kind and the times (ms) of its start and end events relative
+ * to the start event of the first timed launch.  Each launch is bracketed by events on the stream
+ * it was launched on, so the start event completes once that stream reached the launch (its event
+ * waits satisfied); kernels of the two internal streams can then be seen running side by side (the
+ * time in which a shard-sum runs with no GEMM beside it is the reduction left exposed, "实现与优化").
+ * Writes min(capacity, count) entries; *count receives the number of timed launches.  Synchronises
+ * on the events it reads. */
+DOMINO_API domino_status domino_timing_trace(domino_handle handle, int64_t capacity, int32_t* kinds,
+                                             double* start_ms, double* end_ms, int64_t* count);
+
+/* Measurement hook for the exposed-reduction figure ("按行切分输入 X：可达 100% 的通信隐藏": how
+ * much of the reduction the chunk pipeline hides): with enable != 0, calls through `handle` under
+ * the stream schedules (SERIAL, INTRA, INTER) run the same schedule with every shard-sum (the
+ * AllReduce stand-in) replaced by a kernel of the same grid that does no reduction -- in layer
+ * stacks it copies the residual into the output, elsewhere it does nothing -- and the call's last
+ * chunk, which INTRA / INTER reduce inside its GEMM, runs the plain fp32-partial GEMM instead.  The
+ * step time without the reduction is then comparable with the normal one.  Outputs written by a
+ * shard-sum (Y, gX, the layer outputs) are WRONG while it is on; FUSED calls fail with
+ * DOMINO_ERR_UNSUPPORTED.  0 (the default) restores the normal path. */
+DOMINO_API domino_status domino_debug_skip_reduce(domino_handle handle, int32_t enable);
 
 /* Failure-path self-test: launches a one-CTA kernel whose mbarrier wait can never complete.
  * After timeout_us (1 .. 1,000,000 microseconds) the bounded wait gives up, records

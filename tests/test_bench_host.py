@@ -81,17 +81,29 @@ def test_reduction_roofline_and_traffic_lookup():
     work = bench.kernel_work(s)
     peaks = {"hbm_gbs": 6794.5}
     kern = {"shard_sum": {"launches": 4, "total_ms": 4 * 0.34}}
-    r = bench.reduction_roofline(kern, work, peaks, s.name, bench.kernel_source_sha())
+    r = bench.reduction_roofline(kern, work, peaks, s.name)
     m, n = s.M // s.p, s.h // s.q
     assert r["algorithmic_bytes_per_launch"] == s.t * m * n * 4 + m * n * 2
     assert abs(r["achieved"] - r["algorithmic_bytes_per_launch"] / 0.34e-3 / 1e9) < 1e-6
     assert abs(r["frac"] - r["achieved"] / 6794.5) < 1e-12
     # the fused schedule launches no shard-sum: no reduction roofline
-    assert bench.reduction_roofline({}, work, peaks, s.name, "x") is None
-    # traffic is reported only for the kernel code it was captured on
-    assert bench.traffic_per_launch(s.name, "shard_sum", bench.kernel_source_sha()) is not None
+    assert bench.reduction_roofline({}, work, peaks, s.name) is None
+
+
+def test_traffic_is_reported_only_for_the_code_it_was_captured_on(monkeypatch):
+    s = synth.SHAPES["llama3_8b_swiglu_fwdbwd"]
+    cur = bench.kernel_source_sha("elementwise")
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {(s.name, "shard_sum"): {"bytes_per_launch": 2.0e9, "src_sha": cur},
+                                               (s.name, "gemm_fwd1"): {"bytes_per_launch": 5.0e9,
+                                                                       "src_sha": "0" * 16}})
+    assert bench.traffic_per_launch(s.name, "shard_sum") == 2.0e9
     assert bench.traffic_per_launch(s.name, "shard_sum", "0" * 16) is None
-    assert bench.traffic_per_launch("tiny_gelu", "shard_sum", bench.kernel_source_sha()) is None
+    assert bench.traffic_per_launch("tiny_gelu", "shard_sum") is None
+    # a GEMM entry keyed to other GEMM code is not reported
+    assert bench.traffic_per_launch(s.name, "gemm_fwd1") is None
+    # each kind is keyed to its own sources: the GEMM and shard-sum hashes differ
+    assert bench.source_group("gemm_dgrad_x") == "gemm" and bench.source_group("shard_sum") == "elementwise"
+    assert bench.kernel_source_sha("gemm") != cur
 
 
 def test_kernel_hash_ignores_comments():
@@ -125,3 +137,33 @@ def test_clock_summary_keeps_the_timed_window():
     assert "hw_thermal_slowdown" in every["reasons"]
     empty = bench.summarize_clocks(text, t0 + 10.0, t0 + 11.0)
     assert empty["in_window"] is False and empty["samples"] == 6
+
+
+def test_reduction_alone_on_a_timeline():
+    """The exposed part of each shard-sum is its time minus the union of the other kernels' spans."""
+    K_RED, K_G1, K_G2 = 2, 0, 1
+    trace = [(K_G1, 0.0, 10.0),      # GEMM of chunk 0
+             (K_G2, 9.0, 20.0),      # next GEMM, overlapping the first
+             (K_RED, 8.0, 12.0),     # reduction fully under the GEMMs
+             (K_RED, 19.0, 23.0),    # reduction half exposed: 20 .. 23
+             (K_G1, 22.0, 30.0),     # GEMM starting before that reduction ends: 22 .. 23 hidden
+             (K_RED, 31.0, 32.5)]    # reduction after everything: exposed
+    total, alone = bench.reduction_alone_ms(trace, K_RED)
+    assert abs(total - (4.0 + 4.0 + 1.5)) < 1e-12
+    assert abs(alone - (0.0 + 2.0 + 1.5)) < 1e-12
+    assert bench.reduction_alone_ms([(K_G1, 0.0, 1.0)], K_RED) == (0.0, 0.0)
+
+
+def test_exposure_summary_of_alternating_windows():
+    steps = 50
+    wins = [("normal", 50 * 22.0, 1500.0), ("noreduce", 50 * 21.0, 1540.0),
+            ("normal", 50 * 22.2, 1510.0), ("noreduce", 50 * 21.2, 1530.0)]
+    e = bench.exposure_summary(wins, steps)
+    t_n, t_0, f_n, f_0 = 22.1, 21.1, 1505.0, 1535.0
+    assert abs(e["ms_per_step_normal"] - t_n) < 1e-9 and abs(e["ms_per_step_noreduce"] - t_0) < 1e-9
+    assert abs(e["ms"] - 1.0) < 1e-9 and abs(e["frac"] - 1.0 / t_n) < 1e-12
+    assert e["sm_mhz_normal"] == f_n and e["sm_mhz_noreduce"] == f_0
+    assert abs(e["frac_equal_clock"] - (t_n * f_n - t_0 * f_0) / (t_n * f_n)) < 1e-12
+    assert len(e["windows"]) == 4 and e["steps_per_window"] == steps
+    # without clock samples the equal-clock figure is left out
+    assert "frac_equal_clock" not in bench.exposure_summary([(a, ms, None) for a, ms, _ in wins], steps)

@@ -1,7 +1,9 @@
 """Parity at the five workloads' full sizes, in the launch configuration bench.py times.
 
 The oracle evaluates sampled outputs one by one (rows of Y / gX / the stack output, ffn
-features of the weight gradients); the GPU computes the whole problem.  Row-split results are
+features of the weight gradients); the GPU computes the whole problem.  The samples always hold
+both sides of every row-chunk and tile boundary and the last tile of each chunk (edge_rows), and,
+for the weight gradients, the first and last feature of every shard (edge_feats).  Row-split results are
 also checked bitwise against the unsplit (p = 1) GPU run at full size.
 """
 import numpy as np
@@ -16,6 +18,32 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 N_ROWS = 12
 N_FEATS = 6
+TILE_M = 256   # output rows of one GEMM tile (a CTA pair's 2 x 128)
+TILE_N = 256   # output columns of one GEMM tile
+
+
+def edge_rows(M: int, m: int, seed: int, n_random: int = N_ROWS) -> np.ndarray:
+    """Rows where a row-indexing mistake would show: both sides of every row-chunk boundary (m - 1,
+    m, ...), of the first tile boundaries inside a chunk (127/128 inside a CTA's half, 255/256
+    between tiles) and of the chunk's last tile (m - 256 .. m - 1, the last round of the persistent
+    grid), plus `n_random` rows drawn at random (0 and M - 1 always among them)."""
+    rows = set(synth.sample_indices(M, n_random, seed).tolist())
+    for c0 in range(0, M, m):
+        for off in (0, 1, 127, 128, TILE_M - 1, TILE_M, m - TILE_M - 1, m - TILE_M, m - 129, m - 128, m - 1):
+            if 0 <= off < m:
+                rows.add(c0 + off)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def edge_feats(Fi: int, t: int, seed: int, n_random: int = N_FEATS) -> np.ndarray:
+    """ffn features to check in the weight gradients: the first and last feature of every shard and
+    both sides of the shard's first tile boundary (TILE_N - 1, TILE_N), plus `n_random` at random."""
+    feats = set(synth.sample_indices(Fi * t, n_random, seed).tolist())
+    for i in range(t):
+        for j in (0, TILE_N - 1, TILE_N, Fi - 1):
+            if 0 <= j < Fi:
+                feats.add(i * Fi + j)
+    return np.array(sorted(feats), dtype=np.int64)
 
 
 @pytest.fixture(scope="module")
@@ -44,7 +72,7 @@ def test_forward_full_size(lib, name):
     d = synth.make_inputs(s, seed=0)
     X, A, B = dev_bf16(d["X"]), dev_bf16(d["A"][0]), dev_bf16(d["B"][0])
     Y, _ = lib.fwd(cfg_of(s), X, A, B)
-    rows = synth.sample_indices(s.M, N_ROWS if s.M > 1024 else s.M, 10)
+    rows = edge_rows(s.M, s.M // s.p, 10) if s.M > 1024 else np.arange(s.M, dtype=np.int64)
     ref = oracle.mlp_fwd(d["X"], d["A"][0], d["B"][0], s.t, s.act, rows=rows)
     assert_tol(host_f64(Y[torch.from_numpy(rows).cuda()]), ref, f"{name} sampled rows")
     if s.p > 1:
@@ -58,7 +86,7 @@ def test_stack_full_size(lib):
     d = synth.make_inputs(s, seed=0)
     X, A, B = dev_bf16(d["X"]), dev_bf16(d["A"]), dev_bf16(d["B"])
     Z = lib.stack(cfg_of(s, sched=dm.SCHED_INTER), X, A, B)
-    rows = synth.sample_indices(s.M, N_ROWS, 11)
+    rows = edge_rows(s.M, s.M // s.p, 11)
     ref = oracle.stack_fwd(d["X"], d["A"], d["B"], s.t, s.act, 1e-5, rows=rows)
     assert_tol(host_f64(Z[torch.from_numpy(rows).cuda()]), ref, "stack sampled rows")
     Z1 = lib.stack(cfg_of(s, p=1, sched=dm.SCHED_INTER), X, A, B)
@@ -75,13 +103,13 @@ def test_forward_backward_full_size(lib):
     gA0 = torch.zeros((s.a_rows, s.h), dtype=torch.float32, device="cuda")
     gB0 = torch.zeros((s.t, s.h, s.Fi), dtype=torch.float32, device="cuda")
     gX, gA, gB = lib.bwd(cfg, X, A, B, S, gY, gA0, gB0)
-    rows = synth.sample_indices(s.M, N_ROWS, 12)
+    rows = edge_rows(s.M, s.M // s.p, 12)
     ridx = torch.from_numpy(rows).cuda()
     Yref = oracle.mlp_fwd(d["X"], d["A"][0], d["B"][0], s.t, s.act, rows=rows)
     assert_tol(host_f64(Y[ridx]), Yref, "Y sampled rows")
-    dX, _, _ = oracle.mlp_bwd(d["X"], d["A"][0], d["B"][0], d["gY"], s.t, s.act, rows=rows[:6], want_dw=False)
-    assert_tol(host_f64(gX[ridx[:6]]), dX, "gX sampled rows")
-    feats = synth.sample_indices(s.F, N_FEATS, 13)
+    dX, _, _ = oracle.mlp_bwd(d["X"], d["A"][0], d["B"][0], d["gY"], s.t, s.act, rows=rows, want_dw=False)
+    assert_tol(host_f64(gX[ridx]), dX, "gX sampled rows")
+    feats = edge_feats(s.Fi, s.t, 13)
     _, dA, dB = oracle.mlp_bwd(d["X"], d["A"][0], d["B"][0], d["gY"], s.t, s.act, feats=feats, want_dx=False)
     gA_h, gB_h = gA.cpu().numpy().astype(np.float64), gB.cpu().numpy().astype(np.float64)
     for k, f in enumerate(feats):
