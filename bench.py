@@ -49,19 +49,20 @@ def source_group(kernel: str) -> str:
 
 
 # DRAM traffic per launch from ncu captures, keyed by workload and kernel kind, with the hash of
-# the kind's sources at capture time.  See profiles/ for the capture commands and summaries.
-_SHA_GEMM = "7ec84fc9782f21d5"
+# the kind's sources at capture time (profiles/traffic_llama3_8b_swiglu_fwdbwd.md has the commands).
+# Captured one kernel and one launch at a time on a small case of the workload (M = 8192 tokens in
+# one row chunk, m = 8192 per launch) and scaled x 2 to the m = 16384 launch of the full workload:
+# only kinds whose reduction length does not grow with the tokens are listed, since their traffic
+# grows in proportion to the rows a launch processes.  The weight-gradient GEMMs reduce over the
+# tokens, so theirs does not scale that way and is left out (reported null).
+_SHA_GEMM = "d40b18e9327d2c09"
 _SHA_ELEM = "a7ed1f2e50e41e65"
 NCU_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum (1 pass) on
-    # the full-size forward+backward workload; bytes per launch, mean of the captured launches
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 4.897e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2.590e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2.260e9, "src_sha": _SHA_ELEM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 4.683e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_b"): {"bytes_per_launch": 3.924e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 4.852e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_wgrad_a"): {"bytes_per_launch": 10.415e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 2 * 1.911e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2 * 1.449e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2 * 1.091e9, "src_sha": _SHA_ELEM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 2 * 2.353e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 2 * 2.327e9, "src_sha": _SHA_GEMM},
 }
 
 
@@ -87,8 +88,13 @@ def load_peaks():
     try:
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
-                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "source": "measured"}
+        out = {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+               "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "source": "measured"}
+        # the median SM clock under which the sustained peak was measured, for per-clock comparisons
+        mhz = (d.get("clocks_under_load") or {}).get("sm_mhz_median")
+        if mhz:
+            out["sustained_sm_mhz"] = float(mhz)
+        return out
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
@@ -706,6 +712,13 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic_val, "peak_kind": f"hbm copy ({peaks['source']})",
                 "algorithmic_bytes_per_launch": per_launch, "avg_launch_ms": avg_ms}
+    # the same fraction per SM cycle: a kernel that ran at another clock than the one the sustained
+    # peak was measured at is compared at equal clocks (TFLOP/s per MHz)
+    if bound == "tensor" and clk.get("sm_mhz") and peaks.get("sustained_sm_mhz"):
+        per_mhz_peak = peaks["bf16_tflops_sustained"] * peak_scale / peaks["sustained_sm_mhz"]
+        roof["per_clock"] = {"frac": achieved / clk["sm_mhz"] / per_mhz_peak, "sm_mhz": clk["sm_mhz"],
+                             "peak_sm_mhz": peaks["sustained_sm_mhz"],
+                             "note": "achieved / run clock over sustained peak / its clock"}
     total_k = sum(v["total_ms"] for v in kern.values())
     for name, v in kern.items():
         b, w = work[name]
