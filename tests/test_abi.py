@@ -153,3 +153,20 @@ def test_plan_log(dlib, capfd, monkeypatch):
     err = capfd.readouterr().err
     assert "domino plan: pass=fwd M=512 h=256 ffn=512 t=2 p=2 q=1 (chunk 256 x 256)" in err
     assert f"workspace={n} B" in err and "sched=intra" in err
+
+
+def test_size_limits_are_exact(dlib):
+    """The documented ranges are accepted up to their last value and refused one past it: at most
+    2^31 - 1 tokens, and one reduction launch covering fewer than 2^31 16-byte vectors (m x n / 8)."""
+    big = (1 << 31) - 1
+    assert dlib.domino_workspace_size(dlib.make_cfg(M=big, h=8, ffn=8, t=1), dlib.PASS_FWD) > 0
+    with pytest.raises(dlib.DominoError) as e:
+        dlib.domino_workspace_size(dlib.make_cfg(M=big + 1, h=8, ffn=8, t=1), dlib.PASS_FWD)
+    assert e.value.status == 2
+    # m x n / 8 = (2^30 - 1) x 2 is the last count below 2^31; 2^30 x 2 is refused
+    assert dlib.domino_workspace_size(dlib.make_cfg(M=(1 << 30) - 1, h=16, ffn=8, t=1), dlib.PASS_FWD) > 0
+    with pytest.raises(dlib.DominoError) as e:
+        dlib.domino_workspace_size(dlib.make_cfg(M=1 << 30, h=16, ffn=8, t=1), dlib.PASS_FWD)
+    assert e.value.status == 2
+    # a row split brings the same problem back under the reduction limit
+    assert dlib.domino_workspace_size(dlib.make_cfg(M=1 << 30, h=16, ffn=8, t=1, p=2), dlib.PASS_FWD) > 0
