@@ -55,22 +55,32 @@ constexpr int epi_warps() { return 4; }
 // The fused shard-sum adds four finaliser warps (one per lane quarter) after the epilogue warps.
 template <int EPI>
 constexpr int fin_warps() { return EPI == EPI_F32_REDUCE ? 4 : 0; }
+// The activation backward and the non-gated forward activation add two helper warps (sub-partitions
+// 2 and 3) that do the arithmetic of lane quarter 1 for its reader warp, which shares a
+// sub-partition with the MMA issuer.
 template <int EPI>
-constexpr int block_threads() { return 64 + 32 * (epi_warps<EPI>() + fin_warps<EPI>()); }
+constexpr int helper_warps() { return (is_act_bwd(EPI) || EPI == EPI_ACT_BF16) ? 2 : 0; }
+template <int EPI>
+constexpr int block_threads() { return 64 + 32 * (epi_warps<EPI>() + fin_warps<EPI>() + helper_warps<EPI>()); }
 // Epilogues that move data with TMA stage it in shared memory, per epilogue warp:
 //  fp32 partials: two 4 KiB buffers (32 rows x 32 fp32, 128-byte swizzle);
-//  activation backward: 4 KiB of inputs (Z or G, U) and 6 KiB of outputs (dZ or dG, dU; H), as
-//  32 rows x 32 bf16 boxes with 64-byte swizzle.
-//  forward activation: up to three 2 KiB output boxes (H; saved Z, or G and U), 64-byte swizzle.
+//  activation backward: per warp that does arithmetic (epilogue warps 2-4 and the two helpers; the
+//  reader of quarter 1 needs none) 4 KiB of inputs (Z or G, U) and 6 KiB of outputs (dZ or dG, dU;
+//  H), as 32 rows x 32 bf16 boxes with 64-byte swizzle, then the reader's two 4 KiB slots.
+//  forward activation: up to three 2 KiB output boxes (H; saved Z, or G and U), 64-byte swizzle; the
+//  non-gated form (two boxes) for warps 2-4 and its two helpers, then the reader's two slots.
 constexpr int kActBwdWarpBytes = 10240;
-constexpr int kFwdWarpBytes = 6144;
+constexpr int kFwdWarpBytes = 6144;    // gated forward: H, G, U boxes
+constexpr int kFwdActWarpBytes = 4096; // non-gated forward: H, Z boxes
 constexpr bool is_act_fwd(int epi) { return epi == EPI_ACT_BF16 || epi == EPI_GLU_BF16; }
 constexpr bool is_act_f8(int epi) { return epi == EPI_ACT_F8 || epi == EPI_GLU_F8; }
 constexpr bool is_gated_b(int epi) { return epi == EPI_GLU_BF16 || epi == EPI_GLU_F8; }
 template <int EPI>
 constexpr int staging_bytes() {
   return (EPI == EPI_F32_STORE || EPI == EPI_F32_REDUCE) ? 4 * 2 * 4096
-                              : (is_act_bwd(EPI) ? 4 * kActBwdWarpBytes : (is_act_fwd(EPI) ? 4 * kFwdWarpBytes : 0));
+                              : (is_act_bwd(EPI) ? 5 * kActBwdWarpBytes + 2 * 4096
+                                                 : (EPI == EPI_ACT_BF16 ? 5 * kFwdActWarpBytes + 2 * 4096
+                                                                        : (is_act_fwd(EPI) ? 4 * kFwdWarpBytes : 0)));
 }
 template <bool PAIR, int EPI>
 constexpr int smem_bytes() {
@@ -279,32 +289,96 @@ __device__ __forceinline__ void bwd_act_chunk(const uint32_t (&zi)[16], const ui
   }
 }
 
-// Activation-backward epilogue (EPI_ACT_BWD / EPI_GLU_BWD) for all tiles of one warp (32 rows x 256
+// Where a warp of the activation-backward epilogue takes the accumulator from: its TMEM lane quarter
+// directly, or a shared-memory slot that the quarter's reader warp filled (epilogue_acc_reader).
+enum : int { ACC_TMEM = 0, ACC_SLOT = 1 };
+
+// The accumulator hand-off of one TMEM lane quarter: two 4 KiB slots of 32 rows x 32 fp32 (one
+// 32-column chunk), 128-byte rows with 16-byte piece j of row r at position j ^ (r % 8).
+constexpr uint32_t kAccSlotBytes = 4096;
+
+// Reader warp of TMEM lane quarter 1, the quarter read by the warp that shares a sub-partition with
+// the MMA-issuing warp: for every tile of the unit it copies the accumulator, 32 columns at a time,
+// into slot (chunk index % 2), where the helper warp of that slot takes it (epilogue_act_bwd_tma,
+// ACC_SLOT), and hands the accumulator back to the MMA issuer as soon as all its chunks are copied.
+// The arithmetic of the quarter then runs on other sub-partitions: done by the warp beside the MMA
+// issuer, it delayed the issue of the tensor-core instructions and slowed the main loop (measured).
+// Slot barriers: full (the 32 lanes of the reader arrive) and empty (the 32 lanes of the helper
+// arrive), so every lane's shared-memory accesses are ordered by its own arrive.  False if a bounded
+// wait gave up.
+template <int kOutN>
+__device__ __forceinline__ void epilogue_acc_reader(uint32_t tmem_q, uint32_t full_bar0, uint32_t empty_addr0,
+                                                    uint32_t slot_full0, uint32_t slot_empty0, uint32_t slot_buf0,
+                                                    bool pair, int unit, int units, int total, int lane,
+                                                    volatile int* abort_flag, int* err, int site) {
+  const uint32_t row = static_cast<uint32_t>(lane) * 128u, key = static_cast<uint32_t>(lane) & 7u;
+  uint32_t k = 0;  // chunks handed over so far
+  int it = 0;
+  for (int tile = unit; tile < total; tile += units, ++it) {
+    const int acc = it & 1;
+    const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+    const bool ok = mbar_wait(full_bar0 + 8u * acc, use, abort_flag, err, site);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return;
+    tc_fence_after();
+#pragma unroll 1
+    for (int cc = 0; cc < kOutN; cc += 32, ++k) {
+      const uint32_t slot = k & 1u, sphase = (k >> 1) & 1u;
+      uint32_t r[32];
+      tmem_ld32(tmem_q + static_cast<uint32_t>(acc * kBN + cc), r);
+      const bool free_ok = mbar_wait(slot_empty0 + 8u * slot, sphase ^ 1u, abort_flag, err, site + 1);
+      tmem_ld_wait();
+      if (!__all_sync(0xFFFFFFFFu, free_ok)) return;
+      const uint32_t dst = slot_buf0 + slot * kAccSlotBytes + row;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(dst + ((static_cast<uint32_t>(j) ^ key) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                     r[4 * j + 3]);
+      mbar_arrive(slot_full0 + 8u * slot);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (pair)
+        mbar_arrive_cluster_relaxed(mapa_shared(empty_addr0 + 8u * acc, 0));
+      else
+        mbar_arrive(empty_addr0 + 8u * acc);
+    }
+  }
+}
+
+// Activation-backward epilogue (EPI_ACT_BWD / EPI_GLU_BWD) for the tiles of one warp (32 rows x 256
 // columns of each tile, in 32-column chunks), with every global access a TMA box:
+//  * SRC = ACC_TMEM: the warp reads its own TMEM lane quarter, every chunk of every tile, and hands
+//    each accumulator back after its last chunk;
+//  * SRC = ACC_SLOT: a helper warp for quarter 1 takes chunks c_first, c_first + c_step, ... of every
+//    tile from the reader's slot `slot` (barriers slot_full / slot_empty), never touching TMEM;
 //  * the saved first-linear output of the chunk (Z, or G and U) is loaded into the warp's input
 //    buffer; the next chunk's load is issued as soon as the lanes have read the current one, so it
-//    overlaps the current chunk's TMEM read, arithmetic and stores;
+//    overlaps the current chunk's accumulator read, arithmetic and stores;
 //  * dZ (or dG, dU) and the recomputed activation H are written into the warp's output buffer and
 //    stored with bulk tensor copies (clipped at the tensor edges).
 // Shared-memory boxes are 32 rows x 64 bytes with 64-byte swizzle: 16-byte chunk j of row r sits at
 // position j ^ ((r >> 1) & 3) of the row.
-template <int EPI, int kTileM, int kOutN>
+template <int EPI, int kTileM, int kOutN, int SRC>
 __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const EpiMaps& em, uint32_t tmem_q,
                                                      uint32_t full_bar0, uint32_t empty_addr0, uint32_t in_bar,
-                                                     uint32_t buf, bool pair, int unit, int units, int total,
-                                                     int row_off, int lane, volatile int* abort_flag, int* err) {
+                                                     uint32_t buf, uint32_t slot_full, uint32_t slot_empty,
+                                                     uint32_t slot_buf, int c_first, int c_step, bool pair,
+                                                     int unit, int units, int total, int row_off, int lane,
+                                                     volatile int* abort_flag, int* err) {
   constexpr bool kGlu = EPI == EPI_GLU_BWD;
   constexpr uint32_t kInBytes = kGlu ? 4096u : 2048u;
   const uint32_t ibuf = buf, obuf = buf + 4096u;
   const uint32_t rsw = static_cast<uint32_t>(lane) * 64u;          // this lane's row in a box
   const uint32_t rx = (static_cast<uint32_t>(lane) >> 1) & 3u;      // its 64-byte swizzle key
+  const int c0 = 32 * c_first, cstep = 32 * c_step;
   struct Cursor {
     int tile, cc;
   };
   auto advance = [&](Cursor& c) {
-    c.cc += 32;
+    c.cc += cstep;
     if (c.cc >= kOutN) {
-      c.cc = 0;
+      c.cc = c0;
       c.tile += units;
     }
   };
@@ -329,25 +403,45 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
       if constexpr (kGlu) tma_load_3d(ibuf + 2048u, &em.m[1], in_bar, col, row0, g);
     }
   };
-  Cursor pf{unit, 0};
+  Cursor pf{unit, c0};
   issue(pf);
   advance(pf);
-  uint32_t in_phase = 0, n_stored = 0;
+  uint32_t in_phase = 0, n_stored = 0, n_slot = 0;
+  const uint32_t key = static_cast<uint32_t>(lane) & 7u;
   int it = 0;
   for (int tile = unit; tile < total; tile += units, ++it) {
     const int acc = it & 1;
-    const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-    const bool ok = mbar_wait(full_bar0 + 8u * acc, use, abort_flag, err, a.err_site + 4);
-    if (!__all_sync(0xFFFFFFFFu, ok)) break;
-    tc_fence_after();
+    if constexpr (SRC == ACC_TMEM) {
+      const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+      const bool ok = mbar_wait(full_bar0 + 8u * acc, use, abort_flag, err, a.err_site + 4);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+    }
     bool aborted = false;
 #pragma unroll 1
-    for (int cc = 0; cc < kOutN; cc += 32) {
+    for (int cc = c0; cc < kOutN; cc += cstep) {
       const Cursor cur{tile, cc};
       int g, row0, col;
       const bool valid = chunk(cur, g, row0, col);
       uint32_t r[32];
-      tmem_ld32(tmem_q + static_cast<uint32_t>(acc * kBN + cc), r);
+      if constexpr (SRC == ACC_TMEM) {
+        tmem_ld32(tmem_q + static_cast<uint32_t>(acc * kBN + cc), r);
+      } else {
+        // every chunk passes through the slot, in range or not, so the reader's count stays in step
+        const bool got = mbar_wait(slot_full, n_slot & 1u, abort_flag, err, a.err_site + 8);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          aborted = true;
+          break;
+        }
+        ++n_slot;
+        const uint32_t src = slot_buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 v = ld_shared_v4(src + ((static_cast<uint32_t>(j) ^ key) << 4));
+          r[4 * j] = v.x; r[4 * j + 1] = v.y; r[4 * j + 2] = v.z; r[4 * j + 3] = v.w;
+        }
+        mbar_arrive(slot_empty);
+      }
       uint32_t zi[16], ui[16];
       if (valid) {
         const bool got = mbar_wait(in_bar, in_phase, abort_flag, err, a.err_site + 5);
@@ -357,7 +451,7 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
         }
         if (!__all_sync(0xFFFFFFFFu, got)) {
           aborted = true;
-          tmem_ld_wait();
+          if constexpr (SRC == ACC_TMEM) tmem_ld_wait();
           break;
         }
 #pragma unroll
@@ -374,7 +468,7 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
       __syncwarp();
       issue(pf);
       advance(pf);
-      tmem_ld_wait();
+      if constexpr (SRC == ACC_TMEM) tmem_ld_wait();
       if (!valid) continue;
       uint32_t o1[16], o2[16], oh[16];
       if constexpr (kGlu) {
@@ -409,13 +503,15 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
       ++n_stored;
     }
     if (aborted) break;
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      if (pair)
-        mbar_arrive_cluster_relaxed(mapa_shared(empty_addr0 + 8u * acc, 0));
-      else
-        mbar_arrive(empty_addr0 + 8u * acc);
+    if constexpr (SRC == ACC_TMEM) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (pair)
+          mbar_arrive_cluster_relaxed(mapa_shared(empty_addr0 + 8u * acc, 0));
+        else
+          mbar_arrive(empty_addr0 + 8u * acc);
+      }
     }
   }
   if (lane == 0) {
@@ -432,14 +528,58 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
 // copy is requested, the pre-activation Z (or G and U), each rounded to bf16, written to the warp's
 // staging boxes (64-byte swizzle) and stored with bulk tensor copies.  Maps: m[0] H, m[1] Z or G,
 // m[2] U.  The staging boxes are rewritten once the previous chunk's stores have read them.
+// fwd_chunk_store does one chunk from the accumulator values rz (and ru, the up columns of the gated
+// form) in registers; epilogue_fwd_tma takes them from the warp's TMEM lane quarter.
+template <int EPI>
+__device__ __forceinline__ void fwd_chunk_store(const GemmArgs& a, const EpiMaps& em, const uint32_t (&rz)[32],
+                                                const uint32_t (&ru)[32], int g, int row0, int col, uint32_t buf,
+                                                uint32_t& nstore, int lane) {
+  constexpr bool kGlu = EPI == EPI_GLU_BF16;
+  const bool save = a.out1 != nullptr;
+  const uint32_t rsw = static_cast<uint32_t>(lane) * 64u;
+  const uint32_t rx = (static_cast<uint32_t>(lane) >> 1) & 3u;
+  uint32_t oh[16], oz[16], ou[16];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float z0 = __uint_as_float(rz[e]), z1 = __uint_as_float(rz[e + 1]);
+    if constexpr (kGlu) {
+      const float u0 = __uint_as_float(ru[e]), u1 = __uint_as_float(ru[e + 1]);
+      oh[e >> 1] = pack_bf16x2(glu_fwd(a.act, z0, u0), glu_fwd(a.act, z1, u1));
+      ou[e >> 1] = pack_bf16x2(u0, u1);
+    } else {
+      oh[e >> 1] = pack_bf16x2(act_fwd(a.act, z0), act_fwd(a.act, z1));
+    }
+    oz[e >> 1] = pack_bf16x2(z0, z1);
+  }
+  if (lane == 0 && nstore > 0) bulk_wait_group_read<0>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t off = rsw + ((static_cast<uint32_t>(j) ^ rx) << 4);
+    st_shared_v4(buf + off, oh[4 * j], oh[4 * j + 1], oh[4 * j + 2], oh[4 * j + 3]);
+    if (save) {
+      st_shared_v4(buf + 2048u + off, oz[4 * j], oz[4 * j + 1], oz[4 * j + 2], oz[4 * j + 3]);
+      if constexpr (kGlu) st_shared_v4(buf + 4096u + off, ou[4 * j], ou[4 * j + 1], ou[4 * j + 2], ou[4 * j + 3]);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(&em.m[0], buf, col, row0, g);
+    if (save) {
+      tma_store_3d(&em.m[1], buf + 2048u, col, row0, g);
+      if constexpr (kGlu) tma_store_3d(&em.m[2], buf + 4096u, col, row0, g);
+    }
+    bulk_commit_group();
+  }
+  ++nstore;
+}
+
 template <int EPI, int NC>
 __device__ __forceinline__ void epilogue_fwd_tma(const GemmArgs& a, const EpiMaps& em, uint32_t tacc, int g,
                                                  int row0, int col0, uint32_t buf, uint32_t& nstore, int lane) {
   constexpr bool kGlu = EPI == EPI_GLU_BF16;
   if (row0 >= a.M) return;
-  const bool save = a.out1 != nullptr;
-  const uint32_t rsw = static_cast<uint32_t>(lane) * 64u;
-  const uint32_t rx = (static_cast<uint32_t>(lane) >> 1) & 3u;
 #pragma unroll 1
   for (int cc = 0; cc < NC; cc += 32) {
     const int col = col0 + cc;
@@ -448,42 +588,48 @@ __device__ __forceinline__ void epilogue_fwd_tma(const GemmArgs& a, const EpiMap
     tmem_ld32(tacc + cc, rz);
     if constexpr (kGlu) tmem_ld32(tacc + 128 + cc, ru);
     tmem_ld_wait();
-    uint32_t oh[16], oz[16], ou[16];
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const float z0 = __uint_as_float(rz[e]), z1 = __uint_as_float(rz[e + 1]);
-      if constexpr (kGlu) {
-        const float u0 = __uint_as_float(ru[e]), u1 = __uint_as_float(ru[e + 1]);
-        oh[e >> 1] = pack_bf16x2(glu_fwd(a.act, z0, u0), glu_fwd(a.act, z1, u1));
-        ou[e >> 1] = pack_bf16x2(u0, u1);
-      } else {
-        oh[e >> 1] = pack_bf16x2(act_fwd(a.act, z0), act_fwd(a.act, z1));
-      }
-      oz[e >> 1] = pack_bf16x2(z0, z1);
-    }
-    if (lane == 0 && nstore > 0) bulk_wait_group_read<0>();
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t off = rsw + ((static_cast<uint32_t>(j) ^ rx) << 4);
-      st_shared_v4(buf + off, oh[4 * j], oh[4 * j + 1], oh[4 * j + 2], oh[4 * j + 3]);
-      if (save) {
-        st_shared_v4(buf + 2048u + off, oz[4 * j], oz[4 * j + 1], oz[4 * j + 2], oz[4 * j + 3]);
-        if constexpr (kGlu) st_shared_v4(buf + 4096u + off, ou[4 * j], ou[4 * j + 1], ou[4 * j + 2], ou[4 * j + 3]);
-      }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_3d(&em.m[0], buf, col, row0, g);
-      if (save) {
-        tma_store_3d(&em.m[1], buf + 2048u, col, row0, g);
-        if constexpr (kGlu) tma_store_3d(&em.m[2], buf + 4096u, col, row0, g);
-      }
-      bulk_commit_group();
-    }
-    ++nstore;
+    fwd_chunk_store<EPI>(a, em, rz, ru, g, row0, col, buf, nstore, lane);
   }
+}
+
+// Helper warp of the non-gated forward epilogue for TMEM lane quarter 1 (see epilogue_acc_reader): for
+// every tile of the unit, chunks c_first, c_first + 2, ... of its 256 columns arrive in slot
+// `slot_buf` (barriers slot_full / slot_empty) and leave through fwd_chunk_store, rows row_off + lane.
+template <int EPI, int kTileM, int kOutN>
+__device__ __forceinline__ void epilogue_fwd_helper(const GemmArgs& a, const EpiMaps& em, uint32_t buf,
+                                                    uint32_t slot_full, uint32_t slot_empty, uint32_t slot_buf,
+                                                    int c_first, int unit, int units, int total, int row_off,
+                                                    int lane, volatile int* abort_flag, int* err) {
+  const uint32_t src = slot_buf + static_cast<uint32_t>(lane) * 128u, key = static_cast<uint32_t>(lane) & 7u;
+  uint32_t n_slot = 0, nstore = 0;
+  for (int tile = unit; tile < total; tile += units) {
+    int g, mt, nt;
+    decode_tile(tile, a, g, mt, nt);
+    const int row0 = mt * kTileM + row_off;
+    bool aborted = false;
+#pragma unroll 1
+    for (int cc = 32 * c_first; cc < kOutN; cc += 64) {
+      // every chunk passes through the slot, in range or not, so the reader's count stays in step
+      const bool got = mbar_wait(slot_full, n_slot & 1u, abort_flag, err, a.err_site + 8);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        aborted = true;
+        break;
+      }
+      ++n_slot;
+      uint32_t rz[32], ru[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 v = ld_shared_v4(src + ((static_cast<uint32_t>(j) ^ key) << 4));
+        rz[4 * j] = v.x; rz[4 * j + 1] = v.y; rz[4 * j + 2] = v.z; rz[4 * j + 3] = v.w;
+      }
+      mbar_arrive(slot_empty);
+      const int col = nt * kOutN + cc;
+      if (row0 < a.M && col < a.N) fwd_chunk_store<EPI>(a, em, rz, ru, g, row0, col, buf, nstore, lane);
+    }
+    if (aborted) break;
+  }
+  if (lane == 0) bulk_wait_group_all();  // stores done before the staging memory goes away
+  __syncwarp();
 }
 
 // Four fp32 values -> four E4M3 codes (nearest, ties to even, saturating at +-448), the first in the
@@ -725,7 +871,9 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
   constexpr int kBarFinReady = kBarEpiIn + epi_warps<EPI>(), kBarFinDone = kBarFinReady + 8;
   // the peer CTA's producer reports how many ring uses it issued (CTA pair, leader's barrier)
   constexpr int kBarPeerCount = kBarFinDone + 8;
-  static_assert(8 * (kBarPeerCount + 1) <= 512, "barriers overlap the TMEM slot");
+  // activation backward: the helpers' input barriers and the two accumulator slots (full, empty)
+  constexpr int kBarHelperIn = kBarPeerCount + 1, kBarSlotFull = kBarHelperIn + 2, kBarSlotEmpty = kBarSlotFull + 2;
+  static_assert(8 * (kBarSlotEmpty + 2) <= 512, "barriers overlap the TMEM slot");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -759,6 +907,13 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     if constexpr (EPI == EPI_F32_REDUCE)
       for (int i = 0; i < 16; ++i) mbar_init(bar(kBarFinReady + i), 1);
     mbar_init(bar(kBarPeerCount), 1);
+    if constexpr (helper_warps<EPI>() > 0) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(bar(kBarHelperIn + i), 1);
+        mbar_init(bar(kBarSlotFull + i), 32);   // every lane of the reader arrives
+        mbar_init(bar(kBarSlotEmpty + i), 32);  // every lane of the helper arrives
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -950,10 +1105,45 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     const uint32_t staging = stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * 8192u;
     uint32_t nchunk = 0, nfin = 0;
     if constexpr (is_act_bwd(EPI)) {
-      epilogue_act_bwd_tma<EPI, R::kTileM, kOutN>(
-          args, em, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16), bar(kBarTmemFull), bar(kBarTmemEmpty),
-          bar(kBarEpiIn + (warp - 2)), stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * kActBwdWarpBytes,
-          PAIR, unit, units, total, static_cast<int>(rank) * kBM + quarter * 32, lane, abort_flag, err);
+      // warps 2-4: lane quarters 2, 3, 0 in full; warp 5 (quarter 1, beside the MMA issuer) only moves
+      // its accumulator into two slots; helper warps 6 and 7 take the quarter's even and odd chunks
+      const uint32_t ebase = stage0 + S * R::kStageBytes;
+      const uint32_t slots = ebase + 5u * kActBwdWarpBytes;
+      const int q1_row = static_cast<int>(rank) * kBM + 32;
+      if (warp == 5) {
+        epilogue_acc_reader<kOutN>(tmem_base + (1u << (5 + 16)), bar(kBarTmemFull), bar(kBarTmemEmpty),
+                                   bar(kBarSlotFull), bar(kBarSlotEmpty), slots, PAIR, unit, units, total, lane,
+                                   abort_flag, err, args.err_site + 9);
+      } else if (warp < 5) {
+        epilogue_act_bwd_tma<EPI, R::kTileM, kOutN, ACC_TMEM>(
+            args, em, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16), bar(kBarTmemFull), bar(kBarTmemEmpty),
+            bar(kBarEpiIn + (warp - 2)), ebase + static_cast<uint32_t>(warp - 2) * kActBwdWarpBytes, 0u, 0u, 0u, 0, 1,
+            PAIR, unit, units, total, static_cast<int>(rank) * kBM + quarter * 32, lane, abort_flag, err);
+      } else {
+        const int h = warp - 6;
+        epilogue_act_bwd_tma<EPI, R::kTileM, kOutN, ACC_SLOT>(
+            args, em, 0u, 0u, 0u, bar(kBarHelperIn + h), ebase + static_cast<uint32_t>(3 + h) * kActBwdWarpBytes,
+            bar(kBarSlotFull + h), bar(kBarSlotEmpty + h), slots + static_cast<uint32_t>(h) * kAccSlotBytes, h, 2,
+            PAIR, unit, units, total, q1_row, lane, abort_flag, err);
+      }
+    } else if (EPI == EPI_ACT_BF16 && warp >= 5) {
+      // non-gated forward activation: warp 5 moves lane quarter 1's accumulator into the slots and
+      // helper warps 6 and 7 do its even and odd chunks
+      if constexpr (EPI == EPI_ACT_BF16) {
+      const uint32_t ebase = stage0 + S * R::kStageBytes;
+      const uint32_t slots = ebase + 5u * kFwdActWarpBytes;
+      if (warp == 5) {
+        epilogue_acc_reader<kOutN>(tmem_base + (1u << (5 + 16)), bar(kBarTmemFull), bar(kBarTmemEmpty),
+                                   bar(kBarSlotFull), bar(kBarSlotEmpty), slots, PAIR, unit, units, total, lane,
+                                   abort_flag, err, args.err_site + 9);
+      } else {
+        const int h = warp - 6;
+        epilogue_fwd_helper<EPI, R::kTileM, kOutN>(args, em, ebase + static_cast<uint32_t>(3 + h) * kFwdActWarpBytes,
+                                                   bar(kBarSlotFull + h), bar(kBarSlotEmpty + h),
+                                                   slots + static_cast<uint32_t>(h) * kAccSlotBytes, h, unit, units,
+                                                   total, static_cast<int>(rank) * kBM + 32, lane, abort_flag, err);
+      }
+      }
     } else {
       int g, mt, nt;
       for (int it = 0; tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
@@ -977,10 +1167,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
             break;
         }
         else if constexpr (is_act_fwd(EPI))
-          epilogue_fwd_tma<EPI, kHalfOut>(args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
-                                          nt * kOutN + half * kHalfOut,
-                                          stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * kFwdWarpBytes,
-                                          nchunk, lane);
+          epilogue_fwd_tma<EPI, kHalfOut>(
+              args, em, tacc, g, mt * R::kTileM + row_in_tile - lane, nt * kOutN + half * kHalfOut,
+              stage0 + S * R::kStageBytes +
+                  static_cast<uint32_t>(warp - 2) * (EPI == EPI_ACT_BF16 ? kFwdActWarpBytes : kFwdWarpBytes),
+              nchunk, lane);
         else
           epilogue_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
         tc_fence_before();
