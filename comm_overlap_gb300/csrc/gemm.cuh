@@ -55,11 +55,14 @@ constexpr int epi_warps() { return 4; }
 // The fused shard-sum adds four finaliser warps (one per lane quarter) after the epilogue warps.
 template <int EPI>
 constexpr int fin_warps() { return EPI == EPI_F32_REDUCE ? 4 : 0; }
-// The activation backward and the non-gated forward activation add two helper warps (sub-partitions
-// 2 and 3) that do the arithmetic of lane quarter 1 for its reader warp, which shares a
-// sub-partition with the MMA issuer.
+// The activation backward and the non-gated bf16 forward activation add two helper warps
+// (sub-partitions 2 and 3) that do the arithmetic of lane quarter 1 for its reader warp, which shares
+// a sub-partition with the MMA issuer.  (The same split for the E4M3 GeLU epilogue sped up its kernel
+// alone but not the step, where it runs beside the previous chunk's shard-sum; not used there.)
 template <int EPI>
 constexpr int helper_warps() { return (is_act_bwd(EPI) || EPI == EPI_ACT_BF16) ? 2 : 0; }
+// Accumulator slots between the reader and the helpers (4 KiB each, see epilogue_acc_reader).
+constexpr int kAccSlots = 2;
 template <int EPI>
 constexpr int block_threads() { return 64 + 32 * (epi_warps<EPI>() + fin_warps<EPI>() + helper_warps<EPI>()); }
 // Epilogues that move data with TMA stage it in shared memory, per epilogue warp:
@@ -293,20 +296,22 @@ __device__ __forceinline__ void bwd_act_chunk(const uint32_t (&zi)[16], const ui
 // directly, or a shared-memory slot that the quarter's reader warp filled (epilogue_acc_reader).
 enum : int { ACC_TMEM = 0, ACC_SLOT = 1 };
 
-// The accumulator hand-off of one TMEM lane quarter: two 4 KiB slots of 32 rows x 32 fp32 (one
-// 32-column chunk), 128-byte rows with 16-byte piece j of row r at position j ^ (r % 8).
+// The accumulator hand-off of one TMEM lane quarter: 4 KiB slots of 32 rows x 32 fp32 (one 32-column
+// chunk), 128-byte rows with 16-byte piece j of row r at position j ^ (r % 8).  Chunk k of the unit's
+// sequence (8 per tile) goes to slot k % kAccSlots, so the reader runs one chunk ahead of each helper.
 constexpr uint32_t kAccSlotBytes = 4096;
 
 // Reader warp of TMEM lane quarter 1, the quarter read by the warp that shares a sub-partition with
 // the MMA-issuing warp: for every tile of the unit it copies the accumulator, 32 columns at a time,
-// into slot (chunk index % 2), where the helper warp of that slot takes it (epilogue_act_bwd_tma,
-// ACC_SLOT), and hands the accumulator back to the MMA issuer as soon as all its chunks are copied.
+// into the slots, where the helper warp of the chunk (even chunks: helper 0, odd: helper 1) takes it
+// (epilogue_act_bwd_tma with ACC_SLOT, epilogue_fwd_helper, epilogue_f8_helper), and hands the
+// accumulator back to the MMA issuer as soon as all its chunks are copied.
 // The arithmetic of the quarter then runs on other sub-partitions: done by the warp beside the MMA
 // issuer, it delayed the issue of the tensor-core instructions and slowed the main loop (measured).
 // Slot barriers: full (the 32 lanes of the reader arrive) and empty (the 32 lanes of the helper
 // arrive), so every lane's shared-memory accesses are ordered by its own arrive.  False if a bounded
 // wait gave up.
-template <int kOutN>
+template <int kOutN, int kSlots>
 __device__ __forceinline__ void epilogue_acc_reader(uint32_t tmem_q, uint32_t full_bar0, uint32_t empty_addr0,
                                                     uint32_t slot_full0, uint32_t slot_empty0, uint32_t slot_buf0,
                                                     bool pair, int unit, int units, int total, int lane,
@@ -322,7 +327,7 @@ __device__ __forceinline__ void epilogue_acc_reader(uint32_t tmem_q, uint32_t fu
     tc_fence_after();
 #pragma unroll 1
     for (int cc = 0; cc < kOutN; cc += 32, ++k) {
-      const uint32_t slot = k & 1u, sphase = (k >> 1) & 1u;
+      const uint32_t slot = k % kSlots, sphase = (k / kSlots) & 1u;
       uint32_t r[32];
       tmem_ld32(tmem_q + static_cast<uint32_t>(acc * kBN + cc), r);
       const bool free_ok = mbar_wait(slot_empty0 + 8u * slot, sphase ^ 1u, abort_flag, err, site + 1);
@@ -351,7 +356,7 @@ __device__ __forceinline__ void epilogue_acc_reader(uint32_t tmem_q, uint32_t fu
 //  * SRC = ACC_TMEM: the warp reads its own TMEM lane quarter, every chunk of every tile, and hands
 //    each accumulator back after its last chunk;
 //  * SRC = ACC_SLOT: a helper warp for quarter 1 takes chunks c_first, c_first + c_step, ... of every
-//    tile from the reader's slot `slot` (barriers slot_full / slot_empty), never touching TMEM;
+//    tile from the reader's kSlots slots (bases slot_full / slot_empty / slot_buf), never touching TMEM;
 //  * the saved first-linear output of the chunk (Z, or G and U) is loaded into the warp's input
 //    buffer; the next chunk's load is issued as soon as the lanes have read the current one, so it
 //    overlaps the current chunk's accumulator read, arithmetic and stores;
@@ -359,7 +364,7 @@ __device__ __forceinline__ void epilogue_acc_reader(uint32_t tmem_q, uint32_t fu
 //    stored with bulk tensor copies (clipped at the tensor edges).
 // Shared-memory boxes are 32 rows x 64 bytes with 64-byte swizzle: 16-byte chunk j of row r sits at
 // position j ^ ((r >> 1) & 3) of the row.
-template <int EPI, int kTileM, int kOutN, int SRC>
+template <int EPI, int kTileM, int kOutN, int SRC, int kSlots = 2>
 __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const EpiMaps& em, uint32_t tmem_q,
                                                      uint32_t full_bar0, uint32_t empty_addr0, uint32_t in_bar,
                                                      uint32_t buf, uint32_t slot_full, uint32_t slot_empty,
@@ -406,7 +411,7 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
   Cursor pf{unit, c0};
   issue(pf);
   advance(pf);
-  uint32_t in_phase = 0, n_stored = 0, n_slot = 0;
+  uint32_t in_phase = 0, n_stored = 0;
   const uint32_t key = static_cast<uint32_t>(lane) & 7u;
   int it = 0;
   for (int tile = unit; tile < total; tile += units, ++it) {
@@ -427,20 +432,21 @@ __device__ __forceinline__ void epilogue_act_bwd_tma(const GemmArgs& a, const Ep
       if constexpr (SRC == ACC_TMEM) {
         tmem_ld32(tmem_q + static_cast<uint32_t>(acc * kBN + cc), r);
       } else {
-        // every chunk passes through the slot, in range or not, so the reader's count stays in step
-        const bool got = mbar_wait(slot_full, n_slot & 1u, abort_flag, err, a.err_site + 8);
+        // every chunk passes through its slot, in range or not, so the reader's count stays in step
+        const uint32_t k = static_cast<uint32_t>(it) * (kOutN / 32) + static_cast<uint32_t>(cc / 32);
+        const uint32_t slot = k % kSlots;
+        const bool got = mbar_wait(slot_full + 8u * slot, (k / kSlots) & 1u, abort_flag, err, a.err_site + 8);
         if (!__all_sync(0xFFFFFFFFu, got)) {
           aborted = true;
           break;
         }
-        ++n_slot;
-        const uint32_t src = slot_buf + static_cast<uint32_t>(lane) * 128u;
+        const uint32_t src = slot_buf + slot * kAccSlotBytes + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint4 v = ld_shared_v4(src + ((static_cast<uint32_t>(j) ^ key) << 4));
           r[4 * j] = v.x; r[4 * j + 1] = v.y; r[4 * j + 2] = v.z; r[4 * j + 3] = v.w;
         }
-        mbar_arrive(slot_empty);
+        mbar_arrive(slot_empty + 8u * slot);
       }
       uint32_t zi[16], ui[16];
       if (valid) {
@@ -593,36 +599,39 @@ __device__ __forceinline__ void epilogue_fwd_tma(const GemmArgs& a, const EpiMap
 }
 
 // Helper warp of the non-gated forward epilogue for TMEM lane quarter 1 (see epilogue_acc_reader): for
-// every tile of the unit, chunks c_first, c_first + 2, ... of its 256 columns arrive in slot
-// `slot_buf` (barriers slot_full / slot_empty) and leave through fwd_chunk_store, rows row_off + lane.
-template <int EPI, int kTileM, int kOutN>
+// every tile of the unit, chunks c_first, c_first + 2, ... of its 256 columns arrive in the reader's
+// kSlots slots (bases slot_full / slot_empty / slot_buf) and leave through fwd_chunk_store, rows
+// row_off + lane.
+template <int EPI, int kTileM, int kOutN, int kSlots>
 __device__ __forceinline__ void epilogue_fwd_helper(const GemmArgs& a, const EpiMaps& em, uint32_t buf,
                                                     uint32_t slot_full, uint32_t slot_empty, uint32_t slot_buf,
                                                     int c_first, int unit, int units, int total, int row_off,
                                                     int lane, volatile int* abort_flag, int* err) {
   const uint32_t src = slot_buf + static_cast<uint32_t>(lane) * 128u, key = static_cast<uint32_t>(lane) & 7u;
-  uint32_t n_slot = 0, nstore = 0;
-  for (int tile = unit; tile < total; tile += units) {
+  uint32_t nstore = 0;
+  int it = 0;
+  for (int tile = unit; tile < total; tile += units, ++it) {
     int g, mt, nt;
     decode_tile(tile, a, g, mt, nt);
     const int row0 = mt * kTileM + row_off;
     bool aborted = false;
 #pragma unroll 1
     for (int cc = 32 * c_first; cc < kOutN; cc += 64) {
-      // every chunk passes through the slot, in range or not, so the reader's count stays in step
-      const bool got = mbar_wait(slot_full, n_slot & 1u, abort_flag, err, a.err_site + 8);
+      // every chunk passes through its slot, in range or not, so the reader's count stays in step
+      const uint32_t k = static_cast<uint32_t>(it) * (kOutN / 32) + static_cast<uint32_t>(cc / 32);
+      const uint32_t slot = k % kSlots;
+      const bool got = mbar_wait(slot_full + 8u * slot, (k / kSlots) & 1u, abort_flag, err, a.err_site + 8);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         aborted = true;
         break;
       }
-      ++n_slot;
       uint32_t rz[32], ru[32];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint4 v = ld_shared_v4(src + ((static_cast<uint32_t>(j) ^ key) << 4));
+        const uint4 v = ld_shared_v4(src + slot * kAccSlotBytes + ((static_cast<uint32_t>(j) ^ key) << 4));
         rz[4 * j] = v.x; rz[4 * j + 1] = v.y; rz[4 * j + 2] = v.z; rz[4 * j + 3] = v.w;
       }
-      mbar_arrive(slot_empty);
+      mbar_arrive(slot_empty + 8u * slot);
       const int col = nt * kOutN + cc;
       if (row0 < a.M && col < a.N) fwd_chunk_store<EPI>(a, em, rz, ru, g, row0, col, buf, nstore, lane);
     }
@@ -871,9 +880,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
   constexpr int kBarFinReady = kBarEpiIn + epi_warps<EPI>(), kBarFinDone = kBarFinReady + 8;
   // the peer CTA's producer reports how many ring uses it issued (CTA pair, leader's barrier)
   constexpr int kBarPeerCount = kBarFinDone + 8;
-  // activation backward: the helpers' input barriers and the two accumulator slots (full, empty)
-  constexpr int kBarHelperIn = kBarPeerCount + 1, kBarSlotFull = kBarHelperIn + 2, kBarSlotEmpty = kBarSlotFull + 2;
-  static_assert(8 * (kBarSlotEmpty + 2) <= 512, "barriers overlap the TMEM slot");
+  // helper warps: their input barriers and the accumulator slots of lane quarter 1 (full, empty)
+  constexpr int kSlots = kAccSlots;
+  constexpr int kBarHelperIn = kBarPeerCount + 1, kBarSlotFull = kBarHelperIn + 2,
+                kBarSlotEmpty = kBarSlotFull + kSlots;
+  static_assert(8 * (kBarSlotEmpty + kSlots) <= 512, "barriers overlap the TMEM slot");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -908,8 +919,8 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       for (int i = 0; i < 16; ++i) mbar_init(bar(kBarFinReady + i), 1);
     mbar_init(bar(kBarPeerCount), 1);
     if constexpr (helper_warps<EPI>() > 0) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(bar(kBarHelperIn + i), 1);
+      for (int i = 0; i < 2; ++i) mbar_init(bar(kBarHelperIn + i), 1);
+      for (int i = 0; i < kSlots; ++i) {
         mbar_init(bar(kBarSlotFull + i), 32);   // every lane of the reader arrives
         mbar_init(bar(kBarSlotEmpty + i), 32);  // every lane of the helper arrives
       }
@@ -1111,9 +1122,9 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       const uint32_t slots = ebase + 5u * kActBwdWarpBytes;
       const int q1_row = static_cast<int>(rank) * kBM + 32;
       if (warp == 5) {
-        epilogue_acc_reader<kOutN>(tmem_base + (1u << (5 + 16)), bar(kBarTmemFull), bar(kBarTmemEmpty),
-                                   bar(kBarSlotFull), bar(kBarSlotEmpty), slots, PAIR, unit, units, total, lane,
-                                   abort_flag, err, args.err_site + 9);
+        epilogue_acc_reader<kOutN, kSlots>(tmem_base + (1u << (5 + 16)), bar(kBarTmemFull), bar(kBarTmemEmpty),
+                                           bar(kBarSlotFull), bar(kBarSlotEmpty), slots, PAIR, unit, units, total,
+                                           lane, abort_flag, err, args.err_site + 9);
       } else if (warp < 5) {
         epilogue_act_bwd_tma<EPI, R::kTileM, kOutN, ACC_TMEM>(
             args, em, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16), bar(kBarTmemFull), bar(kBarTmemEmpty),
@@ -1121,10 +1132,10 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
             PAIR, unit, units, total, static_cast<int>(rank) * kBM + quarter * 32, lane, abort_flag, err);
       } else {
         const int h = warp - 6;
-        epilogue_act_bwd_tma<EPI, R::kTileM, kOutN, ACC_SLOT>(
+        epilogue_act_bwd_tma<EPI, R::kTileM, kOutN, ACC_SLOT, kSlots>(
             args, em, 0u, 0u, 0u, bar(kBarHelperIn + h), ebase + static_cast<uint32_t>(3 + h) * kActBwdWarpBytes,
-            bar(kBarSlotFull + h), bar(kBarSlotEmpty + h), slots + static_cast<uint32_t>(h) * kAccSlotBytes, h, 2,
-            PAIR, unit, units, total, q1_row, lane, abort_flag, err);
+            bar(kBarSlotFull), bar(kBarSlotEmpty), slots, h, 2, PAIR, unit, units, total, q1_row, lane, abort_flag,
+            err);
       }
     } else if (EPI == EPI_ACT_BF16 && warp >= 5) {
       // non-gated forward activation: warp 5 moves lane quarter 1's accumulator into the slots and
@@ -1133,15 +1144,14 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       const uint32_t ebase = stage0 + S * R::kStageBytes;
       const uint32_t slots = ebase + 5u * kFwdActWarpBytes;
       if (warp == 5) {
-        epilogue_acc_reader<kOutN>(tmem_base + (1u << (5 + 16)), bar(kBarTmemFull), bar(kBarTmemEmpty),
-                                   bar(kBarSlotFull), bar(kBarSlotEmpty), slots, PAIR, unit, units, total, lane,
-                                   abort_flag, err, args.err_site + 9);
+        epilogue_acc_reader<kOutN, kSlots>(tmem_base + (1u << (5 + 16)), bar(kBarTmemFull), bar(kBarTmemEmpty),
+                                           bar(kBarSlotFull), bar(kBarSlotEmpty), slots, PAIR, unit, units, total,
+                                           lane, abort_flag, err, args.err_site + 9);
       } else {
         const int h = warp - 6;
-        epilogue_fwd_helper<EPI, R::kTileM, kOutN>(args, em, ebase + static_cast<uint32_t>(3 + h) * kFwdActWarpBytes,
-                                                   bar(kBarSlotFull + h), bar(kBarSlotEmpty + h),
-                                                   slots + static_cast<uint32_t>(h) * kAccSlotBytes, h, unit, units,
-                                                   total, static_cast<int>(rank) * kBM + 32, lane, abort_flag, err);
+        epilogue_fwd_helper<EPI, R::kTileM, kOutN, kSlots>(
+            args, em, ebase + static_cast<uint32_t>(3 + h) * kFwdActWarpBytes, bar(kBarSlotFull), bar(kBarSlotEmpty),
+            slots, h, unit, units, total, static_cast<int>(rank) * kBM + 32, lane, abort_flag, err);
       }
       }
     } else {
