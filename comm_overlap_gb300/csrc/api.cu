@@ -585,6 +585,7 @@ domino_status mlp_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, Sl
     const int variant = P.gated ? dm::GV_FWD_GLU : dm::GV_FWD_ACT;
     GemmArgs a = gemm_args(variant, P.gated ? P.t : 1, P.m, P.gated ? P.Fi : P.F, P.h, site);
     a.act = P.act;
+    a.cross_batch = 1;  // the shards share X: walk every shard's N-tiles per group of M-tiles
     a.out0 = Hbuf;
     a.ld0 = P.F;
     a.bs0 = P.gated ? P.Fi : 0;
@@ -703,6 +704,7 @@ domino_status mlp_chunk_bwd(domino_handle H, const Plan& P, const Streams& S, Sl
     GemmArgs a = gemm_args(variant, P.t, P.m, P.Fi, P.h, 3);
     a.act = P.act;
     a.b_bmul = 1;
+    a.cross_batch = 1;  // the shards share gY
     a.in0 = save_c;
     a.ldi = P.a_rows;
     a.bsi = P.Ri;
@@ -730,6 +732,7 @@ domino_status mlp_chunk_bwd(domino_handle H, const Plan& P, const Streams& S, Sl
   {
     GemmArgs a = gemm_args(dm::GV_WGRAD, P.t, P.h, P.Fi, P.m, 4);
     a.b_bmul = 1;
+    a.cross_batch = 1;  // the shards share gY
     a.out0 = gB;
     a.ld0 = P.Fi;
     a.bs0 = P.h * P.Fi;

@@ -92,6 +92,9 @@ constexpr int smem_bytes() {
 }
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kGroupM = 8;  // tiles are visited in groups of 8 M-tiles for L2 reuse of B tiles
+// With cross_batch, groups of 16 M-tiles walk the N-tiles of every batch: an A operand shared by the
+// batches (the first linear's X) is then read once per launch instead of once per batch.
+constexpr int kGroupMCross = 16;
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;
 // How long the leader's producer waits for its peer's count of issued stages: longer than any single
 // bounded wait, so the peer has left its loop by then unless its GPU stopped making progress.
@@ -99,6 +102,19 @@ constexpr uint64_t kPeerCountTimeoutNs = 4000000000ull;
 constexpr uint64_t kPeerCopyGraceNs = 100000ull;  // last resort when the peer's count never came
 
 __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, int& g, int& mt, int& nt) {
+  if (a.cross_batch) {
+    const int ncomb = a.batches * a.n_tiles;  // (batch, N-tile) pairs, batch-major
+    const int span = kGroupMCross * ncomb;
+    const int grp = tile / span;
+    const int first_m = grp * kGroupMCross;
+    const int gsize = min(a.m_tiles - first_m, kGroupMCross);
+    const int in = tile - grp * span;
+    mt = first_m + in % gsize;
+    const int nb = in / gsize;
+    g = nb / a.n_tiles;
+    nt = nb - g * a.n_tiles;
+    return;
+  }
   const int per_batch = a.m_tiles * a.n_tiles;
   g = tile / per_batch;
   const int r = tile - g * per_batch;

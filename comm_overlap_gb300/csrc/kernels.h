@@ -68,6 +68,7 @@ struct GemmArgs {
   int32_t b_row_off, b_bmul;
   int32_t act;
   int32_t err_site;
+  int32_t cross_batch;  // tile order: 0 = batch after batch; 1 = the batches side by side along N (below)
   float alpha;      // FP8 variants: scale of the accumulator (product of the operand scales)
   float out_scale;  // EPI_ACT_F8 / EPI_GLU_F8: factor applied before the E4M3 rounding (1 / sh)
   void* out0;
