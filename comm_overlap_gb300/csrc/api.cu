@@ -623,6 +623,7 @@ domino_status mlp_chunk_fwd_fp8(domino_handle H, const Plan& P, const Streams& S
     const int variant = P.gated ? dm::GV_F8_FWD_GLU : dm::GV_F8_FWD_ACT;
     GemmArgs a = gemm_args(variant, P.gated ? P.t : 1, P.m, P.gated ? P.Fi : P.F, P.h, 10);
     a.act = P.act;
+    a.cross_batch = 1;  // the shards share X8
     a.out0 = H8;
     a.ld0 = P.F;
     a.bs0 = P.gated ? P.Fi : 0;
@@ -881,6 +882,7 @@ domino_status attn_chunk_fwd(domino_handle H, const Plan& P, const Streams& S, S
   {
     GemmArgs a = gemm_args(dm::GV_FWD_ACT, 1, P.m, 3 * P.h, P.h, 7);
     a.act = DOMINO_ACT_NONE;
+    a.cross_batch = 1;  // groups of 16 M-tiles, as for the MLP's first linear
     a.out0 = QKV;
     a.ld0 = 3 * P.h;
     dm::EpiMaps em = {};
