@@ -11,7 +11,7 @@ import pytest
 import oracle
 from comm_overlap_gb300 import domino as dm
 from comm_overlap_gb300 import synth
-from gpu_helpers import assert_tol, bf16_round, host_bits, host_f64
+from gpu_helpers import assert_tol, bf16_round, edge_rows, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -124,7 +124,8 @@ def test_fp8_validation(handle):
 @pytest.mark.parametrize("workload", ["llama2_7b_swiglu", "gpt3_2.7b_mlp"])
 def test_fp8_full_size_sampled(handle, workload):
     """The FP8 forward at the full size the bench times (its inputs and scales), fused schedule:
-    sampled rows against the oracle, and bit-identical to the two-stream schedule."""
+    rows at every row-chunk and tile edge plus a few at random against the oracle, and bit-identical
+    to the two-stream schedule."""
     import torch
 
     import bench
@@ -134,6 +135,6 @@ def test_fp8_full_size_sampled(handle, workload):
     Yf = run_fp8(handle, X8, A8, B8, s.t, s.act, sc, s.p, s.q, dm.SCHED_FUSED)
     Yi = run_fp8(handle, X8, A8, B8, s.t, s.act, sc, s.p, s.q, dm.SCHED_INTRA)
     assert np.array_equal(host_bits(Yf), host_bits(Yi))
-    rows = synth.sample_indices(s.M, 6, 73)
+    rows = edge_rows(s.M, s.M // s.p, 73, n_random=6)   # every chunk and tile edge, and 6 at random
     ref = oracle.mlp_fwd_fp8(X8, A8, B8, s.t, s.act, sc, rows=rows)
     assert_tol(host_f64(Yf[torch.from_numpy(rows).cuda()]), ref, "FP8 forward, sampled rows")

@@ -12,39 +12,9 @@ import pytest
 import oracle
 from comm_overlap_gb300 import domino as dm
 from comm_overlap_gb300 import synth
-from gpu_helpers import Lib, assert_tol, dev_bf16, host_bits, host_f64
+from gpu_helpers import Lib, assert_tol, dev_bf16, edge_feats, edge_rows, host_bits, host_f64
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
-
-N_ROWS = 12
-N_FEATS = 6
-TILE_M = 256   # output rows of one GEMM tile (a CTA pair's 2 x 128)
-TILE_N = 256   # output columns of one GEMM tile
-
-
-def edge_rows(M: int, m: int, seed: int, n_random: int = N_ROWS) -> np.ndarray:
-    """Rows where a row-indexing mistake would show: both sides of every row-chunk boundary (m - 1,
-    m, ...), of the first tile boundaries inside a chunk (127/128 inside a CTA's half, 255/256
-    between tiles) and of the chunk's last tile (m - 256 .. m - 1, the last round of the persistent
-    grid), plus `n_random` rows drawn at random (0 and M - 1 always among them)."""
-    rows = set(synth.sample_indices(M, n_random, seed).tolist())
-    for c0 in range(0, M, m):
-        for off in (0, 1, 127, 128, TILE_M - 1, TILE_M, m - TILE_M - 1, m - TILE_M, m - 129, m - 128, m - 1):
-            if 0 <= off < m:
-                rows.add(c0 + off)
-    return np.array(sorted(rows), dtype=np.int64)
-
-
-def edge_feats(Fi: int, t: int, seed: int, n_random: int = N_FEATS) -> np.ndarray:
-    """ffn features to check in the weight gradients: the first and last feature of every shard and
-    both sides of the shard's first tile boundary (TILE_N - 1, TILE_N), plus `n_random` at random."""
-    feats = set(synth.sample_indices(Fi * t, n_random, seed).tolist())
-    for i in range(t):
-        for j in (0, TILE_N - 1, TILE_N, Fi - 1):
-            if 0 <= j < Fi:
-                feats.add(i * Fi + j)
-    return np.array(sorted(feats), dtype=np.int64)
-
 
 @pytest.fixture(scope="module")
 def lib():

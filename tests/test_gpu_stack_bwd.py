@@ -6,7 +6,7 @@ import pytest
 import oracle
 from comm_overlap_gb300 import domino as dm
 from comm_overlap_gb300 import synth
-from gpu_helpers import assert_tol, dev_bf16, host_bits, host_f64
+from gpu_helpers import assert_tol, dev_bf16, edge_rows, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +75,6 @@ def test_stack_backward_full_size(handle):
     s = dataclasses.replace(base, backward=True)
     d = synth.make_inputs(s, seed=0)
     out, gZin, _, _ = run_stack_train(handle, s, d)
-    rows = synth.sample_indices(s.M, 6, 43)
+    rows = edge_rows(s.M, s.M // s.p, 43, n_random=6)   # every chunk and tile edge, and 6 at random
     gZ0, _, _ = oracle.stack_bwd(d["X"], d["A"], d["B"], d["gY"], s.t, s.act, 1e-5, rows=rows)
     assert_tol(host_f64(gZin[torch.from_numpy(rows).cuda()]), gZ0, "stack input gradient, sampled rows")
