@@ -57,6 +57,40 @@ enum : int {
   B_P_FULL = 14, B_PV_DONE = 16, B_O_FREE = 18, B_DRAIN = 20, B_COUNT = 21
 };
 
+// Two-lane fp32 arithmetic (sm_100 and later): each lane is an ordinary fp32 operation with round to
+// nearest, so a pair computes exactly what two scalar operations would, in half the issue slots.  The
+// softmax warps share their sub-partitions with the MMA issuer and the TMA producer; the fewer
+// instructions they issue, the sooner the issuer's tensor-core instructions go out.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// the largest of three (no NaN reaches it: scores are finite or -inf)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void attn_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -311,7 +345,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+          for (int c = 0; c < 128; c += 2)
+            m8[(c >> 1) & 7] = max3(m8[(c >> 1) & 7], __uint_as_float(sr[c >> 5][c & 31]),
+                                    __uint_as_float(sr[c >> 5][(c & 31) + 1]));
 #pragma unroll
           for (int k = 4; k > 0; k >>= 1)
 #pragma unroll
@@ -327,19 +363,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float nmx = -mx;
           // p = 2^(s scale - max), summed in fp32 and rounded to bf16 pairs as it is produced, so
           // that only the 64 packed registers stay live across the wait below
-          float l8[8];
+          // (columns 2c, 2c + 1 as one pair: l8[k] sums the columns e with e % 8 = k, as four pairs)
+          uint64_t l4[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) l8[k] = 0.0f;
+          for (int k = 0; k < 4; ++k) l4[k] = f2(0.0f, 0.0f);
+          const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nmx2 = f2(nmx, nmx);
           uint32_t pk[2][32];
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const int e = 2 * c;
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[e >> 5][e & 31]), a.scale_log2, nmx));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]), a.scale_log2, nmx));
-            l8[e & 7] += p0;
-            l8[(e + 1) & 7] += p1;
+            float y0, y1;
+            f2_split(fma_f2(f2(__uint_as_float(sr[e >> 5][e & 31]), __uint_as_float(sr[e >> 5][(e & 31) + 1])), sc2,
+                            nmx2),
+                     y0, y1);
+            const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+            l4[c & 3] = add_f2(l4[c & 3], f2(p0, p1));
             pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
           }
+          float l8[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) f2_split(l4[k], l8[2 * k], l8[2 * k + 1]);
 #pragma unroll
           for (int k = 4; k > 0; k >>= 1)
 #pragma unroll
@@ -364,8 +407,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               uint32_t o[32];
               tmem_ld32(tO + static_cast<uint32_t>(c * 32), o);
               tmem_ld_wait();
+              const uint64_t al2 = f2(alpha, alpha);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              for (int e = 0; e < 32; e += 2) {
+                float v0, v1;
+                f2_split(mul_f2(f2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), al2), v0, v1);
+                o[e] = __float_as_uint(v0);
+                o[e + 1] = __float_as_uint(v1);
+              }
               tmem_st32(tO + static_cast<uint32_t>(c * 32), o);
             }
           }
