@@ -16,9 +16,15 @@
 // Warp roles:
 //   warp 0 (one lane)  TMA producer: each item's Q tiles, then its K and V tiles into two-deep rings
 //                      (the rings run on across items).
-//   warp 1 (one lane)  MMA issuer, per block j and tile x: O_x += P_x V_j as soon as the softmax
-//                      handed P_x over, then S_x = Q_x K_{j+1}^T (in that order: P_x lives in the
-//                      columns of S_x, and tensor-core operations of one thread run in order).
+//   warps 1, 10        MMA issuers of tile 0 and tile 1 (one lane each), per block j: O_x += P_x V_j
+//   (one lane each)    as soon as the softmax handed P_x over, then S_x = Q_x K_{j+1}^T (in that
+//                      order: P_x lives in the columns of S_x, and the tensor-core operations of
+//                      one thread complete in order).  Issuing a 128 x 128 x 16 product takes a
+//                      thread about as long as the tensor core takes to execute it, so a single
+//                      issuer leaves the tensor core idle while it waits and commits.  The two issuers
+//                      take turns (B_TURN) in the order one issuer would use -- per block tile 0's
+//                      products, then tile 1's, so that neither tile's products are spread out by the
+//                      other's -- and each waits for its data before its turn and commits after it.
 //   warps 2-5, 6-9     softmax of tile 0 and tile 1, one query row per thread (TMEM lane quarter =
 //                      warp % 4): scores from TMEM, running max / sum in fp32, O_x rescaled in TMEM
 //                      when a row maximum grew, P rounded to bf16 and stored into TMEM; at the end
@@ -44,18 +50,21 @@ constexpr int kAttnBlk = 128;                       // query rows / key-value po
 constexpr uint32_t kTile = kAttnBlk * kAttnD * 2;   // 32 KiB: one Q, K or V tile
 constexpr uint32_t kHalf = kTile / 2;               // one 64-column (128-byte) swizzle panel
 constexpr uint32_t kOBox = 32 * 64 * 2;             // 4 KiB: one warp's 32 rows x 64 columns of O
-constexpr int kAttnThreads = 320;
+constexpr int kAttnThreads = 352;
+constexpr int kAttnIssuer1 = 10;  // the warp that issues tile 1's products (tile 0's: warp 1)
 // alignment slack, control, Q[2], K[2], V[2], one O staging box per softmax warp
 constexpr int kAttnSmem = 1024 + 1024 + 6 * static_cast<int>(kTile) + 8 * static_cast<int>(kOBox);
 static_assert(kAttnSmem <= 232448, "shared memory beyond the per-CTA limit");
 constexpr uint32_t kAttnTmemCols = 512;
 constexpr uint64_t kAttnDrainNs = 200000000ull;
 
-// barrier indices (pairs are per tile or per ring slot)
+// barrier indices: pairs are per tile or per ring slot; the ring slots' releases are per tile and
+// slot (B_K_EMPTY + 2 x + slot), since the two issuers' products complete independently
 enum : int {
-  B_Q_FULL = 0, B_Q_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 6, B_V_FULL = 8, B_V_EMPTY = 10, B_S_FULL = 12,
-  B_P_FULL = 14, B_PV_DONE = 16, B_O_FREE = 18, B_DRAIN = 20, B_COUNT = 21
+  B_Q_FULL = 0, B_Q_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 6, B_V_FULL = 10, B_V_EMPTY = 12, B_S_FULL = 16,
+  B_P_FULL = 18, B_PV_DONE = 20, B_O_FREE = 22, B_DRAIN = 24, B_TURN = 26, B_COUNT = 28
 };
+static_assert(8 * B_COUNT <= 512, "barriers overlap the TMEM slot");
 
 // Two-lane fp32 arithmetic (sm_100 and later): each lane is an ordinary fp32 operation with round to
 // nearest, so a pair computes exactly what two scalar operations would, in half the issue slots.  The
@@ -172,6 +181,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // ---------------- TMA producer
       uint32_t gb = 0;          // ring position of the item's key block 0
       int nq[2] = {0, 0};       // items so far in which tile x took part
+      // ring slot b's current block: bit 2 b + x set if tile x consumes it (cons); parity of the
+      // blocks of slot b that tile x consumed so far (upar), i.e. of the releases it will have made
+      uint32_t cons = 0, upar = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < w.units && ok; u += gridDim.x) {
         const int nit = attn_unit_items(w, u);
@@ -195,22 +207,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int j = 0; j < it.nblk && ok; ++j) {
             const uint32_t r = gb + static_cast<uint32_t>(j);
             const int b = static_cast<int>(r & 1u);
-            const uint32_t use = (r >> 1) & 1u;
             const int pos = j * kAttnBlk;
-            if (!mbar_wait(bar(B_K_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 1)) {
-              ok = false;
-              break;
-            }
+            // the slot is refilled once every tile that consumed its previous block has released it
+            for (int x = 0; x < 2 && ok; ++x)
+              if ((cons >> (2 * b + x)) & 1u)
+                ok = mbar_wait(bar(B_K_EMPTY + 2 * x + b), ((upar >> (2 * b + x)) & 1u) ^ 1u, abort_flag, err,
+                               a.err_site + 1);
+            if (!ok) break;
             mbar_arrive_expect_tx(bar(B_K_FULL + b), kTile);
             tma_load_4d(sK + b * kTile, &tmQKV, bar(B_K_FULL + b), 0, slot_k, pos, it.sq);
             tma_load_4d(sK + b * kTile + kHalf, &tmQKV, bar(B_K_FULL + b), 64, slot_k, pos, it.sq);
-            if (!mbar_wait(bar(B_V_EMPTY + b), use ^ 1u, abort_flag, err, a.err_site + 2)) {
-              ok = false;
-              break;
-            }
+            for (int x = 0; x < 2 && ok; ++x)
+              if ((cons >> (2 * b + x)) & 1u)
+                ok = mbar_wait(bar(B_V_EMPTY + 2 * x + b), ((upar >> (2 * b + x)) & 1u) ^ 1u, abort_flag, err,
+                               a.err_site + 2);
+            if (!ok) break;
             mbar_arrive_expect_tx(bar(B_V_FULL + b), kTile);
             tma_load_4d(sV + b * kTile, &tmQKV, bar(B_V_FULL + b), 0, slot_v, pos, it.sq);
             tma_load_4d(sV + b * kTile + kHalf, &tmQKV, bar(B_V_FULL + b), 64, slot_v, pos, it.sq);
+            // tile 0 consumes key blocks 0 .. q0, tile 1 (if any) every block of the item
+            const uint32_t users = (j <= it.q0 ? 1u : 0u) | (it.ntiles == 2 ? 2u : 0u);
+            cons = (cons & ~(3u << (2 * b))) | (users << (2 * b));
+            upar ^= users << (2 * b);
           }
           gb += static_cast<uint32_t>(it.nblk);
         }
@@ -223,85 +241,115 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kAttnIssuer1) {
     if (lane == 0) {
-      // ---------------- MMA issuer
+      // ---------------- MMA issuer of tile x
+      const uint32_t x = warp == 1 ? 0u : 1u;
       constexpr uint32_t kIdQK = idesc_bf16_f32(kAttnBlk, kAttnBlk, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(kAttnBlk, kAttnD, false, true);
       // Shared-memory descriptors are built once; a K step adds its byte offset / 16 to the start
       // address field (bits 0-13: shared addresses below 256 KiB never carry out of it).
-      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dK0 = sdesc_sw128(sK, 16, 1024),
+      const uint64_t dQ = sdesc_sw128(sQ + x * kTile, 16, 1024), dK0 = sdesc_sw128(sK, 16, 1024),
                      dV0 = sdesc_sw128(sV, kHalf, 1024);
-      uint32_t gb = 0;
-      int nq[2] = {0, 0};
-      uint32_t cbm[2] = {0u, 0u};  // key blocks of tile x handed over so far (phase of P_FULL)
+      const uint32_t tS = tmem_base + 128u * x, tO = tmem_base + 256u + 128u * x;
+      // S_x = Q_x K^T (K in ring slot kb) into TMEM columns 128 x
+      auto qk = [=](uint32_t kb) {
+        const uint64_t dk = dK0 + ((static_cast<uint64_t>(kb) * kTile) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kAttnD / 16; ++kk) {
+          const uint64_t off = (static_cast<uint64_t>(kk >> 2) * kHalf + static_cast<uint64_t>(kk & 3) * 32u) >> 4;
+          umma_bf16(tS, dQ + off, dk + off, kIdQK, static_cast<uint32_t>(kk != 0));
+        }
+      };
+      // O_x (+)= P_x V (V in ring slot vb); A = P_x from TMEM (8 columns of bf16 pairs per K step of
+      // 16); B = V, MN-major: its two 64-column panels of d sit kHalf apart, 8-row groups of positions
+      // 1024 bytes apart
+      auto pv = [=](uint32_t vb, bool first) {
+        const uint64_t dv = dV0 + ((static_cast<uint64_t>(vb) * kTile) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kAttnBlk / 16; ++kk)
+          umma_bf16_tmem_a(tO, tS + 8u * kk, dv + ((static_cast<uint64_t>(kk) * 2048u) >> 4), kIdPV,
+                           static_cast<uint32_t>(!first || kk != 0));
+      };
+      uint32_t gb = 0;  // ring position of the item's key block 0
+      // bit 0: parity of the items so far in which tile x took part; bit 1: there was one;
+      // bit 2: parity of the key blocks handed over so far (phase of P_FULL); bit 3: parity of the
+      // turns received (phase of B_TURN + x)
+      uint32_t st = 0;
+      int prev_nt = 0;  // tiles of the previous item
       bool ok = true;
+      // this issuer's turn: wait for the other issuer to hand it over
+      auto take_turn = [&](bool needed) -> bool {
+        if (!needed) return true;
+        if (!mbar_wait(bar(B_TURN + x), (st >> 3) & 1u, abort_flag, err, a.err_site + 13)) return false;
+        st ^= 8u;
+        return true;
+      };
       for (int u = blockIdx.x; u < w.units && ok; u += gridDim.x) {
         const int nit = attn_unit_items(w, u);
         for (int half = 0; half < nit && ok; ++half) {
           const AttnItem it = attn_item(a, w, u, half);
-          const int last_tile = it.ntiles - 1;  // the tile with the most blocks: the last user of K_j, V_j
-          // S_x = Q_x K_j^T into TMEM columns 128 x; after tile x's last one its Q buffer is free
-          auto issue_qk = [&](int x, int j) -> bool {
-            const uint32_t r = gb + static_cast<uint32_t>(j);
-            const int b = static_cast<int>(r & 1u);
-            if (!mbar_wait(bar(B_K_FULL + b), (r >> 1) & 1u, abort_flag, err, a.err_site + 3)) return false;
-            tc_fence_after();
-            const uint64_t dq = dQ0 + ((static_cast<uint64_t>(x) * kTile) >> 4),
-                           dk = dK0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kAttnD / 16; ++kk) {
-              const uint64_t off = (static_cast<uint64_t>(kk >> 2) * kHalf + static_cast<uint64_t>(kk & 3) * 32u) >> 4;
-              umma_bf16(tmem_base + 128u * x, dq + off, dk + off, kIdQK, static_cast<uint32_t>(kk != 0));
+          const int nt = it.ntiles;
+          if (static_cast<int>(x) >= nt) {  // a last query block of its own: tile 0 only
+            gb += static_cast<uint32_t>(it.nblk);
+            prev_nt = nt;
+            continue;
+          }
+          const int q0 = it.q0, qlast = q0 + static_cast<int>(x);  // tile x attends to key blocks 0 .. qlast
+          // the item's first product S_x = Q_x K_0^T; tile 0 after the previous item's last products
+          // (tile 1's if it had two tiles), tile 1 after tile 0's first product
+          if (!mbar_wait(bar(B_Q_FULL + x), st & 1u, abort_flag, err, a.err_site + 5) ||
+              !mbar_wait(bar(B_K_FULL + (gb & 1u)), (gb >> 1) & 1u, abort_flag, err, a.err_site + 3) ||
+              !take_turn(x == 0 ? prev_nt == 2 : true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          qk(gb & 1u);
+          if (nt == 2) mbar_arrive(bar(B_TURN + (x ^ 1u)));
+          umma_commit(bar(B_S_FULL + x));
+          umma_commit(bar(B_K_EMPTY + 2 * x + (gb & 1u)));
+          if (qlast == 0) umma_commit(bar(B_Q_EMPTY + x));
+          for (int j = 0; j <= qlast && ok; ++j) {
+            const uint32_t r = gb + static_cast<uint32_t>(j), r1 = r + 1u;
+            // the waits that are usually over first, the softmax hand-off (the critical path) last
+            if (!mbar_wait(bar(B_V_FULL + (r & 1u)), (r >> 1) & 1u, abort_flag, err, a.err_site + 7) ||
+                (j < qlast &&
+                 !mbar_wait(bar(B_K_FULL + (r1 & 1u)), (r1 >> 1) & 1u, abort_flag, err, a.err_site + 3)) ||
+                // O_x is overwritten by the item's first product: the previous item's O_x must be read
+                (j == 0 && (st & 2u) &&
+                 !mbar_wait(bar(B_O_FREE + x), (st & 1u) ^ 1u, abort_flag, err, a.err_site + 12)) ||
+                // tile 0 takes its turn in every block of a two-tile item, tile 1 in every block but
+                // its last (which follows its own products of block q0)
+                !take_turn(nt == 2 && (x == 0 || j <= q0)) ||
+                // P_FULL completes once per key block the tile processes, in this order
+                !mbar_wait(bar(B_P_FULL + x), (st >> 2) & 1u, abort_flag, err, a.err_site + 6)) {
+              ok = false;
+              break;
             }
-            umma_commit(bar(B_S_FULL + x));
-            if (x == last_tile) umma_commit(bar(B_K_EMPTY + b));
-            if (j == it.q0 + x) umma_commit(bar(B_Q_EMPTY + x));
-            return true;
-          };
-          for (int x = 0; x < it.ntiles && ok; ++x)
-            ok = mbar_wait(bar(B_Q_FULL + x), static_cast<uint32_t>(nq[x]) & 1u, abort_flag, err, a.err_site + 5) &&
-                 issue_qk(x, 0);
-          for (int j = 0; j < it.nblk && ok; ++j) {
-            const uint32_t r = gb + static_cast<uint32_t>(j);
-            const int b = static_cast<int>(r & 1u);
-            for (int x = 0; x < it.ntiles && ok; ++x) {
-              if (j > it.q0 + x) continue;  // tile x is done
-              // P_FULL of tile x completes once per key block the tile processes, in this order
-              if (!mbar_wait(bar(B_P_FULL + x), cbm[x] & 1u, abort_flag, err, a.err_site + 6) ||
-                  !mbar_wait(bar(B_V_FULL + b), (r >> 1) & 1u, abort_flag, err, a.err_site + 7)) {
-                ok = false;
-                break;
-              }
-              // O_x is overwritten by the item's first product: the previous item's O_x must be read
-              if (j == 0 && nq[x] > 0 &&
-                  !mbar_wait(bar(B_O_FREE + x), static_cast<uint32_t>(nq[x] - 1) & 1u, abort_flag, err,
-                             a.err_site + 12)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint64_t dv = dV0 + ((static_cast<uint64_t>(b) * kTile) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < kAttnBlk / 16; ++kk)
-                // A = P_x from TMEM (8 columns of bf16 pairs per K step of 16); B = V_j, MN-major: its
-                // two 64-column panels of d sit kHalf apart, 8-row groups of positions 1024 bytes apart
-                umma_bf16_tmem_a(tmem_base + 256u + 128u * x, tmem_base + 128u * x + 8u * kk,
-                                 dv + ((static_cast<uint64_t>(kk) * 2048u) >> 4), kIdPV,
-                                 static_cast<uint32_t>((j | kk) != 0));
-              umma_commit(bar(B_PV_DONE + x));
-              if (x == last_tile) umma_commit(bar(B_V_EMPTY + b));
-              ++cbm[x];
-              if (j + 1 <= it.q0 + x && !issue_qk(x, j + 1)) ok = false;
+            tc_fence_after();
+            pv(r & 1u, j == 0);
+            // S_x = Q_x K_{j+1}^T overwrites P_x only after the product above (issue order)
+            if (j < qlast) qk(r1 & 1u);
+            // hand the turn over, unless this issuer's own products of block q0 + 1 come next
+            if (nt == 2 && (x == 0 || j != q0)) mbar_arrive(bar(B_TURN + (x ^ 1u)));
+            umma_commit(bar(B_PV_DONE + x));
+            umma_commit(bar(B_V_EMPTY + 2 * x + (r & 1u)));
+            st ^= 4u;
+            if (j < qlast) {
+              umma_commit(bar(B_S_FULL + x));
+              umma_commit(bar(B_K_EMPTY + 2 * x + (r1 & 1u)));
+              if (j + 1 == qlast) umma_commit(bar(B_Q_EMPTY + x));  // its Q buffer is free
             }
           }
-          for (int x = 0; x < it.ntiles; ++x) ++nq[x];
+          st = (st ^ 1u) | 2u;
           gb += static_cast<uint32_t>(it.nblk);
+          prev_nt = nt;
         }
       }
-      // every MMA this thread issued has completed once the drain barrier flips
-      umma_commit(bar(B_DRAIN));
-      attn_wait_drain(bar(B_DRAIN), 0);
+      // every MMA this thread issued has completed once its drain barrier flips
+      umma_commit(bar(B_DRAIN + x));
+      attn_wait_drain(bar(B_DRAIN + x), 0);
     }
     __syncwarp();
   } else {
