@@ -322,8 +322,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // tile 0 takes its turn in every block of a two-tile item, tile 1 in every block but
                 // its last (which follows its own products of block q0)
                 !take_turn(nt == 2 && (x == 0 || j <= q0)) ||
-                // P_FULL completes once per key block the tile processes, in this order
-                !mbar_wait(bar(B_P_FULL + x), (st >> 2) & 1u, abort_flag, err, a.err_site + 6)) {
+                // P_FULL completes once per key block the tile processes, in this order; it is the
+                // critical path, so it is polled rather than waited on with a suspending try_wait
+                !mbar_poll(bar(B_P_FULL + x), (st >> 2) & 1u, abort_flag, err, a.err_site + 6)) {
               ok = false;
               break;
             }
@@ -437,16 +438,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int i = 0; i < k; ++i) l8[i] += l8[i + k];
           l_run = l_run * alpha + l8[0];
           m_run = mx;
-          if (j > 0) {
-            // O_x and the P_x columns are free once the previous block's O_x += P_x V has completed
-            ok = mbar_wait(bar(B_PV_DONE + x), (cb - 1u) & 1u, abort_flag, err, a.err_site + 9);
-            if (!__all_sync(0xFFFFFFFFu, ok)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          // P_x -> the first 64 columns of S_x
+          // P_x -> the first 64 columns of S_x.  They and O_x are free: the previous block's
+          // O_x += P_x V was issued before this block's S_x = Q_x K^T by the same thread, so it has
+          // completed once S_FULL has (a commit arrives when all earlier operations of its thread have)
           tmem_st32(tS, pk[0]);
           tmem_st32(tS + 32u, pk[1]);
           if (j > 0 && raise) {

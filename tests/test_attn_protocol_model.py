@@ -281,9 +281,7 @@ class Model:
             for j in range(qblk + 1):
                 while not self.wait(f"SF{x}", cb & 1, cb + 1):
                     yield
-                if j > 0:
-                    while not self.wait(f"PD{x}", (cb - 1) & 1, cb):
-                        yield
+                # no wait for the previous P_x V: S_FULL is committed after it by the same issuer
                 assert self.pv_pending[x] == 0, "P_x written while a P_x V product is in flight"
                 self.bars[f"PF{x}"].arrive(4)
                 cb += 1
