@@ -127,19 +127,44 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, int& g,
   nt = in / gsize;
 }
 
+// Output tile o (0, 1, ...) of a unit of the fused shard-sum: tiles unit, unit + units, ... of the
+// (M, N) space while whole rounds of tiles remain.  A last round that would keep at most half the
+// units busy is split into half-width tiles (256 x 128, half = 0 or 1; otherwise half = -1), two
+// per tile, so that twice as many units share it.  Every element is computed exactly as in a whole
+// tile: the same products over the same K steps, the same shard order.
+__device__ __forceinline__ bool fused_tile(int o, const GemmArgs& a, int unit, int units, int& mt, int& nt,
+                                           int& half) {
+  const int tiles = a.m_tiles * a.n_tiles;
+  const int full = tiles / units, rest = tiles - full * units;
+  const bool split = kPairMma && rest > 0 && 2 * rest <= units;
+  int g, ot;
+  if (o < full || (o == full && !split)) {
+    ot = unit + o * units;
+    half = -1;
+  } else {
+    if (o > full || unit >= 2 * rest) return false;
+    ot = full * units + (unit >> 1);
+    half = unit & 1;
+  }
+  if (ot >= tiles) return false;
+  decode_tile(ot, a, g, mt, nt);
+  return true;
+}
+
 // Sub-tile s (0, 1, ...) of a unit's sequence.  Every variant but the fused shard-sum visits tiles
-// unit, unit + units, ... of the (batch, M, N) tile space; the fused shard-sum visits output tiles
-// unit, unit + units, ... of the (M, N) space and, for each, its `batches` shards in order, so that
-// one unit produces every partial of the tiles it owns.  False past the end of the sequence.
+// unit, unit + units, ... of the (batch, M, N) tile space (half = -1); the fused shard-sum visits its
+// output tiles (fused_tile) and, for each, its `batches` shards in order, so that one unit produces
+// every partial of the tiles it owns.  False past the end of the sequence.
 template <int EPI>
-__device__ __forceinline__ bool tile_at(int s, const GemmArgs& a, int unit, int units, int& g, int& mt, int& nt) {
+__device__ __forceinline__ bool tile_at(int s, const GemmArgs& a, int unit, int units, int& g, int& mt, int& nt,
+                                        int& half) {
   if constexpr (EPI == EPI_F32_REDUCE) {
-    const int ot = unit + (s / a.batches) * units;
-    if (ot >= a.m_tiles * a.n_tiles) return false;
-    decode_tile(ot, a, g, mt, nt);
-    g = s - (s / a.batches) * a.batches;
+    const int o = s / a.batches;
+    if (!fused_tile(o, a, unit, units, mt, nt, half)) return false;
+    g = s - o * a.batches;
     return true;
   } else {
+    half = -1;
     const int tile = unit + s * units;
     if (tile >= a.batches * a.m_tiles * a.n_tiles) return false;
     decode_tile(tile, a, g, mt, nt);
@@ -753,13 +778,15 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtens
 // counted by `nfin`).  Returns false if a bounded wait gave up.
 template <int NC, bool SCALE>
 __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const EpiMaps& em, uint32_t tacc, int g,
-                                                    int row0, int col0, uint32_t staging, uint32_t& nchunk,
-                                                    uint32_t fin_ready, uint32_t fin_done, uint32_t& nfin,
-                                                    int lane, volatile int* abort_flag, int* err) {
+                                                    int row0, int col0, int width, uint32_t staging,
+                                                    uint32_t& nchunk, uint32_t fin_ready, uint32_t fin_done,
+                                                    uint32_t& nfin, int lane, volatile int* abort_flag, int* err) {
   if (row0 >= a.M) return true;
-  const int nch = (min(NC, a.N - col0) + 31) / 32;  // chunks of this sub-tile (the same for every shard)
+  // chunks of this sub-tile (the same for every shard): width columns (NC, or half of it for a
+  // half-width tile), clipped at the matrix edge
+  const int nch = (max(0, min(width, a.N - col0)) + 31) / 32;
 #pragma unroll 1
-  for (int cc = 0; cc < NC; cc += 32) {
+  for (int cc = 0; cc < width; cc += 32) {
     if (col0 + cc >= a.N) break;
     const uint32_t buf = staging + (nchunk & 1u) * 4096u;
     if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
@@ -814,11 +841,9 @@ __device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const Epi
 __device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, int units, int tile_m, int row_base,
                                                   uint32_t fin_ready, uint32_t fin_done, int lane,
                                                   volatile int* abort_flag, int* err) {
-  const int out_tiles = a.m_tiles * a.n_tiles;
   uint32_t nfin = 0;
-  for (int ot = unit; ot < out_tiles; ot += units) {
-    int g, mt, nt;
-    decode_tile(ot, a, g, mt, nt);
+  int mt, nt, half;
+  for (int o = 0; fused_tile(o, a, unit, units, mt, nt, half); ++o) {
     const int row0 = mt * tile_m + row_base;
     if (row0 >= a.M) continue;
     const uint32_t slot = nfin & 1u, use = (nfin >> 1) & 1u;
@@ -826,8 +851,9 @@ __device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, i
     const bool ok = mbar_wait(fin_ready + 8u * slot, use, abort_flag, err, a.err_site + 7);
     if (!__all_sync(0xFFFFFFFFu, ok)) return;
     fence_proxy_async_global();
-    const int c = nt * kBN + lane * 8;
-    const bool col_ok = c < a.N;  // N is a multiple of 8: a lane's 8 columns are all in or all out
+    // a half-width tile's 128 columns are lanes 0-15's
+    const int c = nt * kBN + (half > 0 ? kBN / 2 : 0) + lane * 8;
+    const bool col_ok = c < a.N && (half < 0 || lane < 16);  // N % 8 = 0: a lane's 8 columns are all in or out
     const float* S = static_cast<const float*>(a.out0);
     const uint16_t* res = static_cast<const uint16_t*>(a.in0);
     uint16_t* Y = static_cast<uint16_t*>(a.out1);
@@ -889,6 +915,9 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
   constexpr int kKe = F8 ? 128 : kBK;  // K elements per stage (always 128 bytes per row)
   constexpr uint32_t kIdesc =
       F8 ? idesc_e4m3_f32(R::kTileM, kBN, A_MN, B_MN) : idesc_bf16_f32(R::kTileM, kBN, A_MN, B_MN);
+  // half-width tiles of the fused shard-sum's last round (fused_tile)
+  constexpr uint32_t kIdescHalf =
+      F8 ? idesc_e4m3_f32(R::kTileM, kBN / 2, A_MN, B_MN) : idesc_bf16_f32(R::kTileM, kBN / 2, A_MN, B_MN);
   // barrier indices in the control block
   constexpr int kBarFull = 0, kBarEmpty = S, kBarTmemFull = 2 * S, kBarTmemEmpty = 2 * S + 2,
                 kBarDrain = 2 * S + 4, kBarEpiIn = 2 * S + 5;  // kBarEpiIn: one per epilogue warp
@@ -981,10 +1010,14 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       // ---------------- TMA producer (both CTAs of a pair load their own halves)
       uint32_t s = 0, ph = 0, armed = 0, armed_ph = 0, issued = 0;
       bool ok = true;
-      int g, mt, nt;
-      for (int sq = 0; ok && tile_at<EPI>(sq, args, unit, units, g, mt, nt); ++sq) {
+      int g, mt, nt, hw;
+      for (int sq = 0; ok && tile_at<EPI>(sq, args, unit, units, g, mt, nt, hw); ++sq) {
         const int m0 = mt * R::kTileM + static_cast<int>(rank) * kBM + args.a_row_off;
-        const int n0 = nt * kOutN + args.b_row_off + ((PAIR && !kGatedB) ? static_cast<int>(rank) * 128 : 0);
+        // a half-width tile (hw = 0, 1: fused shard-sum only) takes 64 B rows per CTA of the pair;
+        // the 128-row box brings 64 more that its product does not read
+        const int n0 = nt * kOutN + args.b_row_off +
+                       (hw < 0 ? ((PAIR && !kGatedB) ? static_cast<int>(rank) * 128 : 0)
+                               : 128 * hw + static_cast<int>(rank) * 64);
         const int ga = g * args.a_bmul, gb = g * args.b_bmul;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, err, args.err_site + 1)) {
@@ -1067,8 +1100,9 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       // ---------------- MMA issuer (the leader CTA of a pair issues for both)
       uint32_t s = 0, ph = 0;
       bool ok = true;
-      int g, mt, nt;
-      for (int it = 0; ok && tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
+      int g, mt, nt, hw;
+      for (int it = 0; ok && tile_at<EPI>(it, args, unit, units, g, mt, nt, hw); ++it) {
+        const uint32_t idesc = hw < 0 ? kIdesc : kIdescHalf;
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait(bar(kBarTmemEmpty + acc), use ^ 1u, abort_flag, err, args.err_site + 2)) break;
@@ -1088,11 +1122,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
             if constexpr (F8)
-              umma_f8_pair(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
+              umma_f8_pair(d_tmem, ad, bd, idesc, static_cast<uint32_t>((kb | kk) != 0));
             else if constexpr (PAIR)
-              umma_bf16_pair(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
+              umma_bf16_pair(d_tmem, ad, bd, idesc, static_cast<uint32_t>((kb | kk) != 0));
             else
-              umma_bf16(d_tmem, ad, bd, kIdesc, static_cast<uint32_t>((kb | kk) != 0));
+              umma_bf16(d_tmem, ad, bd, idesc, static_cast<uint32_t>((kb | kk) != 0));
           }
           if constexpr (PAIR)
             umma_commit_pair_multicast(bar(kBarEmpty + s), 0x3);
@@ -1171,8 +1205,8 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
       }
       }
     } else {
-      int g, mt, nt;
-      for (int it = 0; tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
+      int g, mt, nt, hw;
+      for (int it = 0; tile_at<EPI>(it, args, unit, units, g, mt, nt, hw); ++it) {
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         const bool ok = mbar_wait(bar(kBarTmemFull + acc), use, abort_flag, err, args.err_site + 4);
@@ -1186,10 +1220,11 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         else if constexpr (is_act_f8(EPI))
           epilogue_f8_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
         else if constexpr (EPI == EPI_F32_REDUCE) {
-          if (!epilogue_f32_reduce<kHalfOut, F8>(args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
-                                             nt * kOutN + half * kHalfOut, staging, nchunk,
-                                             bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), nfin,
-                                             lane, abort_flag, err))
+          if (!epilogue_f32_reduce<kHalfOut, F8>(
+                  args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
+                  nt * kOutN + half * kHalfOut + (hw > 0 ? kHalfOut / 2 : 0), hw < 0 ? kHalfOut : kHalfOut / 2,
+                  staging, nchunk, bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), nfin, lane,
+                  abort_flag, err))
             break;
         }
         else if constexpr (is_act_fwd(EPI))
@@ -1275,10 +1310,13 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ep
     }
     max_units_of[dev].store(max_units, std::memory_order_release);
   }
-  // units own whole output tiles (with all their shards) in the fused shard-sum
+  // units own whole output tiles (with all their shards) in the fused shard-sum, whose tiles of a
+  // last round that keeps at most half the units busy are split in two (fused_tile): a launch with
+  // at most half as many tiles as units gets two units per tile
   const int64_t tiles = int64_t(EPI == EPI_F32_REDUCE ? 1 : args.batches) * args.m_tiles * args.n_tiles;
   if (tiles == 0 || args.batches == 0) return cudaSuccess;
-  const int units = static_cast<int>(tiles < max_units ? tiles : max_units);
+  const int64_t want = (EPI == EPI_F32_REDUCE && P && 2 * tiles <= max_units) ? 2 * tiles : tiles;
+  const int units = static_cast<int>(want < max_units ? want : max_units);
   if constexpr (P) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
