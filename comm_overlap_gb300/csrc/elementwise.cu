@@ -137,11 +137,66 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const uint16_t* __restri
   }
 }
 
+// The same LayerNorm with the row read from memory once: each lane keeps its (at most NPL) 16-byte
+// pieces of the row in registers across the three passes.  Every sum takes the same terms in the
+// same order as layernorm_kernel, so the results are the same bit for bit.
+template <int NPL>
+__global__ void __launch_bounds__(256) layernorm_reg_kernel(const uint16_t* __restrict__ Z, int64_t rows,
+                                                            int64_t h, float eps, uint16_t* __restrict__ out,
+                                                            float* __restrict__ rstd_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (r >= rows) return;
+  const uint4* z = reinterpret_cast<const uint4*>(Z + r * h);
+  uint4* o = reinterpret_cast<uint4*>(out + r * h);
+  const int nv = static_cast<int>(h / 8);
+  uint4 w[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) w[i] = (lane + 32 * i < nv) ? z[lane + 32 * i] : make_uint4(0u, 0u, 0u, 0u);
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i < nv)
+      s += bf16lo(w[i].x) + bf16hi(w[i].x) + bf16lo(w[i].y) + bf16hi(w[i].y) + bf16lo(w[i].z) + bf16hi(w[i].z) +
+           bf16lo(w[i].w) + bf16hi(w[i].w);
+  const float mean = warp_sum(s) / static_cast<float>(h);
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i < nv) {
+      const float d[8] = {bf16lo(w[i].x) - mean, bf16hi(w[i].x) - mean, bf16lo(w[i].y) - mean,
+                          bf16hi(w[i].y) - mean, bf16lo(w[i].z) - mean, bf16hi(w[i].z) - mean,
+                          bf16lo(w[i].w) - mean, bf16hi(w[i].w) - mean};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss += d[e] * d[e];
+    }
+  const float rstd = rsqrtf(warp_sum(ss) / static_cast<float>(h) + eps);
+  if (rstd_out && lane == 0) rstd_out[r] = rstd;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i < nv) {
+      uint4 y;
+      y.x = pack_bf16x2((bf16lo(w[i].x) - mean) * rstd, (bf16hi(w[i].x) - mean) * rstd);
+      y.y = pack_bf16x2((bf16lo(w[i].y) - mean) * rstd, (bf16hi(w[i].y) - mean) * rstd);
+      y.z = pack_bf16x2((bf16lo(w[i].z) - mean) * rstd, (bf16hi(w[i].z) - mean) * rstd);
+      y.w = pack_bf16x2((bf16lo(w[i].w) - mean) * rstd, (bf16hi(w[i].w) - mean) * rstd);
+      o[lane + 32 * i] = y;
+    }
+}
+
 cudaError_t launch_layernorm(const uint16_t* Z, int64_t rows, int64_t h, float eps, uint16_t* out,
                              float* rstd, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int grid = static_cast<int>((rows + 7) / 8);
-  layernorm_kernel<<<grid, 256, 0, st>>>(Z, rows, h, eps, out, rstd);
+  const int64_t per_lane = (h / 8 + 31) / 32;  // 16-byte pieces of a row per lane
+  if (per_lane <= 8)
+    layernorm_reg_kernel<8><<<grid, 256, 0, st>>>(Z, rows, h, eps, out, rstd);
+  else if (per_lane <= 16)
+    layernorm_reg_kernel<16><<<grid, 256, 0, st>>>(Z, rows, h, eps, out, rstd);
+  else if (per_lane <= 32)
+    layernorm_reg_kernel<32><<<grid, 256, 0, st>>>(Z, rows, h, eps, out, rstd);
+  else
+    layernorm_kernel<<<grid, 256, 0, st>>>(Z, rows, h, eps, out, rstd);
   return cudaGetLastError();
 }
 
@@ -191,11 +246,72 @@ __global__ void __launch_bounds__(256) layernorm_bwd_kernel(const uint16_t* __re
   }
 }
 
+// The same backward with gN and N read from memory once (kept in registers across both passes;
+// same sums in the same order as layernorm_bwd_kernel, so the same results bit for bit).
+template <int NPL>
+__global__ void __launch_bounds__(256) layernorm_bwd_reg_kernel(const uint16_t* __restrict__ gN,
+                                                                const uint16_t* __restrict__ N,
+                                                                const float* __restrict__ rstd,
+                                                                const uint16_t* res, uint16_t* out, int64_t rows,
+                                                                int64_t h) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (r >= rows) return;
+  const uint4* g = reinterpret_cast<const uint4*>(gN + r * h);
+  const uint4* n = reinterpret_cast<const uint4*>(N + r * h);
+  const int nv = static_cast<int>(h / 8);
+  uint4 gw[NPL], nw[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const bool in = lane + 32 * i < nv;
+    gw[i] = in ? g[lane + 32 * i] : make_uint4(0u, 0u, 0u, 0u);
+    nw[i] = in ? n[lane + 32 * i] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float sg = 0.0f, sgn = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i < nv) {
+      const uint32_t ga[4] = {gw[i].x, gw[i].y, gw[i].z, gw[i].w}, na[4] = {nw[i].x, nw[i].y, nw[i].z, nw[i].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float g0 = bf16lo(ga[e]), g1 = bf16hi(ga[e]);
+        sg += g0 + g1;
+        sgn += g0 * bf16lo(na[e]) + g1 * bf16hi(na[e]);
+      }
+    }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float mg = warp_sum(sg) * inv_h, mgn = warp_sum(sgn) * inv_h;
+  const float rs = rstd[r];
+  const uint4* rr = reinterpret_cast<const uint4*>(res + r * h);
+  uint4* o = reinterpret_cast<uint4*>(out + r * h);
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i < nv) {
+      const uint4 rw = rr[lane + 32 * i];
+      const uint32_t ga[4] = {gw[i].x, gw[i].y, gw[i].z, gw[i].w}, na[4] = {nw[i].x, nw[i].y, nw[i].z, nw[i].w},
+                     ra[4] = {rw.x, rw.y, rw.z, rw.w};
+      uint32_t oa[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float d0 = rs * (bf16lo(ga[e]) - mg - bf16lo(na[e]) * mgn);
+        const float d1 = rs * (bf16hi(ga[e]) - mg - bf16hi(na[e]) * mgn);
+        oa[e] = pack_bf16x2(bf16lo(ra[e]) + d0, bf16hi(ra[e]) + d1);
+      }
+      o[lane + 32 * i] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    }
+}
+
 cudaError_t launch_layernorm_bwd(const uint16_t* gN, const uint16_t* N, const float* rstd, const uint16_t* res,
                                  uint16_t* out, int64_t rows, int64_t h, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int grid = static_cast<int>((rows + 7) / 8);
-  layernorm_bwd_kernel<<<grid, 256, 0, st>>>(gN, N, rstd, res, out, rows, h);
+  const int64_t per_lane = (h / 8 + 31) / 32;  // 16-byte pieces of a row per lane
+  if (per_lane <= 8)
+    layernorm_bwd_reg_kernel<8><<<grid, 256, 0, st>>>(gN, N, rstd, res, out, rows, h);
+  else if (per_lane <= 16)
+    layernorm_bwd_reg_kernel<16><<<grid, 256, 0, st>>>(gN, N, rstd, res, out, rows, h);
+  else
+    layernorm_bwd_kernel<<<grid, 256, 0, st>>>(gN, N, rstd, res, out, rows, h);
   return cudaGetLastError();
 }
 
