@@ -48,21 +48,21 @@ def source_group(kernel: str) -> str:
     return "attention" if kernel == "attention" else "elementwise"
 
 
-# DRAM traffic per launch from ncu captures, keyed by workload and kernel kind, with the hash of
-# the kind's sources at capture time (profiles/traffic_llama3_8b_swiglu_fwdbwd.md has the commands).
+# DRAM traffic per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
+# workload and kernel kind, with the hash of the kind's sources at capture time.
 # Captured one kernel and one launch at a time on a small case of the workload (M = 8192 tokens in
 # one row chunk, m = 8192 per launch) and scaled x 2 to the m = 16384 launch of the full workload:
 # only kinds whose reduction length does not grow with the tokens are listed, since their traffic
 # grows in proportion to the rows a launch processes.  The weight-gradient GEMMs reduce over the
 # tokens, so theirs does not scale that way and is left out (reported null).
-_SHA_GEMM = "4015170d581ec9f3"
-_SHA_ELEM = "a7ed1f2e50e41e65"
+_SHA_GEMM = "c305f40b5939b891"
+_SHA_ELEM = "6a7ca743efb34cd0"
 NCU_TRAFFIC = {
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 2 * 1.478e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2 * 1.447e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2 * 1.091e9, "src_sha": _SHA_ELEM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 2 * 2.110e9, "src_sha": _SHA_GEMM},
-    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 2 * 2.328e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd1"): {"bytes_per_launch": 2 * 1.535e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_fwd2"): {"bytes_per_launch": 2 * 1.448e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "shard_sum"): {"bytes_per_launch": 2 * 1.092e9, "src_sha": _SHA_ELEM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_h"): {"bytes_per_launch": 2 * 2.099e9, "src_sha": _SHA_GEMM},
+    ("llama3_8b_swiglu_fwdbwd", "gemm_dgrad_x"): {"bytes_per_launch": 2 * 2.315e9, "src_sha": _SHA_GEMM},
 }
 
 
