@@ -11,8 +11,8 @@
 // The kernel is persistent: one CTA per SM walks a fixed list of units, a unit being the heaviest
 // and the lightest remaining item of one (head, sequence), so that all units cost about the same;
 // consecutive CTAs take consecutive units, which keeps the K/V of the heads in flight in L2.  The
-// next item's Q tiles are loaded as soon as the current item's last Q K^T products have been
-// issued, and its first products start while the current item's O is being written out.
+// next item's Q tiles are loaded as soon as the current item's last Q K^T products have
+// completed, and its first products start while the current item's O is being written out.
 // Warp roles:
 //   warp 0 (one lane)  TMA producer: each item's Q tiles, then its K and V tiles into two-deep rings
 //                      (the rings run on across items).
@@ -24,7 +24,8 @@
 //                      issuer leaves the tensor core idle while it waits and commits.  The two issuers
 //                      take turns (B_TURN) in the order one issuer would use -- per block tile 0's
 //                      products, then tile 1's, so that neither tile's products are spread out by the
-//                      other's -- and each waits for its data before its turn and commits after it.
+//                      other's -- and each waits for its data before its turn (the softmax hand-off
+//                      last, polled: it is the critical path) and commits after it.
 //   warps 2-5, 6-9     softmax of tile 0 and tile 1, one query row per thread (TMEM lane quarter =
 //                      warp % 4): scores from TMEM, running max / sum in fp32, O_x rescaled in TMEM
 //                      when a row maximum grew, P rounded to bf16 and stored into TMEM; at the end
