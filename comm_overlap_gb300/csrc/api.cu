@@ -213,10 +213,10 @@ domino_status make_plan_impl(const domino_cfg* c, int pass, Plan* P) {
       off = align_up(off + size_t(p.M) * p.h * 2);
     }
   }
-  // partial slots of t x m x n fp32; the fused schedule needs only one m x n fp32 sum
+  // partial slots of t x m x n fp32; the fused schedule keeps its sums on chip and needs none
   if (p.sched == DOMINO_SCHED_FUSED) {
     p.nslots = 1;
-    p.part_slot = align_up(size_t(p.m) * p.n * 4);
+    p.part_slot = 0;
   } else {
     p.part_slot = align_up(size_t(p.t) * p.m * p.n * 4);
   }
@@ -384,13 +384,14 @@ GemmArgs gemm_args(int variant, int batches, int64_t M, int64_t N, int64_t K, in
   return a;
 }
 
-// `em`: the epilogue's tensor maps (fp32-partial and activation-backward variants); others ignore it.
+// `em`: the epilogue's tensor maps (fp32-partial and activation variants); others ignore it.
 domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap& ta,
                        const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st,
                        const dm::EpiMaps* em = nullptr) {
   const int64_t tiles = int64_t(a.batches) * a.m_tiles * a.n_tiles;
   if (tiles == 0) return DOMINO_OK;
-  const bool needs = variant != dm::GV_WGRAD && variant != dm::GV_F8_FWD_ACT && variant != dm::GV_F8_FWD_GLU;
+  const bool needs = variant != dm::GV_WGRAD && variant != dm::GV_F8_FWD_ACT && variant != dm::GV_F8_FWD_GLU &&
+                     variant != dm::GV_FWD_REDUCE && variant != dm::GV_BWD_REDUCE && variant != dm::GV_F8_FWD_REDUCE;
   if (needs && em == nullptr) return fail(DOMINO_ERR_INVALID_ARG, "internal: GEMM epilogue without its maps");
   static const dm::EpiMaps kNone = {};
   const dm::EpiMaps& e = em ? *em : kNone;
@@ -403,21 +404,15 @@ domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap
   });
 }
 
-// The fused second linear (or input-gradient GEMM) + shard-sum of one column chunk: `Sbuf` is the
-// m x n fp32 sum, `res` (nullable) and `Y` are row-major with leading dimension ld.
-domino_status run_fused_reduce(domino_handle H, int kind, int variant, const Plan& P, const CUtensorMap& ta,
-                               const CUtensorMap& tb, GemmArgs a, float* Sbuf, const uint16_t* res, uint16_t* Y,
-                               int64_t ld, cudaStream_t st) {
-  a.out0 = Sbuf;
-  a.ld0 = P.n;
-  a.bs0 = 0;
+// The fused second linear (or input-gradient GEMM) + shard-sum of one column chunk, the sums held
+// on chip: `res` (nullable) and `Y` are row-major with leading dimension ld.
+domino_status run_fused_reduce(domino_handle H, int kind, int variant, const CUtensorMap& ta, const CUtensorMap& tb,
+                               GemmArgs a, const uint16_t* res, uint16_t* Y, int64_t ld, cudaStream_t st) {
   a.out1 = Y;
   a.ld1 = ld;
   a.in0 = res;
   a.ldi = ld;
-  dm::EpiMaps em = {};
-  DM_TRY(map_f32_out(&em.m[0], Sbuf, P.n, P.m, 1));
-  return run_gemm(H, kind, variant, ta, tb, a, st, &em);
+  return run_gemm(H, kind, variant, ta, tb, a, st, nullptr);
 }
 
 domino_status run_shard_sum(domino_handle H, const float* P, int t, int64_t rows, int64_t cols,
@@ -525,19 +520,19 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
                             const uint16_t* res_c, uint16_t* Yc, int site, bool fp8 = false, float alpha = 1.0f) {
   const int v_reduce = fp8 ? dm::GV_F8_FWD_REDUCE : dm::GV_FWD_REDUCE;
   const int v_partial = fp8 ? dm::GV_F8_FWD_PARTIAL : dm::GV_FWD_PARTIAL;
-  // column chunk qc with the shard-sum folded into the GEMM, its fp32 sum in `sum`
-  auto fused = [&](int qc, float* sum) {
+  // column chunk qc with the shard-sum folded into the GEMM
+  auto fused = [&](int qc) {
     GemmArgs a = gemm_args(v_reduce, P.t, P.m, P.n, Kc, site);
     a.a_bmul = 1;
     a.b_row_off = int32_t(qc * P.n);
     a.b_bmul = 1;
     a.alpha = alpha;
-    return run_fused_reduce(H, kind, v_reduce, P, mapH, mapB, a, sum, res_c ? res_c + qc * P.n : nullptr,
-                            Yc + qc * P.n, P.h, S.comp);
+    return run_fused_reduce(H, kind, v_reduce, mapH, mapB, a, res_c ? res_c + qc * P.n : nullptr, Yc + qc * P.n,
+                            P.h, S.comp);
   };
   for (int qc = 0; qc < P.q; ++qc) {
     if (P.sched == DOMINO_SCHED_FUSED) {
-      DM_TRY(fused(qc, parts));
+      DM_TRY(fused(qc));
       continue;
     }
     int slot;
@@ -546,9 +541,9 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
     if (S.overlap && R.tail && qc == P.q - 1 && !H->skip_reduce) {
       // The call's last reduction would run with nothing left to overlap: the fused kernel adds the
       // shard partials tile by tile inside the GEMM instead (same order, same single rounding, so the
-      // same bits), its fp32 sum in the slot's memory; the reduction stream then waits for it, so the
-      // row events and the join that follow on that stream cover it.
-      DM_TRY(fused(qc, part));
+      // same bits); the slot is taken and handed over only so that the reduction stream waits for
+      // it, and the row events and the join that follow on that stream cover it.
+      DM_TRY(fused(qc));
       DM_TRY(slot_handoff(H, S, slot));
       DM_TRY(slot_release(H, S, R, slot));
       continue;
@@ -746,8 +741,8 @@ domino_status mlp_chunk_bwd(domino_handle H, const Plan& P, const Streams& S, Sl
       a.a_bmul = 1;
       a.b_row_off = int32_t(qc * P.n);
       a.b_bmul = 1;
-      DM_TRY(run_fused_reduce(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_REDUCE, P, C.mapDZk, C.mapAmn, a, C.parts,
-                              nullptr, gX_c + qc * P.n, P.h, S.comp));
+      DM_TRY(run_fused_reduce(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_REDUCE, C.mapDZk, C.mapAmn, a, nullptr,
+                              gX_c + qc * P.n, P.h, S.comp));
       continue;
     }
     int slot;

@@ -12,8 +12,9 @@
 //                      barriers.
 //   warps 2-5          epilogue: tcgen05.ld of the accumulator (each warp its 32-lane quarter, one
 //                      row per thread), the variant's epilogue, then the accumulator is handed
-//                      back so tile i+1's epilogue overlaps tile i+2's main loop.
-//   warps 6-9          (fused shard-sum only) finalisers: sum -> bf16 output.
+//                      back so tile i+1's epilogue overlaps tile i+2's main loop.  The fused
+//                      shard-sum has eight epilogue warps (2-9, two per quarter) that keep their
+//                      rows' running sums over the shards in registers.
 // Every wait is bounded (ptx.cuh); on expiry the CTA drains what it has in flight, frees TMEM
 // and returns, leaving a code in the translation unit's error word.
 #pragma once
@@ -48,13 +49,11 @@ struct Ring {
 };
 constexpr int kCtrlBytes = 1024;
 
-// Four epilogue warps, one per TMEM lane quarter (32 rows), all accumulator columns.
-// Block = TMA warp + MMA warp + epilogue warps.
+// Four epilogue warps, one per TMEM lane quarter (32 rows), all accumulator columns; the fused
+// shard-sum has eight, two per lane quarter with 128 columns each, whose threads keep their row's
+// running sums in registers.  Block = TMA warp + MMA warp + epilogue warps.
 template <int EPI>
-constexpr int epi_warps() { return 4; }
-// The fused shard-sum adds four finaliser warps (one per lane quarter) after the epilogue warps.
-template <int EPI>
-constexpr int fin_warps() { return EPI == EPI_F32_REDUCE ? 4 : 0; }
+constexpr int epi_warps() { return EPI == EPI_F32_REDUCE ? 8 : 4; }
 // The activation backward and the non-gated bf16 forward activation add two helper warps
 // (sub-partitions 2 and 3) that do the arithmetic of lane quarter 1 for its reader warp, which shares
 // a sub-partition with the MMA issuer.  (The same split for the E4M3 GeLU epilogue sped up its kernel
@@ -64,7 +63,12 @@ constexpr int helper_warps() { return (is_act_bwd(EPI) || EPI == EPI_ACT_BF16) ?
 // Accumulator slots between the reader and the helpers (4 KiB each, see epilogue_acc_reader).
 constexpr int kAccSlots = 2;
 template <int EPI>
-constexpr int block_threads() { return 64 + 32 * (epi_warps<EPI>() + fin_warps<EPI>() + helper_warps<EPI>()); }
+constexpr int block_threads() { return 64 + 32 * (epi_warps<EPI>() + helper_warps<EPI>()); }
+// Threads a CTA is compiled for.  The fused shard-sum's ten warps put three on some sub-partitions,
+// whose 16K registers then allow at most 168 a thread; compiling it as if for 384 threads keeps
+// the compiler within that bound.
+template <int EPI>
+constexpr int bound_threads() { return EPI == EPI_F32_REDUCE ? 384 : block_threads<EPI>(); }
 // Epilogues that move data with TMA stage it in shared memory, per epilogue warp:
 //  fp32 partials: two 4 KiB buffers (32 rows x 32 fp32, 128-byte swizzle);
 //  activation backward: per warp that does arithmetic (epilogue warps 2-4 and the two helpers; the
@@ -80,7 +84,7 @@ constexpr bool is_act_f8(int epi) { return epi == EPI_ACT_F8 || epi == EPI_GLU_F
 constexpr bool is_gated_b(int epi) { return epi == EPI_GLU_BF16 || epi == EPI_GLU_F8; }
 template <int EPI>
 constexpr int staging_bytes() {
-  return (EPI == EPI_F32_STORE || EPI == EPI_F32_REDUCE) ? 4 * 2 * 4096
+  return EPI == EPI_F32_STORE ? 4 * 2 * 4096
                               : (is_act_bwd(EPI) ? 5 * kActBwdWarpBytes + 2 * 4096
                                                  : (EPI == EPI_ACT_BF16 ? 5 * kFwdActWarpBytes + 2 * 4096
                                                                         : (is_act_fwd(EPI) ? 4 * kFwdWarpBytes : 0)));
@@ -765,144 +769,73 @@ __device__ __forceinline__ void epilogue_f32_tma(const GemmArgs& a, const CUtens
   }
 }
 
-// Fused shard-sum epilogue (EPI_F32_REDUCE) of one sub-tile, shard g of an output tile, for the
-// warp's 32 rows, in 32-column chunks staged as in epilogue_f32_tma.  A unit visits the shards of
-// an output tile consecutively, so the warp that handles these rows for shard g handled them for
-// every earlier shard too.  Shard 0 stores its fp32 partial into the sum S (out0, map m[0]); shard
-// g > 0 has the TMA unit add its partial into S at L2.  Each 32-column chunk is one bulk group and
-// every shard of a tile has the same number of chunks (nch), so the same chunk of shard g-1 was
-// committed nch groups earlier: waiting until at most nch - 1 groups are pending before issuing a
-// chunk's add orders it after that chunk's previous write, and every element of S receives
-// ((P_0 + P_1) + ...) + P_g in shard order, each add rounded to nearest.  After the last shard's adds complete, the rows are handed to the
-// finaliser warp of the same lane quarter (two-slot mbarrier ring `fin_ready` / `fin_done`,
-// counted by `nfin`).  Returns false if a bounded wait gave up.
-template <int NC, bool SCALE>
-__device__ __forceinline__ bool epilogue_f32_reduce(const GemmArgs& a, const EpiMaps& em, uint32_t tacc, int g,
-                                                    int row0, int col0, int width, uint32_t staging,
-                                                    uint32_t& nchunk, uint32_t fin_ready, uint32_t fin_done,
-                                                    uint32_t& nfin, int lane, volatile int* abort_flag, int* err) {
-  if (row0 >= a.M) return true;
-  // chunks of this sub-tile (the same for every shard): width columns (NC, or half of it for a
-  // half-width tile), clipped at the matrix edge
-  const int nch = (max(0, min(width, a.N - col0)) + 31) / 32;
-#pragma unroll 1
-  for (int cc = 0; cc < width; cc += 32) {
-    if (col0 + cc >= a.N) break;
-    const uint32_t buf = staging + (nchunk & 1u) * 4096u;
-    if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
-    __syncwarp();
-    uint32_t r[32];
-    tmem_ld32(tacc + cc, r);
-    tmem_ld_wait();
-    if constexpr (SCALE) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a.alpha);
-    }
-    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u)) << 4), r[4 * j],
-                   r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      // the sum stays in L2 until its tile is finalised
-      const uint64_t keep = l2_policy_evict_last();
-      if (g == 0) {
-        tma_store_3d_hint(&em.m[0], buf, col0 + cc, row0, 0, keep);
-      } else {
-        bulk_wait_group_upto(nch - 1);  // this chunk's write for shard g-1 has completed
-        tma_reduce_add_3d_hint(&em.m[0], buf, col0 + cc, row0, 0, keep);
-      }
-      bulk_commit_group();
-    }
-    ++nchunk;
-  }
-  if (g < a.batches - 1) return true;
-  const uint32_t slot = nfin & 1u, use = (nfin >> 1) & 1u;
-  ++nfin;
-  bool ok = true;
-  if (lane == 0) {
-    bulk_wait_group_all();       // S holds the full sum for these rows
-    fence_proxy_async_global();  // ... and the finaliser's generic loads come after those writes
-    ok = mbar_wait(fin_done + 8u * slot, use ^ 1u, abort_flag, err, a.err_site + 6);
-    if (ok) mbar_arrive(fin_ready + 8u * slot);
-  }
-  return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+// One 16-column piece of this thread's TMEM lane (32x32b shape, warp-collective).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
-// Finaliser warp of the fused shard-sum: for each output tile of the unit whose rows of this lane
-// quarter are in range, waits until the epilogue warp of the quarter handed the completed sum over,
-// then writes Y = bf16(res + S) (out1 / ld1; residual in0 / ldi, nullable) with coalesced loads and
-// stores (lane l covers columns 8l .. 8l+7 of one row at a time, four rows in flight), and hands
-// the slot back.  It works while the epilogue and MMA warps go on with the next tile's shards.
-// When S rows are whole 128-byte lines (ld0 % 32 == 0), every line of the tile belongs to this
-// tile alone, and once read it is dropped from L2 without a write-back: S is scratch.
-__device__ __forceinline__ void finalize_sum_rows(const GemmArgs& a, int unit, int units, int tile_m, int row_base,
-                                                  uint32_t fin_ready, uint32_t fin_done, int lane,
-                                                  volatile int* abort_flag, int* err) {
-  uint32_t nfin = 0;
-  int mt, nt, half;
-  for (int o = 0; fused_tile(o, a, unit, units, mt, nt, half); ++o) {
-    const int row0 = mt * tile_m + row_base;
-    if (row0 >= a.M) continue;
-    const uint32_t slot = nfin & 1u, use = (nfin >> 1) & 1u;
-    ++nfin;
-    const bool ok = mbar_wait(fin_ready + 8u * slot, use, abort_flag, err, a.err_site + 7);
-    if (!__all_sync(0xFFFFFFFFu, ok)) return;
-    fence_proxy_async_global();
-    // a half-width tile's 128 columns are lanes 0-15's
-    const int c = nt * kBN + (half > 0 ? kBN / 2 : 0) + lane * 8;
-    const bool col_ok = c < a.N && (half < 0 || lane < 16);  // N % 8 = 0: a lane's 8 columns are all in or out
-    const float* S = static_cast<const float*>(a.out0);
-    const uint16_t* res = static_cast<const uint16_t*>(a.in0);
-    uint16_t* Y = static_cast<uint16_t*>(a.out1);
-    const bool drop = (a.ld0 & 31) == 0 && (lane & 3) == 0;  // lanes 0, 4, ... start a 128-byte line
-#pragma unroll 1
-    for (int r = 0; r < 32; r += 4) {
-      float4 lo[4], hi[4];
-      uint4 rv[4];
+// Fused shard-sum (EPI_F32_REDUCE), one sub-tile: shard g's partial of an output tile, for the
+// calling thread's row and `width` accumulator columns from `tacc` (its warp's 128 columns, or 64
+// of a half-width tile).  A unit visits the shards of an output tile consecutively and every warp
+// takes the same rows and columns of each, so the row's running sum stays in the thread's
+// registers: S = P_0, then S = S + P_g for g = 1, 2, ..., one fp32 add rounded to nearest per
+// shard -- the order and the roundings of the stand-alone shard-sum over stored partials (E4M3
+// operands: each partial is first scaled by alpha and rounded, as the partial store does).  No
+// partial leaves the SM.
+template <bool SCALE>
+__device__ __forceinline__ void sum_partial_regs(const GemmArgs& a, uint32_t tacc, int g, int width,
+                                                 float (&s)[128]) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int row = row0 + r + u;
-        const bool in = col_ok && row < a.M;
-        const float* sp = S + static_cast<int64_t>(row) * a.ld0 + c;
-        lo[u] = in ? __ldcg(reinterpret_cast<const float4*>(sp)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        hi[u] = in ? __ldcg(reinterpret_cast<const float4*>(sp + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        rv[u] = (in && res) ? __ldcg(reinterpret_cast<const uint4*>(res + static_cast<int64_t>(row) * a.ldi + c))
-                            : make_uint4(0u, 0u, 0u, 0u);
-      }
+  for (int c = 0; c < 128; c += 16) {
+    if (c >= width) break;
+    uint32_t r[16];
+    tmem_ld16(tacc + static_cast<uint32_t>(c), r);
+    tmem_ld_wait();
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int row = row0 + r + u;
-        if (!(col_ok && row < a.M)) continue;
-        float v[8] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w, hi[u].x, hi[u].y, hi[u].z, hi[u].w};
-        if (res) {
-          // residual first, then the sum, as in the stand-alone shard-sum: res + S, one rounding
-          v[0] = bf16lo(rv[u].x) + v[0]; v[1] = bf16hi(rv[u].x) + v[1];
-          v[2] = bf16lo(rv[u].y) + v[2]; v[3] = bf16hi(rv[u].y) + v[3];
-          v[4] = bf16lo(rv[u].z) + v[4]; v[5] = bf16hi(rv[u].z) + v[5];
-          v[6] = bf16lo(rv[u].w) + v[6]; v[7] = bf16hi(rv[u].w) + v[7];
-        }
-        store8_bf16(Y + static_cast<int64_t>(row) * a.ld1 + c, v);
-      }
-      __syncwarp();  // every lane has its values before a line is dropped
-      if (drop) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int row = row0 + r + u;
-          if (col_ok && row < a.M) discard_l2_line(S + static_cast<int64_t>(row) * a.ld0 + c);
-        }
-      }
+    for (int e = 0; e < 16; ++e) {
+      float v = __uint_as_float(r[e]);
+      if constexpr (SCALE) v = __fmul_rn(v, a.alpha);
+      s[c + e] = g == 0 ? v : __fadd_rn(s[c + e], v);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(fin_done + 8u * slot);
+  }
+}
+
+// After an output tile's last shard: Y = bf16(res + S) (out1 / ld1; residual in0 / ldi, nullable)
+// for the calling thread's row, `width` columns from col0, straight from the registers.  Rows past
+// M and columns past N are not written (N % 8 = 0: eight columns are all in or all out).
+__device__ __forceinline__ void store_sum_row(const GemmArgs& a, int row, int col0, int width,
+                                              const float (&s)[128]) {
+  if (row >= a.M) return;
+  uint16_t* y = static_cast<uint16_t*>(a.out1) + static_cast<int64_t>(row) * a.ld1 + col0;
+  const uint16_t* res = static_cast<const uint16_t*>(a.in0);
+  const uint16_t* rp = res ? res + static_cast<int64_t>(row) * a.ldi + col0 : nullptr;
+#pragma unroll
+  for (int c = 0; c < 128; c += 8) {
+    if (c >= width || col0 + c >= a.N) break;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = s[c + e];
+    if (rp) {
+      // residual first, then the sum, as in the stand-alone shard-sum: res + S, one rounding
+      const uint4 w = __ldcg(reinterpret_cast<const uint4*>(rp + c));
+      v[0] = bf16lo(w.x) + v[0]; v[1] = bf16hi(w.x) + v[1];
+      v[2] = bf16lo(w.y) + v[2]; v[3] = bf16hi(w.y) + v[3];
+      v[4] = bf16lo(w.z) + v[4]; v[5] = bf16hi(w.z) + v[5];
+      v[6] = bf16lo(w.w) + v[6]; v[7] = bf16hi(w.w) + v[7];
+    }
+    store8_bf16(y + c, v);
   }
 }
 
 // F8: operands are E4M3 codes (kind::f8f6f4), 128 elements per 128-byte K step.
 template <int EPI, bool A_MN, bool B_MN, bool PAIR, bool F8 = false>
-__global__ void __launch_bounds__(block_threads<EPI>(), 1)
+__global__ void __launch_bounds__(bound_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ EpiMaps em, const GemmArgs args) {
   using R = Ring<PAIR, EPI>;
@@ -921,10 +854,8 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
   // barrier indices in the control block
   constexpr int kBarFull = 0, kBarEmpty = S, kBarTmemFull = 2 * S, kBarTmemEmpty = 2 * S + 2,
                 kBarDrain = 2 * S + 4, kBarEpiIn = 2 * S + 5;  // kBarEpiIn: one per epilogue warp
-  // fused shard-sum hand-off, two slots per lane quarter: ready (epilogue -> finaliser), done (back)
-  constexpr int kBarFinReady = kBarEpiIn + epi_warps<EPI>(), kBarFinDone = kBarFinReady + 8;
   // the peer CTA's producer reports how many ring uses it issued (CTA pair, leader's barrier)
-  constexpr int kBarPeerCount = kBarFinDone + 8;
+  constexpr int kBarPeerCount = kBarEpiIn + epi_warps<EPI>();
   // helper warps: their input barriers and the accumulator slots of lane quarter 1 (full, empty)
   constexpr int kSlots = kAccSlots;
   constexpr int kBarHelperIn = kBarPeerCount + 1, kBarSlotFull = kBarHelperIn + 2,
@@ -960,8 +891,6 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     }
     mbar_init(bar(kBarDrain), 1);
     for (int e = 0; e < epi_warps<EPI>(); ++e) mbar_init(bar(kBarEpiIn + e), 1);
-    if constexpr (EPI == EPI_F32_REDUCE)
-      for (int i = 0; i < 16; ++i) mbar_init(bar(kBarFinReady + i), 1);
     mbar_init(bar(kBarPeerCount), 1);
     if constexpr (helper_warps<EPI>() > 0) {
       for (int i = 0; i < 2; ++i) mbar_init(bar(kBarHelperIn + i), 1);
@@ -977,7 +906,6 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
     if constexpr (EPI == EPI_F32_STORE) tma_prefetch_map(&em.m[0]);
-    if constexpr (EPI == EPI_F32_REDUCE) tma_prefetch_map(&em.m[0]);
     if constexpr (is_act_fwd(EPI)) {
       tma_prefetch_map(&em.m[0]);
       if (args.out1) tma_prefetch_map(&em.m[1]);
@@ -1150,21 +1078,16 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         umma_commit(bar(kBarDrain));
       mbar_wait_drain(bar(kBarDrain), 0);
     }
-  } else if (fin_warps<EPI>() > 0 && warp >= 2 + epi_warps<EPI>()) {
-    // ---------------- finaliser warps of the fused shard-sum (rows of lane quarter warp % 4)
-    const int quarter = warp & 3;
-    finalize_sum_rows(args, unit, units, R::kTileM, static_cast<int>(rank) * kBM + quarter * 32,
-                      bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), lane, abort_flag, err);
   } else {
-    // ---------------- epilogue warps 2-5: TMEM lane quarter = warp % 4 (the column split below
-    // generalises to more than one warp per quarter; every variant uses one)
+    // ---------------- epilogue warps: TMEM lane quarter = warp % 4; with two warps per quarter (the
+    // fused shard-sum) warps 2-5 take the first and warps 6-9 the second half of the columns
     constexpr int kParts = epi_warps<EPI>() / 4;
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     constexpr int kHalfOut = kOutN / kParts;
     const int row_in_tile = static_cast<int>(rank) * kBM + quarter * 32 + lane;
     const uint32_t staging = stage0 + S * R::kStageBytes + static_cast<uint32_t>(warp - 2) * 8192u;
-    uint32_t nchunk = 0, nfin = 0;
+    uint32_t nchunk = 0;
     if constexpr (is_act_bwd(EPI)) {
       // warps 2-4: lane quarters 2, 3, 0 in full; warp 5 (quarter 1, beside the MMA issuer) only moves
       // its accumulator into two slots; helper warps 6 and 7 take the quarter's even and odd chunks
@@ -1204,6 +1127,42 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
             slots, h, unit, units, total, static_cast<int>(rank) * kBM + 32, lane, abort_flag, err);
       }
       }
+    } else if constexpr (EPI == EPI_F32_REDUCE) {
+      // fused shard-sum: per output tile of the unit (fused_tile), its shards in order, the running
+      // sums of the thread's row in registers; the k-th sub-tile of the unit is in accumulator k % 2
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] = 0.0f;  // every shard 0 overwrites it
+      uint32_t k = 0;
+      bool ok = true;
+      int mt, nt, hw;
+      for (int o = 0; ok && fused_tile(o, args, unit, units, mt, nt, hw); ++o) {
+        // a half-width tile's 128 accumulator columns: 64 per warp of the quarter
+        const int width = hw < 0 ? kHalfOut : kHalfOut / 2;
+        const int cofs = half * width;
+        const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(cofs);
+        for (int g = 0; g < args.batches; ++g, ++k) {
+          const uint32_t acc = k & 1u;
+          ok = mbar_wait(bar(kBarTmemFull + acc), (k >> 1) & 1u, abort_flag, err, args.err_site + 4);
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          sum_partial_regs<F8>(args, tq + acc * kBN, g, width, s);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (PAIR)
+              mbar_arrive_cluster_relaxed(mapa_shared(bar(kBarTmemEmpty + acc), 0));
+            else
+              mbar_arrive(bar(kBarTmemEmpty + acc));
+          }
+        }
+        // the accumulators are handed back; the sum goes out while the next tile's shards run
+        if (ok)
+          store_sum_row(args, mt * R::kTileM + row_in_tile, nt * kOutN + (hw > 0 ? kBN / 2 : 0) + cofs, width, s);
+      }
     } else {
       int g, mt, nt, hw;
       for (int it = 0; tile_at<EPI>(it, args, unit, units, g, mt, nt, hw); ++it) {
@@ -1219,14 +1178,6 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
                                          nt * kOutN + half * kHalfOut, staging, nchunk, lane);
         else if constexpr (is_act_f8(EPI))
           epilogue_f8_cols<EPI, kHalfOut>(args, tacc, g, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut);
-        else if constexpr (EPI == EPI_F32_REDUCE) {
-          if (!epilogue_f32_reduce<kHalfOut, F8>(
-                  args, em, tacc, g, mt * R::kTileM + row_in_tile - lane,
-                  nt * kOutN + half * kHalfOut + (hw > 0 ? kHalfOut / 2 : 0), hw < 0 ? kHalfOut : kHalfOut / 2,
-                  staging, nchunk, bar(kBarFinReady + 2 * quarter), bar(kBarFinDone + 2 * quarter), nfin, lane,
-                  abort_flag, err))
-            break;
-        }
         else if constexpr (is_act_fwd(EPI))
           epilogue_fwd_tma<EPI, kHalfOut>(
               args, em, tacc, g, mt * R::kTileM + row_in_tile - lane, nt * kOutN + half * kHalfOut,
@@ -1245,7 +1196,7 @@ __global__ void __launch_bounds__(block_threads<EPI>(), 1)
         }
       }
     }
-    if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_REDUCE || is_act_fwd(EPI)) {
+    if constexpr (EPI == EPI_F32_STORE || is_act_fwd(EPI)) {
       if (lane == 0) bulk_wait_group_all();  // stores done before the staging memory goes away
       __syncwarp();
     }

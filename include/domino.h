@@ -87,12 +87,13 @@ typedef enum {
  *  FUSED : the reduction is overlapped at tile granularity inside the second linear (and the
  *          input-gradient GEMM of the backward), the one-GPU analogue of GEMM + reduce-scatter
  *          tile pipelining ("04 · TP/SP 的通信-计算 overlap 与工程优化" §3, userbuffers): one
- *          persistent kernel computes, per output tile, the t shard partials in shard order;
- *          each leaves the SM as an fp32 tile that the TMA unit adds into an fp32 sum at L2
- *          (shard 0 stores, shard i > 0 adds after shard i-1's adds completed), and the last
- *          shard's epilogue rounds the sum (plus the residual) once to bf16.  Same arithmetic
- *          and order as the other schedules; everything runs on the caller's stream; the
- *          workspace holds one m x n fp32 sum instead of the partial slots. */
+ *          persistent kernel computes, per output tile, the t shard partials in shard order
+ *          and adds each, as it leaves the tensor-core accumulator, into an fp32 running sum
+ *          held in the epilogue threads' registers (P_0, then + P_1, ..., one rounding per
+ *          add); after the last shard the sum (plus the residual) is rounded once to bf16.
+ *          No partial is written to memory.  Same arithmetic and order as the other
+ *          schedules; everything runs on the caller's stream; the workspace holds no partial
+ *          slots. */
 typedef enum {
   DOMINO_SCHED_SERIAL = 0,
   DOMINO_SCHED_INTRA = 1,

@@ -68,12 +68,12 @@ def test_workspace_size_formula(dlib):
     m, n = 16384, 2048
     assert dlib.domino_workspace_size(cfg, dlib.PASS_STACK) == up(m * 16384 * 2) + up(m * 4096 * 2) + 2 * up(
         4 * m * n * 4)
-    # the fused schedule keeps one m x n fp32 sum instead of the two t x m x n partial slots
+    # the fused schedule keeps its sums on chip: no partial slots at all
     cfg = dlib.make_cfg(M=32768, h=4096, ffn=16384, t=4, p=2, q=2, layers=4, sched=dlib.SCHED_FUSED)
-    assert dlib.domino_workspace_size(cfg, dlib.PASS_STACK) == up(m * 16384 * 2) + up(m * 4096 * 2) + up(m * n * 4)
+    assert dlib.domino_workspace_size(cfg, dlib.PASS_STACK) == up(m * 16384 * 2) + up(m * 4096 * 2)
     M, h, F, t, p, q = 16384, 2560, 10240, 8, 2, 1
     m, n = M // p, h // q
-    assert ws(dlib, M=M, h=h, ffn=F, t=t, p=p, q=q, sched=dlib.SCHED_FUSED) == up(m * F * 2) + up(m * n * 4)
+    assert ws(dlib, M=M, h=h, ffn=F, t=t, p=p, q=q, sched=dlib.SCHED_FUSED) == up(m * F * 2)
     # empty input needs nothing
     assert ws(dlib, M=0, h=64, ffn=64, t=2) == 0
 

@@ -63,8 +63,9 @@ def buffers(c, pass_, off, total):
     gated = c["act"] in (3, 4)
     a_rows = 2 * F if gated else F
     fused = c["sched"] == 3
-    slots = 1 if (fused or p * q < 2) else 2
-    part = m * n * 4 if fused else t * m * n * 4
+    # the fused schedule keeps its shard sums on chip: no partial slots
+    slots = 0 if fused else (1 if p * q < 2 else 2)
+    part = t * m * n * 4
     out = []
     if pass_ in (0, 2):
         out.append(("h", off["h"], m * F * 2))
