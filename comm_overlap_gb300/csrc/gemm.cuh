@@ -806,30 +806,50 @@ __device__ __forceinline__ void sum_partial_regs(const GemmArgs& a, uint32_t tac
   }
 }
 
+// Brings the 128-byte line holding p into L2 (a hint; no fault for any address of a mapped buffer).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // After an output tile's last shard: Y = bf16(res + S) (out1 / ld1; residual in0 / ldi, nullable)
 // for the calling thread's row, `width` columns from col0, straight from the registers.  Rows past
-// M and columns past N are not written (N % 8 = 0: eight columns are all in or all out).
+// M and columns past N are not written (N % 8 = 0: eight columns are all in or all out).  Y may be
+// the residual itself (a layer stack updates Z in place), so each residual load must precede the
+// stores that could overwrite it: the residual is read 16 columns at a time, two independent
+// loads in flight, before those columns are stored (four would need registers that the 128 sums
+// leave no room for).
 __device__ __forceinline__ void store_sum_row(const GemmArgs& a, int row, int col0, int width,
                                               const float (&s)[128]) {
   if (row >= a.M) return;
   uint16_t* y = static_cast<uint16_t*>(a.out1) + static_cast<int64_t>(row) * a.ld1 + col0;
   const uint16_t* res = static_cast<const uint16_t*>(a.in0);
   const uint16_t* rp = res ? res + static_cast<int64_t>(row) * a.ldi + col0 : nullptr;
+  constexpr int kResGroup = 2;
 #pragma unroll
-  for (int c = 0; c < 128; c += 8) {
-    if (c >= width || col0 + c >= a.N) break;
-    float v[8];
+  for (int c0 = 0; c0 < 128; c0 += 8 * kResGroup) {
+    uint4 w[kResGroup];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = s[c + e];
-    if (rp) {
-      // residual first, then the sum, as in the stand-alone shard-sum: res + S, one rounding
-      const uint4 w = __ldcg(reinterpret_cast<const uint4*>(rp + c));
-      v[0] = bf16lo(w.x) + v[0]; v[1] = bf16hi(w.x) + v[1];
-      v[2] = bf16lo(w.y) + v[2]; v[3] = bf16hi(w.y) + v[3];
-      v[4] = bf16lo(w.z) + v[4]; v[5] = bf16hi(w.z) + v[5];
-      v[6] = bf16lo(w.w) + v[6]; v[7] = bf16hi(w.w) + v[7];
+    for (int q = 0; q < kResGroup; ++q) {
+      const int c = c0 + 8 * q;
+      w[q] = (rp && c < width && col0 + c < a.N) ? __ldcg(reinterpret_cast<const uint4*>(rp + c))
+                                                : make_uint4(0u, 0u, 0u, 0u);
     }
-    store8_bf16(y + c, v);
+#pragma unroll
+    for (int q = 0; q < kResGroup; ++q) {
+      const int c = c0 + 8 * q;
+      if (c >= width || col0 + c >= a.N) continue;
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = s[c + e];
+      if (rp) {
+        // residual first, then the sum, as in the stand-alone shard-sum: res + S, one rounding
+        v[0] = bf16lo(w[q].x) + v[0]; v[1] = bf16hi(w[q].x) + v[1];
+        v[2] = bf16lo(w[q].y) + v[2]; v[3] = bf16hi(w[q].y) + v[3];
+        v[4] = bf16lo(w[q].z) + v[4]; v[5] = bf16hi(w[q].z) + v[5];
+        v[6] = bf16lo(w[q].w) + v[6]; v[7] = bf16hi(w[q].w) + v[7];
+      }
+      store8_bf16(y + c, v);
+    }
   }
 }
 
@@ -1143,6 +1163,14 @@ __global__ void __launch_bounds__(bound_threads<EPI>(), 1)
         const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(cofs);
         for (int g = 0; g < args.batches; ++g, ++k) {
           const uint32_t acc = k & 1u;
+          if (g == args.batches - 1 && args.in0) {
+            // the residual row segment this thread adds at the end, into L2 while the last shard runs
+            const int row = mt * R::kTileM + row_in_tile, col0 = nt * kOutN + (hw > 0 ? kBN / 2 : 0) + cofs;
+            if (row < args.M) {
+              const uint16_t* rp = static_cast<const uint16_t*>(args.in0) + static_cast<int64_t>(row) * args.ldi + col0;
+              for (int c = 0; c < width && col0 + c < args.N; c += 64) prefetch_l2(rp + c);
+            }
+          }
           ok = mbar_wait(bar(kBarTmemFull + acc), (k >> 1) & 1u, abort_flag, err, args.err_site + 4);
           if (!__all_sync(0xFFFFFFFFu, ok)) {
             ok = false;
