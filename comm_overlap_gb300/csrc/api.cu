@@ -93,6 +93,24 @@ bool gated(int act) { return act == DOMINO_ACT_SWIGLU || act == DOMINO_ACT_BILIN
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// CTA pairs a GB300 keeps resident for the GEMMs (152 SMs); the workspace is sized for it, and the
+// launcher skips the fused shard split on a device whose count needs more (a host-only size query
+// cannot ask the device).
+constexpr int kGb300Pairs = 76;
+
+// Scratch of the fused shard-sum's shard split (the launcher in gemm.cuh) for an m x n output of t
+// shards on `units` CTA pairs: a partial slot of 256 x 256 fp32 per shard of each tile of a last
+// round of at most half as many tiles as units (or of every tile when there are fewer tiles than
+// units), then a 32-bit counter per slot; 0 when no round is split.
+size_t fused_split_bytes(int64_t m, int64_t n, int t, int units) {
+  const int64_t tiles = cdiv(m, dm::kTileM) * cdiv(n, dm::kBN);
+  if (tiles == 0 || t < 2) return 0;
+  const int64_t u = tiles < units ? std::min<int64_t>(tiles * t, units) : units;
+  const int64_t rest = tiles % u;
+  if (rest == 0 || u / rest < 2) return 0;
+  return size_t(rest * t) * (size_t(dm::kTileM) * dm::kBN * 4 + 4);
+}
+
 struct Plan {
   int64_t M, h, F, Fi, m, n, a_rows, Ri;
   int t, p, q, act, sched, layers, nslots;
@@ -213,10 +231,11 @@ domino_status make_plan_impl(const domino_cfg* c, int pass, Plan* P) {
       off = align_up(off + size_t(p.M) * p.h * 2);
     }
   }
-  // partial slots of t x m x n fp32; the fused schedule keeps its sums on chip and needs none
+  // partial slots of t x m x n fp32; the fused schedule keeps its sums on chip and needs only the
+  // scratch of the shard split of its last round of tiles (fused_split_bytes)
   if (p.sched == DOMINO_SCHED_FUSED) {
     p.nslots = 1;
-    p.part_slot = 0;
+    p.part_slot = align_up(fused_split_bytes(p.m, p.n, p.t, kGb300Pairs));
   } else {
     p.part_slot = align_up(size_t(p.t) * p.m * p.n * 4);
   }
@@ -405,9 +424,13 @@ domino_status run_gemm(domino_handle H, int kind, int variant, const CUtensorMap
 }
 
 // The fused second linear (or input-gradient GEMM) + shard-sum of one column chunk, the sums held
-// on chip: `res` (nullable) and `Y` are row-major with leading dimension ld.
+// on chip: `res` (nullable) and `Y` are row-major with leading dimension ld; `scratch` (nullable,
+// `scratch_bytes` long) takes the partials of a split last round of tiles (fused_split_bytes).
 domino_status run_fused_reduce(domino_handle H, int kind, int variant, const CUtensorMap& ta, const CUtensorMap& tb,
-                               GemmArgs a, const uint16_t* res, uint16_t* Y, int64_t ld, cudaStream_t st) {
+                               GemmArgs a, const uint16_t* res, uint16_t* Y, int64_t ld, void* scratch,
+                               size_t scratch_bytes, cudaStream_t st) {
+  a.part = scratch;
+  a.part_bytes = int64_t(scratch_bytes);
   a.out1 = Y;
   a.ld1 = ld;
   a.in0 = res;
@@ -520,19 +543,19 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
                             const uint16_t* res_c, uint16_t* Yc, int site, bool fp8 = false, float alpha = 1.0f) {
   const int v_reduce = fp8 ? dm::GV_F8_FWD_REDUCE : dm::GV_FWD_REDUCE;
   const int v_partial = fp8 ? dm::GV_F8_FWD_PARTIAL : dm::GV_FWD_PARTIAL;
-  // column chunk qc with the shard-sum folded into the GEMM
-  auto fused = [&](int qc) {
+  // column chunk qc with the shard-sum folded into the GEMM; `scratch`: P.part_slot bytes
+  auto fused = [&](int qc, void* scratch) {
     GemmArgs a = gemm_args(v_reduce, P.t, P.m, P.n, Kc, site);
     a.a_bmul = 1;
     a.b_row_off = int32_t(qc * P.n);
     a.b_bmul = 1;
     a.alpha = alpha;
     return run_fused_reduce(H, kind, v_reduce, mapH, mapB, a, res_c ? res_c + qc * P.n : nullptr, Yc + qc * P.n,
-                            P.h, S.comp);
+                            P.h, scratch, P.part_slot, S.comp);
   };
   for (int qc = 0; qc < P.q; ++qc) {
     if (P.sched == DOMINO_SCHED_FUSED) {
-      DM_TRY(fused(qc));
+      DM_TRY(fused(qc, parts));
       continue;
     }
     int slot;
@@ -541,9 +564,10 @@ domino_status second_linear(domino_handle H, const Plan& P, const Streams& S, Sl
     if (S.overlap && R.tail && qc == P.q - 1 && !H->skip_reduce) {
       // The call's last reduction would run with nothing left to overlap: the fused kernel adds the
       // shard partials tile by tile inside the GEMM instead (same order, same single rounding, so the
-      // same bits); the slot is taken and handed over only so that the reduction stream waits for
-      // it, and the row events and the join that follow on that stream cover it.
-      DM_TRY(fused(qc));
+      // same bits); the slot's memory takes the partials of a split last round of tiles, and it is
+      // handed over so that the reduction stream waits for it and the row events and the join that
+      // follow on that stream cover it.
+      DM_TRY(fused(qc, part));
       DM_TRY(slot_handoff(H, S, slot));
       DM_TRY(slot_release(H, S, R, slot));
       continue;
@@ -742,7 +766,7 @@ domino_status mlp_chunk_bwd(domino_handle H, const Plan& P, const Streams& S, Sl
       a.b_row_off = int32_t(qc * P.n);
       a.b_bmul = 1;
       DM_TRY(run_fused_reduce(H, DOMINO_K_GEMM_DGRAD_X, dm::GV_BWD_REDUCE, C.mapDZk, C.mapAmn, a, nullptr,
-                              gX_c + qc * P.n, P.h, S.comp));
+                              gX_c + qc * P.n, P.h, C.parts, P.part_slot, S.comp));
       continue;
     }
     int slot;

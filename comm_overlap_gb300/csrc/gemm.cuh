@@ -131,44 +131,65 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, int& g,
   nt = in / gsize;
 }
 
-// Output tile o (0, 1, ...) of a unit of the fused shard-sum: tiles unit, unit + units, ... of the
-// (M, N) space while whole rounds of tiles remain.  A last round that would keep at most half the
-// units busy is split into half-width tiles (256 x 128, half = 0 or 1; otherwise half = -1), two
-// per tile, so that twice as many units share it.  Every element is computed exactly as in a whole
-// tile: the same products over the same K steps, the same shard order.
-__device__ __forceinline__ bool fused_tile(int o, const GemmArgs& a, int unit, int units, int& mt, int& nt,
-                                           int& half) {
-  const int tiles = a.m_tiles * a.n_tiles;
+// Roles of a unit on an output tile of the fused shard-sum.
+enum : int {
+  FT_WHOLE = 0,   // all shards, sums in registers, writes Y
+  FT_HEAD = 1,    // its shards [lo, hi) in registers, then the helpers' partials in shard order, writes Y
+  FT_HELPER = 2,  // stores the partials of its shards [lo, hi) for the head
+};
+struct FusedTile {
+  int mt, nt;  // output tile
+  int lo, hi;  // shards this unit computes, in order
+  int role;
+  int slot0;   // the tile's partial slots: slot0 + g holds shard g (split tiles only)
+};
+
+// Output tile o (0, 1, ...) of a unit of the fused shard-sum.  Units take tiles unit, unit + units,
+// ... of the (M, N) space while whole rounds remain.  With a.split = s > 1, each of the `rest` tiles
+// of the last round is shared by s units: unit u < rest * s takes tile j = u / s, shards
+// [i t / s, (i + 1) t / s) for i = u % s; i = 0 is the tile's head.  Every partial is computed exactly
+// as in a whole tile (the same products over the same K steps), and the head adds them in shard order.
+__device__ __forceinline__ bool fused_tile(int o, const GemmArgs& a, int unit, int units, FusedTile& f) {
+  const int tiles = a.m_tiles * a.n_tiles, t = a.batches;
   const int full = tiles / units, rest = tiles - full * units;
-  const bool split = kPairMma && rest > 0 && 2 * rest <= units;
-  int g, ot;
-  if (o < full || (o == full && !split)) {
-    ot = unit + o * units;
-    half = -1;
+  int ot;
+  if (o < full || (o == full && a.split <= 1)) {
+    ot = o * units + unit;
+    f.lo = 0;
+    f.hi = t;
+    f.role = FT_WHOLE;
+    f.slot0 = 0;
   } else {
-    if (o > full || unit >= 2 * rest) return false;
-    ot = full * units + (unit >> 1);
-    half = unit & 1;
+    if (o > full || unit >= rest * a.split) return false;
+    const int j = unit / a.split, i = unit - j * a.split;
+    ot = full * units + j;
+    f.lo = i * t / a.split;
+    f.hi = (i + 1) * t / a.split;
+    f.role = i == 0 ? FT_HEAD : FT_HELPER;
+    f.slot0 = j * t;
   }
   if (ot >= tiles) return false;
-  decode_tile(ot, a, g, mt, nt);
+  int g;
+  decode_tile(ot, a, g, f.mt, f.nt);
   return true;
 }
 
 // Sub-tile s (0, 1, ...) of a unit's sequence.  Every variant but the fused shard-sum visits tiles
-// unit, unit + units, ... of the (batch, M, N) tile space (half = -1); the fused shard-sum visits its
-// output tiles (fused_tile) and, for each, its `batches` shards in order, so that one unit produces
-// every partial of the tiles it owns.  False past the end of the sequence.
+// unit, unit + units, ... of the (batch, M, N) tile space; the fused shard-sum visits its output
+// tiles (fused_tile) and, for each, its shards in order.  False past the end of the sequence.
 template <int EPI>
-__device__ __forceinline__ bool tile_at(int s, const GemmArgs& a, int unit, int units, int& g, int& mt, int& nt,
-                                        int& half) {
+__device__ __forceinline__ bool tile_at(int s, const GemmArgs& a, int unit, int units, int& g, int& mt, int& nt) {
   if constexpr (EPI == EPI_F32_REDUCE) {
-    const int o = s / a.batches;
-    if (!fused_tile(o, a, unit, units, mt, nt, half)) return false;
-    g = s - o * a.batches;
+    const int t = a.batches, full = (a.m_tiles * a.n_tiles) / units;
+    const int o = s < full * t ? s / t : full;
+    FusedTile f;
+    if (!fused_tile(o, a, unit, units, f)) return false;
+    g = f.lo + (s - o * t);
+    if (g >= f.hi) return false;
+    mt = f.mt;
+    nt = f.nt;
     return true;
   } else {
-    half = -1;
     const int tile = unit + s * units;
     if (tile >= a.batches * a.m_tiles * a.n_tiles) return false;
     decode_tile(tile, a, g, mt, nt);
@@ -781,19 +802,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 // Fused shard-sum (EPI_F32_REDUCE), one sub-tile: shard g's partial of an output tile, for the
-// calling thread's row and `width` accumulator columns from `tacc` (its warp's 128 columns, or 64
-// of a half-width tile).  A unit visits the shards of an output tile consecutively and every warp
+// calling thread's row and its warp's 128 accumulator columns from `tacc`.  A unit visits the shards of an output tile consecutively and every warp
 // takes the same rows and columns of each, so the row's running sum stays in the thread's
 // registers: S = P_0, then S = S + P_g for g = 1, 2, ..., one fp32 add rounded to nearest per
 // shard -- the order and the roundings of the stand-alone shard-sum over stored partials (E4M3
 // operands: each partial is first scaled by alpha and rounded, as the partial store does).  No
 // partial leaves the SM.
 template <bool SCALE>
-__device__ __forceinline__ void sum_partial_regs(const GemmArgs& a, uint32_t tacc, int g, int width,
-                                                 float (&s)[128]) {
+__device__ __forceinline__ void sum_partial_regs(const GemmArgs& a, uint32_t tacc, int g, float (&s)[128]) {
 #pragma unroll
   for (int c = 0; c < 128; c += 16) {
-    if (c >= width) break;
     uint32_t r[16];
     tmem_ld16(tacc + static_cast<uint32_t>(c), r);
     tmem_ld_wait();
@@ -812,14 +830,13 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 }
 
 // After an output tile's last shard: Y = bf16(res + S) (out1 / ld1; residual in0 / ldi, nullable)
-// for the calling thread's row, `width` columns from col0, straight from the registers.  Rows past
+// for the calling thread's row, 128 columns from col0, straight from the registers.  Rows past
 // M and columns past N are not written (N % 8 = 0: eight columns are all in or all out).  Y may be
 // the residual itself (a layer stack updates Z in place), so each residual load must precede the
 // stores that could overwrite it: the residual is read 16 columns at a time, two independent
 // loads in flight, before those columns are stored (four would need registers that the 128 sums
 // leave no room for).
-__device__ __forceinline__ void store_sum_row(const GemmArgs& a, int row, int col0, int width,
-                                              const float (&s)[128]) {
+__device__ __forceinline__ void store_sum_row(const GemmArgs& a, int row, int col0, const float (&s)[128]) {
   if (row >= a.M) return;
   uint16_t* y = static_cast<uint16_t*>(a.out1) + static_cast<int64_t>(row) * a.ld1 + col0;
   const uint16_t* res = static_cast<const uint16_t*>(a.in0);
@@ -831,13 +848,13 @@ __device__ __forceinline__ void store_sum_row(const GemmArgs& a, int row, int co
 #pragma unroll
     for (int q = 0; q < kResGroup; ++q) {
       const int c = c0 + 8 * q;
-      w[q] = (rp && c < width && col0 + c < a.N) ? __ldcg(reinterpret_cast<const uint4*>(rp + c))
+      w[q] = (rp && col0 + c < a.N) ? __ldcg(reinterpret_cast<const uint4*>(rp + c))
                                                 : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int q = 0; q < kResGroup; ++q) {
       const int c = c0 + 8 * q;
-      if (c >= width || col0 + c >= a.N) continue;
+      if (col0 + c >= a.N) continue;
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = s[c + e];
@@ -851,6 +868,141 @@ __device__ __forceinline__ void store_sum_row(const GemmArgs& a, int row, int co
       store8_bf16(y + c, v);
     }
   }
+}
+
+// Split tiles of the fused shard-sum (fused_tile).  A partial slot holds one shard's 256 x 256 fp32
+// partial of one output tile (256 KiB) in thread order: 16-byte piece q (columns 4q .. 4q+3 of the
+// thread's 128) of lane l of epilogue warp w of CTA r at ((r * 8 + w) * 32 + q) * 32 + l.  A warp's
+// piece q is then 512 contiguous bytes, and each warp's block (16 KiB) is contiguous.  The slot's
+// counter reaches kSlotWriters (every epilogue warp of both CTAs) once all pieces are written.
+constexpr int64_t kSlotBytes = 256 * 256 * 4;
+constexpr uint32_t kSlotWriters = 16;
+constexpr uint32_t kSlotWarpBytes = 32 * 32 * 16;
+
+// Split tile: this thread's 128 accumulator columns of one shard into its pieces of the shard's slot
+// (w: its piece 0), scaled and rounded as the partial store does.
+template <bool SCALE>
+__device__ __forceinline__ void store_partial_slot(const GemmArgs& a, uint32_t tacc, uint4* w) {
+#pragma unroll
+  for (int c = 0; c < 128; c += 16) {
+    uint32_t r[16];
+    tmem_ld16(tacc + static_cast<uint32_t>(c), r);
+    tmem_ld_wait();
+    if constexpr (SCALE) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__fmul_rn(__uint_as_float(r[e]), a.alpha));
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      __stcg(w + (c / 4 + q) * 32, make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]));
+  }
+}
+
+// Helper, once the warp's pieces of a slot are written: counts the warp in, with release semantics at
+// GPU scope (the lanes' stores precede lane 0's fence through the warp barrier).
+__device__ __forceinline__ void publish_slot(uint32_t* counter, int lane) {
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Head: bounded wait until every helper warp has written its pieces of a slot (lane 0 polls; then
+// every lane takes its own acquire of the counter).
+__device__ __forceinline__ bool wait_slot(const uint32_t* counter, volatile int* abort_flag, int* err, int site,
+                                          int lane) {
+  bool ok = true;
+  if (lane == 0) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0; ld_acquire_u32(counter) < kSlotWriters; ++it) {
+      if ((it & 63u) == 63u) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > kWaitTimeoutNs) {
+          *abort_flag = 1;
+          atomicCAS(err, 0, site);
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  if (ok) (void)ld_acquire_u32(counter);
+  return ok;
+}
+
+// Untiled bulk copy global -> this CTA's shared memory, completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Head: adds one shard's partial from its slot into the thread's sums, in shard order (g = 0: the
+// sums start from it).  The warp's
+// 16 KiB block is brought into `buf` (shared memory the warp owns) by one bulk copy on the warp's
+// barrier `bar` (phase `ph`), then each lane adds its 32 pieces.  False if the wait gave up.
+template <bool FIRST>
+__device__ __forceinline__ bool add_partial_slot(const uint8_t* block, uint32_t buf, uint32_t bar, uint32_t ph,
+                                                 int lane, volatile int* abort_flag, int* err, int site,
+                                                 float (&s)[128]) {
+  __syncwarp();  // the lanes' reads of the previous block are done
+  if (lane == 0) {
+    fence_proxy_async_smem();    // ... before the copy that overwrites them
+    fence_proxy_async_global();  // the helpers' writes, acquired above, precede the copy's reads
+    mbar_arrive_expect_tx(bar, kSlotWarpBytes);
+    bulk_load(buf, block, kSlotWarpBytes, bar);
+  }
+  const bool ok = mbar_wait(bar, ph, abort_flag, err, site);
+  if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    const uint4 v = ld_shared_v4(buf + static_cast<uint32_t>((q * 32 + lane) * 16));
+    if constexpr (FIRST) {
+      s[4 * q] = __uint_as_float(v.x);
+      s[4 * q + 1] = __uint_as_float(v.y);
+      s[4 * q + 2] = __uint_as_float(v.z);
+      s[4 * q + 3] = __uint_as_float(v.w);
+    } else {
+      s[4 * q] = __fadd_rn(s[4 * q], __uint_as_float(v.x));
+      s[4 * q + 1] = __fadd_rn(s[4 * q + 1], __uint_as_float(v.y));
+      s[4 * q + 2] = __fadd_rn(s[4 * q + 2], __uint_as_float(v.z));
+      s[4 * q + 3] = __fadd_rn(s[4 * q + 3], __uint_as_float(v.w));
+    }
+  }
+  return true;
+}
+
+// Head of a split tile: sums the tile's slots (block: this warp's block in slot 0, the next slots
+// kSlotBytes apart; counters cnt[g]) in shard order through `buf`, the warp's 16 KiB of shared
+// memory, then writes Y for the thread's row.  A function of its own, so that its 128 sums are
+// allocated apart from the whole-tile loop's.  False if a wait gave up.
+static __device__ __noinline__ bool head_sum_slots(const GemmArgs& a, const uint8_t* block, const uint32_t* cnt, uint32_t buf,
+                                            uint32_t bar, int row, int col0, int lane, volatile int* abort_flag,
+                                            int* err) {
+  float s[128];
+  bool ok = wait_slot(cnt, abort_flag, err, a.err_site + 6, lane) &&
+            add_partial_slot<true>(block, buf, bar, 0u, lane, abort_flag, err, a.err_site + 7, s);
+  for (int g = 1; ok && g < a.batches; ++g)
+    ok = wait_slot(cnt + g, abort_flag, err, a.err_site + 6, lane) &&
+         add_partial_slot<false>(block + static_cast<int64_t>(g) * kSlotBytes, buf, bar, static_cast<uint32_t>(g) & 1u,
+                                 lane, abort_flag, err, a.err_site + 7, s);
+  if (ok) store_sum_row(a, row, col0, s);
+  return ok;
 }
 
 // F8: operands are E4M3 codes (kind::f8f6f4), 128 elements per 128-byte K step.
@@ -868,9 +1020,6 @@ __global__ void __launch_bounds__(bound_threads<EPI>(), 1)
   constexpr int kKe = F8 ? 128 : kBK;  // K elements per stage (always 128 bytes per row)
   constexpr uint32_t kIdesc =
       F8 ? idesc_e4m3_f32(R::kTileM, kBN, A_MN, B_MN) : idesc_bf16_f32(R::kTileM, kBN, A_MN, B_MN);
-  // half-width tiles of the fused shard-sum's last round (fused_tile)
-  constexpr uint32_t kIdescHalf =
-      F8 ? idesc_e4m3_f32(R::kTileM, kBN / 2, A_MN, B_MN) : idesc_bf16_f32(R::kTileM, kBN / 2, A_MN, B_MN);
   // barrier indices in the control block
   constexpr int kBarFull = 0, kBarEmpty = S, kBarTmemFull = 2 * S, kBarTmemEmpty = 2 * S + 2,
                 kBarDrain = 2 * S + 4, kBarEpiIn = 2 * S + 5;  // kBarEpiIn: one per epilogue warp
@@ -958,14 +1107,10 @@ __global__ void __launch_bounds__(bound_threads<EPI>(), 1)
       // ---------------- TMA producer (both CTAs of a pair load their own halves)
       uint32_t s = 0, ph = 0, armed = 0, armed_ph = 0, issued = 0;
       bool ok = true;
-      int g, mt, nt, hw;
-      for (int sq = 0; ok && tile_at<EPI>(sq, args, unit, units, g, mt, nt, hw); ++sq) {
+      int g, mt, nt;
+      for (int sq = 0; ok && tile_at<EPI>(sq, args, unit, units, g, mt, nt); ++sq) {
         const int m0 = mt * R::kTileM + static_cast<int>(rank) * kBM + args.a_row_off;
-        // a half-width tile (hw = 0, 1: fused shard-sum only) takes 64 B rows per CTA of the pair;
-        // the 128-row box brings 64 more that its product does not read
-        const int n0 = nt * kOutN + args.b_row_off +
-                       (hw < 0 ? ((PAIR && !kGatedB) ? static_cast<int>(rank) * 128 : 0)
-                               : 128 * hw + static_cast<int>(rank) * 64);
+        const int n0 = nt * kOutN + args.b_row_off + ((PAIR && !kGatedB) ? static_cast<int>(rank) * 128 : 0);
         const int ga = g * args.a_bmul, gb = g * args.b_bmul;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, err, args.err_site + 1)) {
@@ -1048,9 +1193,9 @@ __global__ void __launch_bounds__(bound_threads<EPI>(), 1)
       // ---------------- MMA issuer (the leader CTA of a pair issues for both)
       uint32_t s = 0, ph = 0;
       bool ok = true;
-      int g, mt, nt, hw;
-      for (int it = 0; ok && tile_at<EPI>(it, args, unit, units, g, mt, nt, hw); ++it) {
-        const uint32_t idesc = hw < 0 ? kIdesc : kIdescHalf;
+      int g, mt, nt;
+      for (int it = 0; ok && tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
+        const uint32_t idesc = kIdesc;
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait(bar(kBarTmemEmpty + acc), use ^ 1u, abort_flag, err, args.err_site + 2)) break;
@@ -1148,36 +1293,40 @@ __global__ void __launch_bounds__(bound_threads<EPI>(), 1)
       }
       }
     } else if constexpr (EPI == EPI_F32_REDUCE) {
-      // fused shard-sum: per output tile of the unit (fused_tile), its shards in order, the running
-      // sums of the thread's row in registers; the k-th sub-tile of the unit is in accumulator k % 2
+      // fused shard-sum (fused_tile): per output tile of the unit, its shards in order; the running
+      // sums of the thread's row (its warp's 128 columns) in registers; the unit's k-th sub-tile is in
+      // accumulator k % 2.
       float s[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) s[i] = 0.0f;  // every shard 0 overwrites it
       uint32_t k = 0;
       bool ok = true;
-      int mt, nt, hw;
-      for (int o = 0; ok && fused_tile(o, args, unit, units, mt, nt, hw); ++o) {
-        // a half-width tile's 128 accumulator columns: 64 per warp of the quarter
-        const int width = hw < 0 ? kHalfOut : kHalfOut / 2;
-        const int cofs = half * width;
-        const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(cofs);
-        for (int g = 0; g < args.batches; ++g, ++k) {
-          const uint32_t acc = k & 1u;
+      const int ew = warp - 2;
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * kHalfOut);
+      // whole tiles (fused_tile: role FT_WHOLE), all shards in registers, then Y; the accumulators are
+      // handed back as they are read, so the sum goes out while the next tile's shards run
+      const int tiles = args.m_tiles * args.n_tiles, full = tiles / units, rest = tiles - full * units;
+      const int nwhole = full + ((args.split <= 1 && unit < rest) ? 1 : 0);
+      for (int o = 0; ok && o < nwhole; ++o) {
+        int gb, mt, nt;
+        decode_tile(o * units + unit, args, gb, mt, nt);
+        for (int g = 0; ok && g < args.batches; ++g, ++k) {
           if (g == args.batches - 1 && args.in0) {
             // the residual row segment this thread adds at the end, into L2 while the last shard runs
-            const int row = mt * R::kTileM + row_in_tile, col0 = nt * kOutN + (hw > 0 ? kBN / 2 : 0) + cofs;
+            const int row = mt * R::kTileM + row_in_tile, col0 = nt * kOutN + half * kHalfOut;
             if (row < args.M) {
               const uint16_t* rp = static_cast<const uint16_t*>(args.in0) + static_cast<int64_t>(row) * args.ldi + col0;
-              for (int c = 0; c < width && col0 + c < args.N; c += 64) prefetch_l2(rp + c);
+              for (int c = 0; c < kHalfOut && col0 + c < args.N; c += 64) prefetch_l2(rp + c);
             }
           }
+          const uint32_t acc = k & 1u;
           ok = mbar_wait(bar(kBarTmemFull + acc), (k >> 1) & 1u, abort_flag, err, args.err_site + 4);
           if (!__all_sync(0xFFFFFFFFu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          sum_partial_regs<F8>(args, tq + acc * kBN, g, width, s);
+          sum_partial_regs<F8>(args, tq + acc * kBN, g, s);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -1187,13 +1336,51 @@ __global__ void __launch_bounds__(bound_threads<EPI>(), 1)
               mbar_arrive(bar(kBarTmemEmpty + acc));
           }
         }
-        // the accumulators are handed back; the sum goes out while the next tile's shards run
-        if (ok)
-          store_sum_row(args, mt * R::kTileM + row_in_tile, nt * kOutN + (hw > 0 ? kBN / 2 : 0) + cofs, width, s);
+        if (ok) store_sum_row(args, mt * R::kTileM + row_in_tile, nt * kOutN + half * kHalfOut, s);
+      }
+      // the unit's share of a split tile of the last round: every unit of the tile, its head included,
+      // writes its shards' partials to their slots straight from TMEM; the head then sums all the
+      // tile's slots in shard order through this warp's part of its operand ring, idle by then (all
+      // of the unit's products have completed), and writes Y
+      FusedTile f;
+      if (ok && args.split > 1 && fused_tile(full, args, unit, units, f)) {
+        const int64_t wofs = static_cast<int64_t>(rank * 8 + ew) * kSlotWarpBytes;  // this warp's block in a slot
+        for (int g = f.lo; ok && g < f.hi; ++g, ++k) {
+          const uint32_t acc = k & 1u;
+          ok = mbar_wait(bar(kBarTmemFull + acc), (k >> 1) & 1u, abort_flag, err, args.err_site + 4);
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          store_partial_slot<F8>(args, tq + acc * kBN,
+                                 reinterpret_cast<uint4*>(static_cast<uint8_t*>(args.part) +
+                                                          static_cast<int64_t>(f.slot0 + g) * kSlotBytes + wofs) +
+                                     lane);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (PAIR)
+              mbar_arrive_cluster_relaxed(mapa_shared(bar(kBarTmemEmpty + acc), 0));
+            else
+              mbar_arrive(bar(kBarTmemEmpty + acc));
+          }
+          publish_slot(args.flags + f.slot0 + g, lane);
+        }
+        if (ok && f.role == FT_HEAD) {
+          const int row = f.mt * R::kTileM + row_in_tile, col0 = f.nt * kOutN + half * kHalfOut;
+          if (args.in0 && row < args.M) {
+            const uint16_t* rp = static_cast<const uint16_t*>(args.in0) + static_cast<int64_t>(row) * args.ldi + col0;
+            for (int c = 0; c < kHalfOut && col0 + c < args.N; c += 64) prefetch_l2(rp + c);
+          }
+          ok = head_sum_slots(args, static_cast<const uint8_t*>(args.part) + static_cast<int64_t>(f.slot0) * kSlotBytes + wofs,
+                              args.flags + f.slot0, stage0 + static_cast<uint32_t>(ew) * kSlotWarpBytes,
+                              bar(kBarEpiIn + ew), row, col0, lane, abort_flag, err);
+        }
       }
     } else {
-      int g, mt, nt, hw;
-      for (int it = 0; tile_at<EPI>(it, args, unit, units, g, mt, nt, hw); ++it) {
+      int g, mt, nt;
+      for (int it = 0; tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         const bool ok = mbar_wait(bar(kBarTmemFull + acc), use, abort_flag, err, args.err_site + 4);
@@ -1289,13 +1476,30 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ep
     }
     max_units_of[dev].store(max_units, std::memory_order_release);
   }
-  // units own whole output tiles (with all their shards) in the fused shard-sum, whose tiles of a
-  // last round that keeps at most half the units busy are split in two (fused_tile): a launch with
-  // at most half as many tiles as units gets two units per tile
+  // The fused shard-sum's units own output tiles with all their shards; a launch with fewer tiles
+  // than units gives each tile up to t units (one per group of shards, fused_tile), and so does a
+  // last round of at most half as many tiles as units, when `part` can hold their partial slots.
+  GemmArgs a = args;
   const int64_t tiles = int64_t(EPI == EPI_F32_REDUCE ? 1 : args.batches) * args.m_tiles * args.n_tiles;
   if (tiles == 0 || args.batches == 0) return cudaSuccess;
-  const int64_t want = (EPI == EPI_F32_REDUCE && P && 2 * tiles <= max_units) ? 2 * tiles : tiles;
-  const int units = static_cast<int>(want < max_units ? want : max_units);
+  int units = static_cast<int>(tiles < max_units ? tiles : max_units);
+  a.split = 1;
+  a.flags = nullptr;
+  if constexpr (EPI == EPI_F32_REDUCE) {
+    const int64_t t = args.batches;
+    if (t > 1 && tiles < max_units) units = static_cast<int>(tiles * t < max_units ? tiles * t : max_units);
+    const int64_t rest = tiles % units;
+    const int64_t split = rest > 0 ? (t < units / rest ? t : units / rest) : 1;
+    const int64_t slots = rest * t;
+    if (split >= 2 && a.part && a.part_bytes >= slots * (kSlotBytes + 4)) {
+      a.split = static_cast<int32_t>(split);
+      a.flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.part) + slots * kSlotBytes);
+      e = cudaMemsetAsync(a.flags, 0, static_cast<size_t>(slots) * 4, st);
+      if (e != cudaSuccess) return e;
+    } else if (tiles < units) {
+      units = static_cast<int>(tiles);
+    }
+  }
   if constexpr (P) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1309,9 +1513,9 @@ cudaError_t launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ep
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, ta, tb, em, args);
+    return cudaLaunchKernelEx(&cfg, fn, ta, tb, em, a);
   } else {
-    fn<<<units, block_threads<EPI>(), smem, st>>>(ta, tb, em, args);
+    fn<<<units, block_threads<EPI>(), smem, st>>>(ta, tb, em, a);
     return cudaGetLastError();
   }
 }

@@ -32,8 +32,8 @@ enum GemmEpi : int {
   EPI_F32_ACCUM = 3, // out0 += D (fp32)
   EPI_ACT_BWD = 4,   // in0 = Z: out0 = bf16(D * act'(Z)); out1 = bf16(act(Z))
   EPI_GLU_BWD = 5,   // in0: G at +0, U at +offi: out0: dG at +0, dU at +off0; out1 = bf16(glu(G, U))
-  EPI_F32_REDUCE = 6, // batch g = shard, the shards of a tile in order: S (fp32, out0) = P_0, S += P_g;
-                      //   then out1 = bf16(in0 + S) (residual in0 nullable)
+  EPI_F32_REDUCE = 6, // batch g = shard, the shards of a tile in order: S = P_0, S += P_g (fp32, held
+                      //   on chip); then out1 = bf16(in0 + S) (residual in0 nullable)
   EPI_ACT_F8 = 7,     // FP8 operands: out0 = e4m3(act(alpha D) * out_scale)
   EPI_GLU_F8 = 8,     // FP8 operands, D = [gate | up]: out0 = e4m3(glu(alpha gate, alpha up) * out_scale)
 };
@@ -77,6 +77,13 @@ struct GemmArgs {
   int64_t ld1, bs1, off1;
   const void* in0;
   int64_t ldi, bsi, offi;
+  // fused shard-sum only: scratch for the shard split of the last round of output tiles (partial
+  // slots of 256 KiB, then one 32-bit counter per slot), `part_bytes` long (0: no split).  The
+  // launcher sets `split` (units sharing each tile of that round, 1 = none) and `flags`.
+  void* part;
+  int64_t part_bytes;
+  uint32_t* flags;
+  int32_t split;
 };
 
 int gemm_out_tile_n(int variant);  // 128 for GV_FWD_GLU, else 256
@@ -88,8 +95,6 @@ int gemm_out_tile_n(int variant);  // 128 for GV_FWD_GLU, else 256
 //  activation-backward variants (GV_BWD_ACT, GV_BWD_GLU), all bf16 with 64-byte swizzle and
 //    (F_i, M, shards) extents: m[0] saved Z or G (read), m[1] saved U (read, gated),
 //    m[2] dZ or dG (written), m[3] dU (written, gated), m[4] recomputed H (written).
-//  fused shard-sum variants (GV_FWD_REDUCE, GV_BWD_REDUCE): m[0] = fp32 sum S (N, M, 1), 128-byte
-//    swizzle (TMA stores and reduce-adds).
 //  Other variants ignore the maps.
 struct EpiMaps {
   CUtensorMap m[5];

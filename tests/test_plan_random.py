@@ -56,6 +56,17 @@ PLAN = re.compile(r"workspace=(\d+) B \[h@(\d+) ln@(\d+) dz@(\d+) hb@(\d+) gn@(\
                   r"partials@(\d+)\]")
 
 
+def fused_split_bytes(m, n, t, units=76):
+    tiles = -(-m // 256) * -(-n // 256)
+    if tiles == 0 or t < 2:
+        return 0
+    u = min(tiles * t, units) if tiles < units else units
+    rest = tiles % u
+    if rest == 0 or u // rest < 2:
+        return 0
+    return rest * t * (256 * 256 * 4 + 4)
+
+
 def buffers(c, pass_, off, total):
     """(name, offset, size) of each buffer the pass uses, from the documented layout."""
     M, h, F, t, p, q = c["M"], c["h"], c["ffn"], c["t"], c["p"], c["q"]
@@ -63,9 +74,12 @@ def buffers(c, pass_, off, total):
     gated = c["act"] in (3, 4)
     a_rows = 2 * F if gated else F
     fused = c["sched"] == 3
-    # the fused schedule keeps its shard sums on chip: no partial slots
-    slots = 0 if fused else (1 if p * q < 2 else 2)
-    part = t * m * n * 4
+    # the fused schedule keeps its shard sums on chip; it needs only the scratch of the shard split
+    # of its last round of tiles (partial slots for the 76 CTA pairs of a GB300, then counters)
+    if fused:
+        slots, part = 1, fused_split_bytes(m, n, t)
+    else:
+        slots, part = (1 if p * q < 2 else 2), t * m * n * 4
     out = []
     if pass_ in (0, 2):
         out.append(("h", off["h"], m * F * 2))
