@@ -91,9 +91,12 @@ typedef enum {
  *          and adds each, as it leaves the tensor-core accumulator, into an fp32 running sum
  *          held in the epilogue threads' registers (P_0, then + P_1, ..., one rounding per
  *          add); after the last shard the sum (plus the residual) is rounded once to bf16.
- *          No partial is written to memory.  Same arithmetic and order as the other
- *          schedules; everything runs on the caller's stream; the workspace holds no partial
- *          slots. */
+ *          A last round of output tiles that would keep at most half the GPU busy is shared
+ *          by several CTA pairs per tile, each computing a group of shards whose partials it
+ *          writes to the workspace; the tile's first pair adds them all in shard order.  Same
+ *          arithmetic and order as the other schedules; everything runs on the caller's
+ *          stream; the workspace holds no partial slots, only those of that last round
+ *          (256 KiB per shard of each of its tiles). */
 typedef enum {
   DOMINO_SCHED_SERIAL = 0,
   DOMINO_SCHED_INTRA = 1,
