@@ -1,11 +1,13 @@
 """GPU parity of the fused schedule (DOMINO_SCHED_FUSED): the second linear and the input-gradient
-GEMM reduce their shard partials tile by tile inside one kernel (fp32 adds at L2 in shard order).
+GEMM reduce their shard partials tile by tile inside one kernel (fp32 running sums in shard order;
+a short last round of tiles is shared by several CTA pairs per tile through partial slots).
 
 * Integer-valued inputs: Y and gX equal the oracle's exact result rounded once to bf16.
 * Real-valued inputs: within the parity tolerance of the double-precision oracle, and bit-identical
   to the two-stream schedule, which sums the same fp32 partials in the same order.
 * Ragged tails in every dimension, t = 1 (the only shard is the last), column and row splits, the
-  residual of the layer stack, the stack backward, and the full-size forward+backward workload.
+  residual of the layer stack, the stack backward, a whole round followed by a split last round, and
+  the full-size forward+backward workload.
 """
 
 import numpy as np
@@ -101,7 +103,8 @@ def test_fused_matches_oracle_and_stream_schedule(lib, shape, act):
 
 
 def test_fused_repeated_calls_identical(lib):
-    """The sum buffer is fully rewritten by every call (shard 0 stores): no state leaks between calls."""
+    """The partial slots and their counters of the split tiles are rewritten and reset by every call:
+    no state leaks between calls."""
     M, h, Fi, t, p, q = 512, 256, 128, 4, 2, 1
     X, A, B, gY = inputs(M, h, Fi, t, synth.ACT_GELU, 52, integer=False)
     first = fwd_bwd(lib, M, h, Fi, t, p, q, synth.ACT_GELU, dm.SCHED_FUSED, X, A, B, gY)
@@ -110,6 +113,22 @@ def test_fused_repeated_calls_identical(lib):
     again = fwd_bwd(lib, M, h, Fi, t, p, q, synth.ACT_GELU, dm.SCHED_FUSED, X, A, B, gY)
     for a, b in zip(first[:2], again[:2]):
         assert np.array_equal(host_bits(a), host_bits(b))
+
+
+def test_fused_split_last_round(lib):
+    """80 output tiles on a GB300's 76 CTA pairs: one whole round, then 4 tiles shared by 8 pairs each
+    (one shard per pair, the partials added by each tile's head).  Bit-identical to the two-stream
+    schedule, and the rows of the split tiles (rows 4096 - 5119, columns 768 - 1023 in the tile
+    order) against the oracle."""
+    M, h, Fi, t, p, q = 5120, 1024, 128, 8, 1, 1
+    X, A, B, gY = inputs(M, h, Fi, t, synth.ACT_GELU, 56, integer=False)
+    Y, gX, _, _ = fwd_bwd(lib, M, h, Fi, t, p, q, synth.ACT_GELU, dm.SCHED_FUSED, X, A, B, gY)
+    Y2, gX2, _, _ = fwd_bwd(lib, M, h, Fi, t, p, q, synth.ACT_GELU, dm.SCHED_INTRA, X, A, B, gY)
+    assert np.array_equal(host_bits(Y), host_bits(Y2)), "Y differs from the two-stream schedule"
+    assert np.array_equal(host_bits(gX), host_bits(gX2)), "gX differs from the two-stream schedule"
+    rows = np.unique(np.array([4096, 4097, 4351, 4352, 4607, 4863, 5118, 5119] + list(synth.sample_indices(M, 4, 57))))
+    Yr = host_f64(Y)[rows]
+    assert_tol(Yr, oracle.mlp_fwd(X, A, B, t, synth.ACT_GELU, rows=rows), "Y rows of the split tiles")
 
 
 def test_fused_stack_forward_and_backward(lib):
