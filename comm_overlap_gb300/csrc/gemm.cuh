@@ -197,6 +197,24 @@ __device__ __forceinline__ bool tile_at(int s, const GemmArgs& a, int unit, int 
   }
 }
 
+// Number of sub-tiles in a unit's sequence (tile_at), in closed form: the MMA issuer needs only the
+// count, and the integer divisions of the tile order, on its thread between two tiles, would keep the
+// tensor core waiting.
+template <int EPI>
+__device__ __forceinline__ int unit_subtiles(const GemmArgs& a, int unit, int units) {
+  if constexpr (EPI == EPI_F32_REDUCE) {
+    const int t = a.batches, tiles = a.m_tiles * a.n_tiles;
+    const int full = tiles / units, rest = tiles - full * units;
+    if (a.split <= 1) return (full + (unit < rest ? 1 : 0)) * t;
+    if (unit >= rest * a.split) return full * t;
+    const int i = unit % a.split;
+    return full * t + (i + 1) * t / a.split - i * t / a.split;
+  } else {
+    const int total = a.batches * a.m_tiles * a.n_tiles;
+    return unit < total ? (total - 1 - unit) / units + 1 : 0;
+  }
+}
+
 // Bounded wait that ignores the abort flag (used while draining after an abort).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -1193,8 +1211,8 @@ __global__ void __launch_bounds__(bound_threads<EPI>(), 1)
       // ---------------- MMA issuer (the leader CTA of a pair issues for both)
       uint32_t s = 0, ph = 0;
       bool ok = true;
-      int g, mt, nt;
-      for (int it = 0; ok && tile_at<EPI>(it, args, unit, units, g, mt, nt); ++it) {
+      const int nsub = unit_subtiles<EPI>(args, unit, units);
+      for (int it = 0; ok && it < nsub; ++it) {
         const uint32_t idesc = kIdesc;
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;

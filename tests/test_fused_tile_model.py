@@ -146,3 +146,36 @@ def test_host_workspace_matches_the_launcher_on_76_pairs():
                 assert split == 1
             # with exactly the planned bytes the launcher splits whenever it would with unlimited scratch
             assert launch(tiles, t, 76, 1 << 40)[1] == split
+
+
+def unit_subtiles(tiles, t, unit, units, split):
+    """gemm.cuh unit_subtiles for the fused shard-sum (the MMA issuer's count)."""
+    full, rest = divmod(tiles, units)
+    if split <= 1:
+        return (full + (1 if unit < rest else 0)) * t
+    if unit >= rest * split:
+        return full * t
+    i = unit % split
+    return full * t + (i + 1) * t // split - i * t // split
+
+
+@pytest.mark.parametrize("max_units", [1, 3, 38, 76])
+def test_mma_count_matches_the_sequence(max_units):
+    for tiles in range(1, 300):
+        for t in (1, 2, 3, 8):
+            units, split = launch(tiles, t, max_units, part_bytes=1 << 40)
+            for u in range(units):
+                k = 0
+                while tile_at(k, tiles, t, u, units, split) is not None:
+                    k += 1
+                assert unit_subtiles(tiles, t, u, units, split) == k, (tiles, t, u)
+
+
+def test_mma_count_of_the_other_variants():
+    # every other variant: tiles unit, unit + units, ... of batches x m_tiles x n_tiles
+    for total in range(0, 500):
+        for units in (1, 7, 76):
+            for u in range(units):
+                want = len(range(u, total, units))
+                got = (total - 1 - u) // units + 1 if u < total else 0
+                assert got == want
