@@ -109,50 +109,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
-// L2 eviction policy that keeps the accessed lines resident in preference to others.
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-// tma_store_3d with an L2 cache policy for the written lines.
-__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
-                                                  int32_t c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
-// Element-wise add of a shared-memory box into global memory, performed by the TMA unit at L2
-// (the tensor map's element type, here fp32), with an L2 cache policy for the lines it updates.
-__device__ __forceinline__ void tma_reduce_add_3d_hint(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
-                                                       int32_t c2, uint64_t policy) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], "
-      "%5;" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
-// Drops the 128-byte L2 line at p (128-byte aligned) without writing it back; its contents become
-// undefined.  For scratch data that no one reads again.
-__device__ __forceinline__ void discard_l2_line(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
-// Element-wise add of a shared-memory box into global memory, performed by the TMA unit at L2
-// (the tensor map's element type, here fp32).  Same box, swizzle and clipping as tma_store_3d.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
-                                                  int32_t c2) {
-  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
                                              int32_t c2, int32_t c3) {
   asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
@@ -174,20 +130,6 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// bulk_wait_group<n> for a run-time n in [0, 7].
-__device__ __forceinline__ void bulk_wait_group_upto(int n) {
-  switch (n) {
-    case 0: bulk_wait_group<0>(); break;
-    case 1: bulk_wait_group<1>(); break;
-    case 2: bulk_wait_group<2>(); break;
-    case 3: bulk_wait_group<3>(); break;
-    case 4: bulk_wait_group<4>(); break;
-    case 5: bulk_wait_group<5>(); break;
-    case 6: bulk_wait_group<6>(); break;
-    default: bulk_wait_group<7>(); break;
-  }
 }
 
 // Wait until every committed bulk group has completed.
