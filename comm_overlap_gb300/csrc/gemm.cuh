@@ -134,7 +134,8 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmArgs& a, int& g,
 // Roles of a unit on an output tile of the fused shard-sum.
 enum : int {
   FT_WHOLE = 0,   // all shards, sums in registers, writes Y
-  FT_HEAD = 1,    // its shards [lo, hi) in registers, then the helpers' partials in shard order, writes Y
+  FT_HEAD = 1,    // stores the partials of its shards [lo, hi), then adds all the tile's slots in
+                  // shard order and writes Y
   FT_HELPER = 2,  // stores the partials of its shards [lo, hi) for the head
 };
 struct FusedTile {
